@@ -1,0 +1,110 @@
+"""Seeded synthetic inputs for kernelized linear attention.
+
+This module is shared by the tests, the benchmark and the smoke check; it
+feeds both the CUDA library and the CPU oracle.  It draws random tensors and
+nothing else: it holds none of the method's arithmetic.
+
+The workloads below are the shapes and value distributions the library is
+measured and checked on.  No dataset is involved; every tensor is drawn from a
+seeded ``torch.Generator`` on the requested device.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    T: int
+    q_heads: int
+    kv_heads: int
+    Dk: int
+    Dv: int
+    dtype: torch.dtype
+    feature_map: str          # "elu_plus_one" | "relu" | "none"
+    use_normalizer: bool
+    eps: float
+    scale: float              # 0.0 -> 1/sqrt(Dk) (ONNX convention)
+    rule: str                 # "linear" | "gated"
+    qk_std: float = 1.0       # q, k ~ N(0, qk_std^2)
+    v_std: float = 1.0
+    k_l2_normalize: bool = False
+    decay_mu: float = 4.0     # gated: g = log(sigmoid(x)), x ~ N(decay_mu, 1)
+    seed: int = 0
+
+
+TINY = Workload("tiny_B1_H2_T64_D16_f32", 1, 64, 2, 2, 16, 16, torch.float32,
+                "elu_plus_one", True, 1e-6, 1.0, "linear", qk_std=0.5, seed=42)
+PREFILL_2K = Workload("causal_prefill_B4_H8_T2048_D64_bf16", 4, 2048, 8, 8, 64, 64,
+                      torch.bfloat16, "elu_plus_one", True, 1e-6, 1.0, "linear", qk_std=0.5)
+LONG_8K = Workload("long_prefill_B8_H16_T8192_D128_bf16_relu", 8, 8192, 16, 16, 128, 128,
+                   torch.bfloat16, "relu", True, 1e-6, 1.0, "linear")
+LONG_8K_UNNORM = dataclasses.replace(LONG_8K, name=LONG_8K.name + "_unnormalized",
+                                     use_normalizer=False)
+DECODE = Workload("decode_B256_H32_D128_prefill4096", 256, 4096, 32, 32, 128, 128,
+                  torch.bfloat16, "elu_plus_one", True, 1e-6, 1.0, "linear")
+DECODE_STEPS = 1024
+ONNX_LINEAR = Workload("onnx_linear_gqa_B2_T32768_Hq32_Hkv8_D128_bf16", 2, 32768, 32, 8,
+                       128, 128, torch.bfloat16, "none", False, 0.0, 1.0 / math.sqrt(128),
+                       "linear", k_l2_normalize=True)
+ONNX_GATED = dataclasses.replace(ONNX_LINEAR, name="onnx_gated_gqa_B2_T32768_Hq32_Hkv8_D128_bf16",
+                                 rule="gated")
+
+ALL = [TINY, PREFILL_2K, LONG_8K, LONG_8K_UNNORM, DECODE, ONNX_LINEAR, ONNX_GATED]
+
+
+def generator(seed: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def normal(shape, gen: torch.Generator, std=1.0, mean=0.0, dtype=torch.float32, device="cpu"):
+    """N(mean, std^2) drawn in fp32 on ``device``, then rounded to ``dtype``."""
+    x = torch.randn(tuple(shape), generator=gen, device=device, dtype=torch.float32)
+    if std != 1.0:
+        x = x * std
+    if mean != 0.0:
+        x = x + mean
+    return x.to(dtype)
+
+
+def make_qkv(w: Workload, device="cpu", T=None, B=None, seed=None):
+    """q (B,T,Hq,Dk), k (B,T,Hkv,Dk), v (B,T,Hkv,Dv) and, for the gated rule,
+    decay (B,T,Hkv) -- contiguous, the packed [B,T,H*D] memory of the ONNX op.
+
+    Draw order q, k, v, decay.  Keys are L2-normalised over Dk in fp32 before
+    rounding when the workload asks for it (the ONNX page recommends
+    normalised keys); the log-decay is log(sigmoid(x)), x ~ N(decay_mu, 1)."""
+    T = w.T if T is None else T
+    B = w.B if B is None else B
+    g = generator(w.seed if seed is None else seed, device)
+    q = normal((B, T, w.q_heads, w.Dk), g, w.qk_std, dtype=w.dtype, device=device)
+    if w.k_l2_normalize:
+        k32 = normal((B, T, w.kv_heads, w.Dk), g, w.qk_std, dtype=torch.float32, device=device)
+        k = (k32 / k32.norm(dim=-1, keepdim=True).clamp_min(1e-12)).to(w.dtype)
+    else:
+        k = normal((B, T, w.kv_heads, w.Dk), g, w.qk_std, dtype=w.dtype, device=device)
+    v = normal((B, T, w.kv_heads, w.Dv), g, w.v_std, dtype=w.dtype, device=device)
+    decay = None
+    if w.rule == "gated":
+        x = normal((B, T, w.kv_heads), g, 1.0, mean=w.decay_mu, dtype=torch.float32,
+                   device=device)
+        decay = torch.nn.functional.logsigmoid(x).to(w.dtype)
+    return q, k, v, decay
+
+
+def tiny_paper_inputs(seed=42, n=32, d=16):
+    """The n=32, d=16 draw of the 'Causal Linear Attention' notebook, replayed
+    with numpy's legacy seeded generator (order Q, K, V; Q and K times 0.5)."""
+    import numpy as np
+    np.random.seed(seed)
+    Q = np.random.randn(n, d).astype(np.float32) * 0.5
+    K = np.random.randn(n, d).astype(np.float32) * 0.5
+    V = np.random.randn(n, d).astype(np.float32)
+    return Q, K, V
