@@ -1,0 +1,410 @@
+"""Benchmark: causal prefill tokens/s (+ % of the HBM roofline) and the decode
+step (us/token, state GB/s) of the kernelized linear attention library.
+
+One JSON line on stdout (rank 0).  Default workload: causal prefill
+B=4, H=8, T=2048, Dk=Dv=64, bf16 q/k/v, fp32 state, elu+1, normalized,
+eps 1e-6; plus the streaming-decode workload (B=256, H=32, D=128, state from a
+4096-token prefill, 1024 single-token steps) as a secondary object.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload on its own
+GPU (independent sequences, no collective on the data path): weak scaling.
+``--impl reference`` times the CPU oracle (the only reference there is) on
+the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import linattn_inputs as inputs  # noqa: E402
+
+METRIC = "causal prefill tokens/s and % roofline; decode step µs/token and state-GB/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (weak scaling: independent replicas)
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# workload definitions
+
+def prefill_kwargs(w):
+    return dict(q_heads=w.q_heads, kv_heads=w.kv_heads, feature_map=w.feature_map,
+                use_normalizer=w.use_normalizer, epsilon=w.eps, scale=w.scale, update_rule=w.rule)
+
+
+def prefill_alg_bytes(w, T=None):
+    T = w.T if T is None else T
+    esz = 2 if w.dtype == torch.bfloat16 else 4
+    qy = w.B * T * w.q_heads * (w.Dk + w.Dv) * esz
+    kv = w.B * T * w.kv_heads * (w.Dk + w.Dv) * esz
+    dec = w.B * T * w.kv_heads * esz if w.rule == "gated" else 0
+    return qy + kv + dec
+
+
+def decode_alg_bytes(w):
+    esz = 2
+    state = w.B * w.kv_heads * (w.Dk * w.Dv + (w.Dk if w.use_normalizer else 0)) * 4
+    tok = w.B * (w.q_heads * (w.Dk + w.Dv) + w.kv_heads * (w.Dk + w.Dv)) * esz
+    return 2 * state + tok, 2 * state
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+
+def time_prefill(la, w, steps, warmup, stream):
+    """Device time of `steps` causal prefill calls on rotating input sets."""
+    set_bytes = prefill_alg_bytes(w)
+    nsets = max(2, -(-3 * L2_BYTES // set_bytes))  # > 3x L2 in flight: every step reads cold data
+    sets = []
+    for s in range(nsets):
+        q, k, v, d = inputs.make_qkv(w, device="cuda", seed=w.seed + s)
+        y = torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype, device="cuda")
+        sets.append((q, k, v, d, y))
+    kw = prefill_kwargs(w)
+    ws = torch.empty(max(1, la.la_workspace_bytes(la.make_params(
+        batch=w.B, seq_len=w.T, q_heads=w.q_heads, kv_heads=w.kv_heads, key_dim=w.Dk, value_dim=w.Dv,
+        io_dtype=w.dtype, feature_map=w.feature_map, use_normalizer=w.use_normalizer, epsilon=w.eps,
+        scale=w.scale, update_rule=w.rule), True)), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        q, k, v, d, y = sets[i % nsets]
+        la.la_forward_causal(q, k, v, decay=d, out=y, workspace=ws, stream=stream, **kw)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    torch.cuda.synchronize()
+    n0 = la.la_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            step(warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    launches = la.la_launch_count() - n0
+    ms = ev0.elapsed_time(ev1) / steps
+    return ms, launches, nsets, sets
+
+
+def time_prefill_e2e(la, w, steps, warmup, stream):
+    """Same call with host-resident inputs: pinned host -> device copies of q, k,
+    v, the call, and the device -> host copy of y, all inside the timed region."""
+    q, k, v, d = inputs.make_qkv(w, device="cpu", seed=w.seed)
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    hd = d.pin_memory() if d is not None else None
+    hy = torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (q, k, v))
+    dd = torch.empty_like(d, device="cuda") if d is not None else None
+    dy = torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype, device="cuda")
+    kw = prefill_kwargs(w)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        if dd is not None:
+            dd.copy_(hd, non_blocking=True)
+        la.la_forward_causal(dq, dk, dv, decay=dd, out=dy, stream=stream, **kw)
+        hy.copy_(dy, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hd,) if hd is not None else ()))
+    return ev0.elapsed_time(ev1) / steps, h2d, hy.numel() * hy.element_size()
+
+
+def time_decode(la, w, n_steps, warmup, stream):
+    """us per decode step of the streaming-decode workload."""
+    kw = prefill_kwargs(w)
+    # state from a causal prefill over the workload's prompt length (untimed)
+    q, k, v, _ = inputs.make_qkv(w, device="cuda", seed=w.seed)
+    _, (S, Z) = la.la_forward_causal(q, k, v, return_state=True, stream=stream, **kw)
+    del q, k, v
+    g = inputs.generator(1000, "cuda")
+    total = warmup + n_steps
+    tq = inputs.normal((total, w.B, 1, w.q_heads, w.Dk), g, dtype=w.dtype, device="cuda")
+    tk = inputs.normal((total, w.B, 1, w.kv_heads, w.Dk), g, dtype=w.dtype, device="cuda")
+    tv = inputs.normal((total, w.B, 1, w.kv_heads, w.Dv), g, dtype=w.dtype, device="cuda")
+    y = torch.empty(w.B, 1, w.q_heads, w.Dv, dtype=w.dtype, device="cuda")
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            la.la_decode_step(tq[i], tk[i], tv[i], S, Z, out=y, stream=stream, **kw)
+    torch.cuda.synchronize()
+    n0 = la.la_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(warmup, total):
+            la.la_decode_step(tq[i], tk[i], tv[i], S, Z, out=y, stream=stream, **kw)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) * 1e3 / n_steps, la.la_launch_count() - n0
+
+
+def cpu_baseline(w, budget_s=8.0):
+    """The oracle as it stands on the host cores, on whole (batch, head)
+    streams of the workload, repeated until the time budget is used."""
+    import oracle
+    q, k, v, d = inputs.make_qkv(w, device="cpu", seed=w.seed)
+    cores = os.cpu_count() or 1
+    n_streams = w.B * w.kv_heads
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.causal(q, k, v, q_heads=w.q_heads, kv_heads=w.kv_heads, feature_map=w.feature_map,
+                      use_normalizer=w.use_normalizer, eps=w.eps, scale=w.scale, rule=w.rule,
+                      decay=d, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    tok_s = reps * w.B * w.T / el
+    return {"value": tok_s, "unit": "tokens/s", "cores": min(cores, n_streams), "kind": "oracle",
+            "sample": f"the full workload ({w.B}x{w.T} tokens, {w.q_heads} heads) run {reps} time(s), "
+                      f"fp64 recurrence, one thread per (batch, kv-head) stream"}
+
+
+def run_gpu(args):
+    import kernelized_linear_attention_02_gb300 as la
+    world, rank, local = dist_init()
+    la.lib()
+    w = inputs.PREFILL_2K
+    wd = inputs.DECODE
+    pk = peaks()
+    stream = torch.cuda.Stream()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms, launches, nsets, _ = time_prefill(la, w, args.steps, args.warmup, stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(ms, world)
+    clocks = clk.summary()
+    tokens = w.B * w.T
+    value = tokens * world / (ms * 1e-3)
+    alg = prefill_alg_bytes(w)
+    achieved = alg / (ms * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = time_prefill_e2e(la, w, args.steps, args.warmup, stream)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+
+    dec = None
+    if not args.skip_decode:
+        with ClockSampler(local) as dclk:
+            us, dlaunch = time_decode(la, wd, args.decode_steps, args.warmup, stream)
+        us = max_over_ranks(us, world)
+        dbytes, sbytes = decode_alg_bytes(wd)
+        dec = {"workload": wd.name, "us_per_step": us, "us_per_token": us / wd.B,
+               "state_GBps": sbytes / (us * 1e-6) / 1e9, "alg_GBps": dbytes / (us * 1e-6) / 1e9,
+               "roofline_frac": dbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"], "steps": args.decode_steps,
+               "gpu_launches": dlaunch, "clocks": dclk.summary()}
+
+    if rank != 0:
+        return
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.q_heads, "Dk": w.Dk, "Dv": w.Dv,
+                   "feature_map": w.feature_map, "use_normalizer": w.use_normalizer, "eps": w.eps,
+                   "state_dtype": "fp32", "parallelism": f"{world} independent replica(s)",
+                   "l2": f"inputs rotate over {nsets} sets ({nsets * alg / 1e6:.0f} MB > L2)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                     "peak_source": pk["source"], "alg_bytes_per_launch": alg},
+        "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "decode": dec,
+    }
+    if world == 1 and not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = inputs.PREFILL_2K
+    import oracle
+    q, k, v, d = inputs.make_qkv(w, device="cpu", seed=w.seed)
+    cores = os.cpu_count() or 1
+
+    def step():
+        oracle.causal(q, k, v, q_heads=w.q_heads, kv_heads=w.kv_heads, feature_map=w.feature_map,
+                      use_normalizer=w.use_normalizer, eps=w.eps, scale=w.scale, rule=w.rule,
+                      decay=d, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = (time.perf_counter() - t0) / args.steps
+    value = w.B * w.T / el
+    sample = f"the full workload ({w.B}x{w.T} tokens, {w.q_heads} heads) per step, fp64 oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.q_heads, "Dk": w.Dk, "Dv": w.Dv},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, w.B * w.kv_heads),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=1024)
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

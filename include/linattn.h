@@ -1,0 +1,155 @@
+/*
+ * linattn.h -- C ABI of the GB300 (sm_103a) kernelized linear attention library.
+ *
+ * The operation (page titles and sections of the sources it follows):
+ *
+ *   "[Feature] LinearAttention layer for Keras", Mathematical definition:
+ *     non-causal  S = sum_j phi(K_j)^T V_j,  Z = sum_j phi(K_j),
+ *                 Y_i = phi(Q_i) S / (phi(Q_i) Z + eps)
+ *     causal      S_t = S_{t-1} + phi(K_t)^T V_t,  Z_t = Z_{t-1} + phi(K_t),
+ *                 Y_t = phi(Q_t) S_t / (phi(Q_t) Z_t + eps)   (token t included)
+ *     use_normalizer = 0:  Y = phi(Q) S.
+ *   same page, Feature maps:  elu_plus_one  phi(x) = elu(x) + 1 (alpha 1);
+ *                              relu          phi(x) = max(x, 0) + eps.
+ *   same page, Streaming State: key_value_state S (B, H, Dk, Dv) and
+ *     key_state Z (B, H, Dk), kept in the accumulator dtype (float32); chunked
+ *     calls that carry the state equal one full-sequence call.
+ *   ONNX-light "LinearAttention" operator: packed [B, T, H*D] activations,
+ *     grouped KV heads (query head h reads kv head h / (Hq/Hkv)), update rules
+ *       linear  S_t = S_{t-1} + k_t (x) v_t
+ *       gated   S_t = exp(g_t) S_{t-1} + k_t (x) v_t   (g_t per kv head, log space)
+ *     with o_t = scale * q_t^T S_t and scale 0.0 meaning 1/sqrt(d_k).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor arguments are DEVICE pointers to contiguous row-major memory
+ *    owned by the caller.  The library never allocates or frees device
+ *    memory; scratch comes from the caller's workspace.
+ *  - Activations: q (B, T, Hq, Dk), k (B, T, Hkv, Dk), v (B, T, Hkv, Dv),
+ *    y (B, T, Hq, Dv) -- the same bytes as the ONNX packed (B, T, H*D).
+ *    decay (B, T, Hkv) in the io dtype, log space.
+ *  - State: S (B, Hkv, Dk, Dv) float32, Z (B, Hkv, Dk) float32.  S[b,h,i,j]
+ *    accumulates phi(k)_i * v_j.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and is asynchronous; the call returns after enqueueing.
+ *  - On any status other than LA_OK nothing has been enqueued, except for
+ *    LA_ERR_CUDA, which reports a failed launch (cudaGetLastError) and may
+ *    follow partially enqueued work.  la_last_error() gives a one-line
+ *    description of the last failure on the calling host thread.
+ *  - Arithmetic: phi in float32; products on tensor cores (bf16 inputs) or
+ *    CUDA cores (float32 inputs); S and Z accumulate in float32; y is
+ *    rounded to out_dtype with round-to-nearest-even.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LINATTN_ABI_VERSION 1
+
+typedef enum la_status {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,  /* bad size, null pointer, bad enum, Hq % Hkv != 0 ... */
+    LA_ERR_UNSUPPORTED = 2,  /* a valid combination the library does not implement */
+    LA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than la_workspace_bytes() */
+    LA_ERR_CUDA = 4          /* a CUDA runtime error while enqueueing */
+} la_status;
+
+typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+typedef enum la_feature_map {
+    LA_FMAP_NONE = 0,          /* identity (ONNX rules) */
+    LA_FMAP_ELU_PLUS_ONE = 1,  /* elu(x) + 1 */
+    LA_FMAP_RELU_EPS = 2       /* max(x, 0) + epsilon */
+} la_feature_map;
+
+typedef enum la_update_rule { LA_RULE_LINEAR = 0, LA_RULE_GATED = 1 } la_update_rule;
+
+/* The CUDA stream type without the CUDA headers: identical to cudaStream_t. */
+typedef struct CUstream_st* la_stream_t;
+
+/* Problem description (the Keras constructor arguments and the ONNX
+ * attributes).  Plain data; the library keeps no pointer to it. */
+typedef struct la_params {
+    int64_t batch;           /* B >= 1 */
+    int64_t seq_len;         /* T >= 0; must be 1 for la_decode_step */
+    int32_t q_heads;         /* Hq >= 1 */
+    int32_t kv_heads;        /* Hkv >= 1, Hq % Hkv == 0 */
+    int32_t key_dim;         /* Dk, 1..128 */
+    int32_t value_dim;       /* Dv, 1..128 */
+    int32_t io_dtype;        /* la_dtype of q, k, v and decay */
+    int32_t out_dtype;       /* la_dtype of y */
+    int32_t feature_map;     /* la_feature_map, applied to q and k */
+    int32_t use_normalizer;  /* 1: divide by phi(q).Z + eps; 0: no Z at all */
+    float epsilon;           /* normalization_epsilon >= 0 (also the relu offset) */
+    float scale;             /* output scale; 0.0 means 1/sqrt(Dk) (ONNX default) */
+    int32_t update_rule;     /* la_update_rule */
+    int32_t reserved;        /* must be 0 */
+} la_params;
+
+/* Zero-filled initial state, Keras get_initial_state / ONNX default
+ * past_state ("Streaming State" section of the Keras request).
+ * S: (B, Hkv, Dk, Dv) float32, required.  Z: (B, Hkv, Dk) float32, may be
+ * NULL (use_normalizer = 0 needs no key_state).  Enqueued memsets. */
+la_status la_get_initial_state(const la_params* p, float* S, float* Z, la_stream_t stream);
+
+/* Bytes of device workspace a call needs (0 when none).  causal: 1 for
+ * la_forward_causal, 0 for la_forward_noncausal.  The workspace must be at
+ * least 256-byte aligned, must not be used by two calls that may run at the
+ * same time, and needs no initialisation. */
+size_t la_workspace_bytes(const la_params* p, int causal);
+
+/* Causal prefill over T tokens (Keras request, Mathematical definition /
+ * Causal; ONNX LinearAttention, prefill T > 1 and decode T = 1).
+ *   q, k, v     activations (io_dtype), required when T > 0.
+ *   decay       (B, T, Hkv) io_dtype, log space; required iff rule = GATED.
+ *   S0, Z0      carried state in (initial_state / past_state); NULL = zeros.
+ *               Z0 is ignored when use_normalizer = 0.
+ *   y           output (B, T, Hq, Dv) out_dtype, required when T > 0.
+ *   S_out,Z_out final state (return_state); NULL = not returned.  S_out may
+ *               alias S0 and Z_out may alias Z0 (in-place streaming).
+ *   ws          workspace of ws_bytes >= la_workspace_bytes(p, 1).
+ * T = 0 copies S0/Z0 (or zeros) to S_out/Z_out.
+ * LA_ERR_UNSUPPORTED: gated rule together with a feature map or the
+ * normalizer (the pages define neither combination). */
+la_status la_forward_causal(const la_params* p, const void* q, const void* k, const void* v,
+                            const void* decay, const float* S0, const float* Z0, void* y,
+                            float* S_out, float* Z_out, void* ws, size_t ws_bytes,
+                            la_stream_t stream);
+
+/* Non-causal attention with the global state (Keras request, Mathematical
+ * definition / Non-causal).  No state in or out ("Non-causal attention does
+ * not expose streaming state").  Only the linear rule. */
+la_status la_forward_noncausal(const la_params* p, const void* q, const void* k, const void* v,
+                               void* y, void* ws, size_t ws_bytes, la_stream_t stream);
+
+/* One streaming token per sequence (seq_len must be 1): the recurrent update
+ * and read-out ("Causal Linear Attention": S_i = S_{i-1} + phi(k_i) v_i^T,
+ * then the read-out with S_i; ONNX LinearAttention decode, T = 1).
+ *   q (B,1,Hq,Dk), k (B,1,Hkv,Dk), v (B,1,Hkv,Dv), decay (B,1,Hkv) or NULL.
+ *   S (B,Hkv,Dk,Dv) and Z (B,Hkv,Dk) float32 are read and updated IN PLACE;
+ *   Z may be NULL when use_normalizer = 0.  y (B,1,Hq,Dv) out_dtype. */
+la_status la_decode_step(const la_params* p, const void* q, const void* k, const void* v,
+                         const void* decay, float* S, float* Z, void* y, la_stream_t stream);
+
+/* Static string for a status code. */
+const char* la_status_string(la_status s);
+
+/* One-line description of the last failure on this host thread ("" if none). */
+const char* la_last_error(void);
+
+/* LINATTN_ABI_VERSION of the loaded library. */
+int la_abi_version(void);
+
+/* Number of CUDA kernels this library has enqueued in this process so far
+ * (memsets and copies are not counted).  For accounting in benchmarks. */
+uint64_t la_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LINATTN_H */

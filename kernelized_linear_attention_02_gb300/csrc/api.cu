@@ -1,0 +1,218 @@
+// api.cu -- the C ABI declared in include/linattn.h: argument checks,
+// workspace sizing and kernel selection.  Every entry point validates all of
+// its arguments before it enqueues anything.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "kernels.h"
+
+namespace la {
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace la
+
+namespace {
+
+thread_local std::string g_last_error;
+
+la_status fail(la_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+la_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(LA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+enum class Call { kCausal, kNonCausal, kDecode, kState };
+
+constexpr size_t kAlign = 256;
+size_t round_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+// Checks every field of the parameter block and resolves it into a Problem.
+la_status make_problem(const la_params* p, Call call, la::Problem* P) {
+    if (!p) return fail(LA_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1) return fail(LA_ERR_INVALID_ARG, "batch must be >= 1 (got %lld)", (long long)p->batch);
+    if (p->seq_len < 0) return fail(LA_ERR_INVALID_ARG, "seq_len must be >= 0");
+    if (call == Call::kDecode && p->seq_len != 1)
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step needs seq_len == 1 (got %lld)", (long long)p->seq_len);
+    if (p->q_heads < 1 || p->kv_heads < 1) return fail(LA_ERR_INVALID_ARG, "head counts must be >= 1");
+    if (p->q_heads % p->kv_heads != 0)
+        return fail(LA_ERR_INVALID_ARG, "q_heads (%d) must be a multiple of kv_heads (%d)", p->q_heads,
+                    p->kv_heads);
+    if (p->key_dim < 1 || p->value_dim < 1) return fail(LA_ERR_INVALID_ARG, "key_dim and value_dim must be >= 1");
+    if (p->key_dim > 128 || p->value_dim > 128)
+        return fail(LA_ERR_UNSUPPORTED, "key_dim and value_dim above 128 are not implemented");
+    if ((p->io_dtype != LA_F32 && p->io_dtype != LA_BF16) || (p->out_dtype != LA_F32 && p->out_dtype != LA_BF16))
+        return fail(LA_ERR_INVALID_ARG, "io_dtype/out_dtype must be LA_F32 or LA_BF16 (floating point only)");
+    if (p->feature_map < LA_FMAP_NONE || p->feature_map > LA_FMAP_RELU_EPS)
+        return fail(LA_ERR_INVALID_ARG, "unknown feature_map %d", p->feature_map);
+    if (p->use_normalizer != 0 && p->use_normalizer != 1)
+        return fail(LA_ERR_INVALID_ARG, "use_normalizer must be 0 or 1");
+    if (!std::isfinite(p->epsilon) || p->epsilon < 0.f) return fail(LA_ERR_INVALID_ARG, "epsilon must be finite and >= 0");
+    if (!std::isfinite(p->scale)) return fail(LA_ERR_INVALID_ARG, "scale must be finite");
+    if (p->update_rule != LA_RULE_LINEAR && p->update_rule != LA_RULE_GATED)
+        return fail(LA_ERR_INVALID_ARG, "unknown update_rule %d", p->update_rule);
+    if (p->reserved != 0) return fail(LA_ERR_INVALID_ARG, "reserved must be 0");
+    if (p->update_rule == LA_RULE_GATED && (p->feature_map != LA_FMAP_NONE || p->use_normalizer))
+        return fail(LA_ERR_UNSUPPORTED, "the gated rule is defined without a feature map or normalizer");
+    if (call == Call::kNonCausal && p->update_rule != LA_RULE_LINEAR)
+        return fail(LA_ERR_UNSUPPORTED, "non-causal attention has no decay (gated rule)");
+    const int64_t grid = p->batch * (int64_t)p->kv_heads;
+    if (grid > 0x7fffffff) return fail(LA_ERR_UNSUPPORTED, "batch * kv_heads too large");
+
+    P->B = p->batch;
+    P->T = p->seq_len;
+    P->Hq = p->q_heads;
+    P->Hkv = p->kv_heads;
+    P->G = p->q_heads / p->kv_heads;
+    P->Dk = p->key_dim;
+    P->Dv = p->value_dim;
+    P->io_bf16 = p->io_dtype == LA_BF16;
+    P->out_bf16 = p->out_dtype == LA_BF16;
+    P->fmap = p->feature_map;
+    P->norm = p->use_normalizer;
+    P->gated = p->update_rule == LA_RULE_GATED;
+    P->eps = p->epsilon;
+    P->scale = p->scale == 0.f ? 1.f / std::sqrt((float)p->key_dim) : p->scale;
+    return LA_OK;
+}
+
+size_t state_bytes(const la::Problem& P) { return sizeof(float) * (size_t)P.B * P.Hkv * P.Dk * P.Dv; }
+size_t key_state_bytes(const la::Problem& P) { return sizeof(float) * (size_t)P.B * P.Hkv * P.Dk; }
+
+size_t workspace_bytes(const la::Problem& P, bool causal) {
+    if (causal) return 0;
+    return round_up(state_bytes(P)) + round_up(key_state_bytes(P));
+}
+
+la_status check_ws(const la::Problem& P, bool causal, void* ws, size_t ws_bytes) {
+    const size_t need = workspace_bytes(P, causal);
+    if (need == 0) return LA_OK;
+    if (!ws || ws_bytes < need)
+        return fail(LA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, ws ? ws_bytes : 0);
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign)
+        return fail(LA_ERR_WORKSPACE, "workspace must be %zu-byte aligned", kAlign);
+    return LA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int la_abi_version(void) { return LINATTN_ABI_VERSION; }
+
+uint64_t la_launch_count(void) { return la::g_launches.load(std::memory_order_relaxed); }
+
+const char* la_last_error(void) { return g_last_error.c_str(); }
+
+const char* la_status_string(la_status s) {
+    switch (s) {
+    case LA_OK: return "ok";
+    case LA_ERR_INVALID_ARG: return "invalid argument";
+    case LA_ERR_UNSUPPORTED: return "unsupported";
+    case LA_ERR_WORKSPACE: return "workspace missing or too small";
+    case LA_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+la_status la_get_initial_state(const la_params* p, float* S, float* Z, la_stream_t stream) {
+    la::Problem P;
+    la_status st = make_problem(p, Call::kState, &P);
+    if (st != LA_OK) return st;
+    if (!S) return fail(LA_ERR_INVALID_ARG, "S is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(S, 0, state_bytes(P), s);
+    if (e == cudaSuccess && Z) e = cudaMemsetAsync(Z, 0, key_state_bytes(P), s);
+    if (e != cudaSuccess) return cuda_fail(e, "la_get_initial_state");
+    g_last_error.clear();
+    return LA_OK;
+}
+
+size_t la_workspace_bytes(const la_params* p, int causal) {
+    la::Problem P;
+    if (make_problem(p, causal ? Call::kCausal : Call::kNonCausal, &P) != LA_OK) return 0;
+    return workspace_bytes(P, causal != 0);
+}
+
+la_status la_forward_causal(const la_params* p, const void* q, const void* k, const void* v,
+                            const void* decay, const float* S0, const float* Z0, void* y,
+                            float* S_out, float* Z_out, void* ws, size_t ws_bytes, la_stream_t stream) {
+    la::Problem P;
+    la_status st = make_problem(p, Call::kCausal, &P);
+    if (st != LA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!P.norm) Z0 = nullptr, Z_out = nullptr;  // no key_state without the normalizer
+    if (P.T == 0) {  // nothing to attend: the state passes through
+        cudaError_t e = cudaSuccess;
+        if (S_out && S_out != S0)
+            e = S0 ? cudaMemcpyAsync(S_out, S0, state_bytes(P), cudaMemcpyDeviceToDevice, s)
+                   : cudaMemsetAsync(S_out, 0, state_bytes(P), s);
+        if (e == cudaSuccess && Z_out && Z_out != Z0)
+            e = Z0 ? cudaMemcpyAsync(Z_out, Z0, key_state_bytes(P), cudaMemcpyDeviceToDevice, s)
+                   : cudaMemsetAsync(Z_out, 0, key_state_bytes(P), s);
+        if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal");
+        g_last_error.clear();
+        return LA_OK;
+    }
+    if (!q || !k || !v || !y) return fail(LA_ERR_INVALID_ARG, "q, k, v and y are required when seq_len > 0");
+    if (P.gated && !decay) return fail(LA_ERR_INVALID_ARG, "the gated rule needs decay");
+    if ((st = check_ws(P, true, ws, ws_bytes)) != LA_OK) return st;
+    cudaError_t e = la::recurrent_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, s);
+    if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal");
+    g_last_error.clear();
+    return LA_OK;
+}
+
+la_status la_forward_noncausal(const la_params* p, const void* q, const void* k, const void* v, void* y,
+                               void* ws, size_t ws_bytes, la_stream_t stream) {
+    la::Problem P;
+    la_status st = make_problem(p, Call::kNonCausal, &P);
+    if (st != LA_OK) return st;
+    if (P.T == 0) {
+        g_last_error.clear();
+        return LA_OK;
+    }
+    if (!q || !k || !v || !y) return fail(LA_ERR_INVALID_ARG, "q, k, v and y are required when seq_len > 0");
+    if ((st = check_ws(P, false, ws, ws_bytes)) != LA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float* S_ws = static_cast<float*>(ws);
+    float* Z_ws = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(state_bytes(P)));
+    cudaError_t e = la::recurrent_noncausal(P, q, k, v, y, S_ws, Z_ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "la_forward_noncausal");
+    g_last_error.clear();
+    return LA_OK;
+}
+
+la_status la_decode_step(const la_params* p, const void* q, const void* k, const void* v, const void* decay,
+                         float* S, float* Z, void* y, la_stream_t stream) {
+    la::Problem P;
+    la_status st = make_problem(p, Call::kDecode, &P);
+    if (st != LA_OK) return st;
+    if (!q || !k || !v || !y || !S) return fail(LA_ERR_INVALID_ARG, "q, k, v, y and S are required");
+    if (P.norm && !Z) return fail(LA_ERR_INVALID_ARG, "Z is required when use_normalizer = 1");
+    if (P.gated && !decay) return fail(LA_ERR_INVALID_ARG, "the gated rule needs decay");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (la::decode_supported(P) && reinterpret_cast<uintptr_t>(S) % 16 == 0)
+        e = la::decode_step(P, q, k, v, P.gated ? decay : nullptr, S, P.norm ? Z : nullptr, y, s);
+    else
+        e = la::recurrent_causal(P, q, k, v, P.gated ? decay : nullptr, S, P.norm ? Z : nullptr, y, S,
+                                 P.norm ? Z : nullptr, s);
+    if (e != cudaSuccess) return cuda_fail(e, "la_decode_step");
+    g_last_error.clear();
+    return LA_OK;
+}
+
+}  // extern "C"

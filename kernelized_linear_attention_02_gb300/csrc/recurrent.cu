@@ -1,0 +1,204 @@
+// recurrent.cu -- the token-by-token recurrence on CUDA cores.
+//
+// This is the float32 path of the library (float32 q/k/v need float32
+// products, which the bf16 tensor-core kernels do not give) and the path for
+// shapes the tensor-core kernels do not cover.  One CTA owns one (batch,
+// kv-head) state stream and walks its tokens in order, exactly the causal
+// recurrence of the Keras request ("Mathematical definition / Causal"):
+// update S and Z with token t first, then read out every query head of the
+// group with S_t ("the current token is included in its own context").
+//
+// The same kernel also runs the two halves of the non-causal form: a state
+// pass (update only; S = sum_j phi(K_j)^T V_j, Z = sum_j phi(K_j)) and a
+// read-out pass with that fixed global state.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace la {
+
+namespace {
+
+constexpr int kThreads = 256;  // 8 warps: warp w owns rows w, w+8, ...; lane c owns columns c, c+32, ...
+constexpr int kRowsPerThread = 16;  // Dk <= 128
+constexpr int kColsPerThread = 4;   // Dv <= 128
+constexpr int kHeadBlock = 4;       // query heads reduced per round
+
+struct RecArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* decay;
+    const float* S0;
+    const float* Z0;
+    void* y;
+    float* S_out;
+    float* Z_out;
+    Problem P;
+    int mode;  // kModeCausal, kModeStateOnly, kModeReadoutOnly
+};
+
+enum { kModeCausal = 0, kModeStateOnly = 1, kModeReadoutOnly = 2 };
+
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(kThreads) recurrent_kernel(RecArgs a) {
+    const Problem& P = a.P;
+    const int Dk = P.Dk, Dv = P.Dv, G = P.G;
+    extern __shared__ float smem[];
+    float* fk = smem;             // [128]   phi(k_t)
+    float* Zs = fk + 128;         // [128]   Z_t
+    float* den = Zs + 128;        // [128]   phi(q).Z + eps per query head of the group
+    float* fq = den + 128;        // [G*Dk]  phi(q_t) of the group
+    float* red = fq + G * Dk;     // [kHeadBlock][8][128] partial read-outs
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t bh = blockIdx.x;
+    const int64_t b = bh / P.Hkv;
+    const int hk = (int)(bh % P.Hkv);
+    const TIn* q = static_cast<const TIn*>(a.q);
+    const TIn* k = static_cast<const TIn*>(a.k);
+    const TIn* v = static_cast<const TIn*>(a.v);
+    const TIn* decay = static_cast<const TIn*>(a.decay);
+    TOut* y = static_cast<TOut*>(a.y);
+    const bool update = a.mode != kModeReadoutOnly;
+    const bool readout = a.mode != kModeStateOnly;
+
+    // state slice owned by this thread: rows warp + 8m, columns lane + 32n
+    float s[kRowsPerThread][kColsPerThread];
+    const float* S0 = a.S0 ? a.S0 + bh * (int64_t)Dk * Dv : nullptr;
+#pragma unroll
+    for (int m = 0; m < kRowsPerThread; ++m)
+#pragma unroll
+        for (int n = 0; n < kColsPerThread; ++n) {
+            const int i = warp + 8 * m, j = lane + 32 * n;
+            s[m][n] = (S0 && i < Dk && j < Dv) ? S0[(int64_t)i * Dv + j] : 0.f;
+        }
+    if (tid < 128) Zs[tid] = (P.norm && a.Z0 && tid < Dk) ? a.Z0[bh * Dk + tid] : 0.f;
+    __syncthreads();  // Z0 may alias Z_out of this same CTA only
+
+    for (int64_t t = 0; t < P.T; ++t) {
+        const int64_t tok = b * P.T + t;
+        if (update)
+            for (int i = tid; i < Dk; i += kThreads)
+                fk[i] = phi<false>(P.fmap, load_in(k, (tok * P.Hkv + hk) * Dk + i), P.eps);
+        if (readout)
+            for (int idx = tid; idx < G * Dk; idx += kThreads) {
+                const int r = idx / Dk, i = idx - r * Dk;
+                fq[idx] = phi<false>(P.fmap, load_in(q, (tok * P.Hq + hk * G + r) * Dk + i), P.eps);
+            }
+        __syncthreads();
+
+        if (update) {
+            const float dec = P.gated ? expf(load_in(decay, tok * P.Hkv + hk)) : 1.f;
+            float vj[kColsPerThread];
+#pragma unroll
+            for (int n = 0; n < kColsPerThread; ++n) {
+                const int j = lane + 32 * n;
+                vj[n] = j < Dv ? load_in(v, (tok * P.Hkv + hk) * Dv + j) : 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < kRowsPerThread; ++m) {
+                const int i = warp + 8 * m;
+                const float f = i < Dk ? fk[i] : 0.f;
+#pragma unroll
+                for (int n = 0; n < kColsPerThread; ++n) s[m][n] = fmaf(f, vj[n], dec * s[m][n]);
+            }
+            if (P.norm && tid < Dk) Zs[tid] += fk[tid];
+        }
+        __syncthreads();          // Zs complete; fk consumed before the next token overwrites it
+        if (!readout) continue;  // uniform across the CTA
+
+        if (P.norm)
+            for (int r = warp; r < G; r += 8) {
+                float d = 0.f;
+                for (int i = lane; i < Dk; i += 32) d = fmaf(fq[r * Dk + i], Zs[i], d);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                if (lane == 0) den[r] = d + P.eps;
+            }
+        for (int r0 = 0; r0 < G; r0 += kHeadBlock) {
+            const int nh = min(kHeadBlock, G - r0);
+            for (int rr = 0; rr < nh; ++rr) {
+                float acc[kColsPerThread] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int m = 0; m < kRowsPerThread; ++m) {
+                    const int i = warp + 8 * m;
+                    const float f = i < Dk ? fq[(r0 + rr) * Dk + i] : 0.f;
+#pragma unroll
+                    for (int n = 0; n < kColsPerThread; ++n) acc[n] = fmaf(f, s[m][n], acc[n]);
+                }
+#pragma unroll
+                for (int n = 0; n < kColsPerThread; ++n)
+                    red[(rr * 8 + warp) * 128 + lane + 32 * n] = acc[n];
+            }
+            __syncthreads();  // red and den complete
+            for (int idx = tid; idx < nh * Dv; idx += kThreads) {
+                const int rr = idx / Dv, j = idx - rr * Dv;
+                float num = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) num += red[(rr * 8 + w) * 128 + j];
+                const float out = P.norm ? num / den[r0 + rr] : num;
+                store_out(y, (tok * P.Hq + hk * G + r0 + rr) * Dv + j, P.scale * out);
+            }
+            __syncthreads();  // red is reused by the next head block / token
+        }
+    }
+
+    if (a.S_out) {
+        float* So = a.S_out + bh * (int64_t)Dk * Dv;
+#pragma unroll
+        for (int m = 0; m < kRowsPerThread; ++m)
+#pragma unroll
+            for (int n = 0; n < kColsPerThread; ++n) {
+                const int i = warp + 8 * m, j = lane + 32 * n;
+                if (i < Dk && j < Dv) So[(int64_t)i * Dv + j] = s[m][n];
+            }
+    }
+    __syncthreads();
+    if (a.Z_out && P.norm && tid < Dk) a.Z_out[bh * Dk + tid] = Zs[tid];
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch(const RecArgs& a, cudaStream_t st) {
+    const Problem& P = a.P;
+    const size_t smem = sizeof(float) * (3 * 128 + (size_t)P.G * P.Dk + kHeadBlock * 8 * 128);
+    auto kern = recurrent_kernel<TIn, TOut>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3((unsigned)(P.B * P.Hkv)), kThreads, smem, st>>>(a);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t dispatch(const RecArgs& a, cudaStream_t st) {
+    if (a.P.io_bf16)
+        return a.P.out_bf16 ? launch<__nv_bfloat16, __nv_bfloat16>(a, st)
+                            : launch<__nv_bfloat16, float>(a, st);
+    return a.P.out_bf16 ? launch<float, __nv_bfloat16>(a, st) : launch<float, float>(a, st);
+}
+
+}  // namespace
+
+size_t recurrent_smem_bytes(const Problem& P) {
+    return sizeof(float) * (3 * 128 + (size_t)P.G * P.Dk + kHeadBlock * 8 * 128);
+}
+
+cudaError_t recurrent_causal(const Problem& P, const void* q, const void* k, const void* v,
+                             const void* decay, const float* S0, const float* Z0, void* y,
+                             float* S_out, float* Z_out, cudaStream_t st) {
+    RecArgs a{q, k, v, decay, S0, Z0, y, S_out, Z_out, P, kModeCausal};
+    return dispatch(a, st);
+}
+
+cudaError_t recurrent_noncausal(const Problem& P, const void* q, const void* k, const void* v,
+                                void* y, float* S_ws, float* Z_ws, cudaStream_t st) {
+    // pass 1: global state; pass 2: read-out with it (no update)
+    RecArgs a1{nullptr, k, v, nullptr, nullptr, nullptr, nullptr, S_ws, Z_ws, P, kModeStateOnly};
+    a1.P.gated = 0;
+    cudaError_t e = dispatch(a1, st);
+    if (e != cudaSuccess) return e;
+    RecArgs a2{q, nullptr, nullptr, nullptr, S_ws, Z_ws, y, nullptr, nullptr, P, kModeReadoutOnly};
+    a2.P.gated = 0;
+    return dispatch(a2, st);
+}
+
+}  // namespace la

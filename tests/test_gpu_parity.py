@@ -1,0 +1,227 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Small cases are compared element by element over the whole output; they span
+several chunks of the tensor-core kernels and end on ragged tails.  The
+workloads at full size are compared on sampled (batch, kv-head) streams the
+oracle computes in full.  Tolerances are in tests/parity_utils.py.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import kernelized_linear_attention_02_gb300 as la
+import linattn_inputs as inputs
+from parity_utils import (assert_close, gpu_slices, oracle_slices, rel_err, to64, tol_for, TOL_F32)
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from kernelized_linear_attention_02_gb300 import build
+    build.build()
+    la.lib()
+
+
+def rand(shape, seed, dtype, std=1.0):
+    g = inputs.generator(seed, DEV)
+    return inputs.normal(shape, g, std, dtype=dtype, device=DEV)
+
+
+def run_case(B, T, Hq, Hkv, Dk, Dv, dtype, out_dtype, fmap, norm, rule="linear", S0=False, seed=0,
+             scale=1.0, eps=1e-6, std=1.0):
+    q = rand((B, T, Hq, Dk), seed, dtype, std)
+    k = rand((B, T, Hkv, Dk), seed + 1, dtype, std)
+    v = rand((B, T, Hkv, Dv), seed + 2, dtype)
+    decay = None
+    if rule == "gated":
+        x = rand((B, T, Hkv), seed + 3, torch.float32) + 3.0
+        decay = torch.nn.functional.logsigmoid(x).to(dtype)
+    init = None
+    if S0:
+        S0t = rand((B, Hkv, Dk, Dv), seed + 4, torch.float32)
+        Z0t = rand((B, Hkv, Dk), seed + 5, torch.float32).abs() + 1.0 if norm else None
+        init = (S0t, Z0t)
+    y, (S, Z) = la.la_forward_causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map=fmap,
+                                     use_normalizer=norm, epsilon=eps, scale=scale, update_rule=rule,
+                                     decay=decay, initial_state=init, return_state=True,
+                                     out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    yr, Sr, Zr = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map=fmap,
+                               use_normalizer=norm, eps=eps, scale=scale, rule=rule, decay=decay,
+                               S0=None if init is None else init[0],
+                               Z0=None if init is None else init[1])
+    tol = tol_for(dtype, out_dtype)
+    assert_close(to64(y), yr, tol, "y")
+    assert_close(to64(S), Sr, tol_for(dtype, torch.float32), "S")
+    if norm:
+        assert_close(to64(Z), Zr, 1e-5, "Z")
+    return y, S, Z
+
+
+# ---------------------------------------------------------------------------
+# the tiny workload: causal, non-causal, and chunks of 16 with carried state
+
+
+def test_tiny_workload_fp32():
+    w = inputs.TINY
+    q, k, v, _ = inputs.make_qkv(w, device=DEV)
+    kw = dict(q_heads=w.q_heads, kv_heads=w.kv_heads, feature_map=w.feature_map,
+              use_normalizer=w.use_normalizer, epsilon=w.eps, scale=w.scale)
+    y, (S, Z) = la.la_forward_causal(q, k, v, return_state=True, **kw)
+    yn = la.la_forward_noncausal(q, k, v, **{k_: v_ for k_, v_ in kw.items()})
+    # four chunks of 16 tokens, the state carried in place
+    Sc, Zc = la.la_get_initial_state(w.B, w.kv_heads, w.Dk, w.Dv)
+    ys = []
+    for c in range(4):
+        sl = slice(16 * c, 16 * (c + 1))
+        ys.append(la.la_forward_causal(q[:, sl].contiguous(), k[:, sl].contiguous(), v[:, sl].contiguous(),
+                                       initial_state=(Sc, Zc), return_state=True, state_out=(Sc, Zc),
+                                       **kw)[0])
+    torch.cuda.synchronize()
+    yr, Sr, Zr = oracle.causal(q, k, v, q_heads=2, kv_heads=2, feature_map=w.feature_map, eps=w.eps)
+    ynr = oracle.noncausal(q, k, v, q_heads=2, kv_heads=2, feature_map=w.feature_map, eps=w.eps)
+    assert_close(to64(y), yr, TOL_F32, "causal")
+    assert_close(to64(yn), ynr, TOL_F32, "non-causal")
+    assert_close(to64(torch.cat(ys, 1)), yr, TOL_F32, "chunked")
+    assert_close(to64(Sc), Sr, TOL_F32, "chunked S")
+    assert_close(to64(Zc), Zr, TOL_F32, "chunked Z")
+    assert_close(to64(S), Sr, TOL_F32, "S")
+
+
+# ---------------------------------------------------------------------------
+# a grid of small shapes: several chunks plus a ragged tail, GQA, odd dims
+
+SHAPES = [  # B, T, Hq, Hkv, Dk, Dv
+    (1, 1, 2, 2, 64, 64),
+    (2, 37, 2, 2, 16, 16),
+    (2, 300, 4, 4, 64, 64),
+    (1, 257, 8, 2, 128, 128),
+    (2, 130, 3, 1, 32, 64),
+    (1, 200, 2, 2, 128, 64),
+    (1, 129, 4, 2, 64, 128),
+]
+MODES = [("elu_plus_one", True), ("relu", True), ("elu_plus_one", False), ("none", False)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: f"{m[0]}-{'norm' if m[1] else 'raw'}")
+def test_causal_small(shape, dtype, mode):
+    B, T, Hq, Hkv, Dk, Dv = shape
+    fmap, norm = mode
+    std = 0.5 if fmap == "elu_plus_one" else 1.0
+    run_case(B, T, Hq, Hkv, Dk, Dv, dtype, torch.float32, fmap, norm, S0=(T % 2 == 0), std=std,
+             seed=T + Dk)
+
+
+@pytest.mark.parametrize("shape", SHAPES[1:5], ids=lambda s: "x".join(map(str, s)))
+def test_causal_small_bf16_output(shape):
+    B, T, Hq, Hkv, Dk, Dv = shape
+    run_case(B, T, Hq, Hkv, Dk, Dv, torch.bfloat16, torch.bfloat16, "elu_plus_one", True, std=0.5)
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_gated_small(shape, dtype):
+    B, T, Hq, Hkv, Dk, Dv = shape
+    run_case(B, T, Hq, Hkv, Dk, Dv, dtype, torch.float32, "none", False, rule="gated", S0=True,
+             scale=0.0, seed=7)
+
+
+@pytest.mark.parametrize("shape", SHAPES[1:], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("mode", MODES[:3], ids=lambda m: f"{m[0]}-{'norm' if m[1] else 'raw'}")
+def test_noncausal_small(shape, dtype, mode):
+    B, T, Hq, Hkv, Dk, Dv = shape
+    fmap, norm = mode
+    q = rand((B, T, Hq, Dk), 11, dtype, 0.5)
+    k = rand((B, T, Hkv, Dk), 12, dtype, 0.5)
+    v = rand((B, T, Hkv, Dv), 13, dtype)
+    y = la.la_forward_noncausal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map=fmap,
+                                use_normalizer=norm, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    yr = oracle.noncausal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map=fmap, use_normalizer=norm)
+    assert_close(to64(y), yr, tol_for(dtype, torch.float32), "non-causal")
+
+
+def test_empty_sequence_passes_state_through():
+    B, H, D = 2, 2, 64
+    q = torch.empty(B, 0, H, D, dtype=torch.bfloat16, device=DEV)
+    S0 = rand((B, H, D, D), 1, torch.float32)
+    Z0 = rand((B, H, D), 2, torch.float32)
+    y, (S, Z) = la.la_forward_causal(q, q, q, q_heads=H, kv_heads=H, initial_state=(S0, Z0),
+                                     return_state=True)
+    torch.cuda.synchronize()
+    assert y.shape == (B, 0, H, D)
+    assert torch.equal(S, S0) and torch.equal(Z, Z0)
+
+
+def test_chunked_equals_full_bf16():
+    """Calls with carried state equal one full call (ragged chunk lengths)."""
+    B, T, H, D = 2, 700, 4, 64
+    q = rand((B, T, H, D), 21, torch.bfloat16, 0.5)
+    k = rand((B, T, H, D), 22, torch.bfloat16, 0.5)
+    v = rand((B, T, H, D), 23, torch.bfloat16)
+    kw = dict(q_heads=H, kv_heads=H, out_dtype=torch.float32)
+    y_full, (S_full, Z_full) = la.la_forward_causal(q, k, v, return_state=True, **kw)
+    S, Z = la.la_get_initial_state(B, H, D, D)
+    ys = []
+    for a, b in zip([0, 1, 129, 300, 555], [1, 129, 300, 555, 700]):
+        ys.append(la.la_forward_causal(q[:, a:b].contiguous(), k[:, a:b].contiguous(),
+                                       v[:, a:b].contiguous(), initial_state=(S, Z), return_state=True,
+                                       state_out=(S, Z), **kw)[0])
+    torch.cuda.synchronize()
+    yr, Sr, Zr = oracle.causal(q, k, v, q_heads=H, kv_heads=H)
+    assert_close(to64(torch.cat(ys, 1)), yr, 2e-3, "chunked")
+    assert_close(to64(y_full), yr, 2e-3, "full")
+    assert_close(to64(S), Sr, 2e-3, "chunked S")
+    assert_close(to64(Z), Zr, 1e-5, "chunked Z")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("rule", ["linear", "gated"])
+def test_decode_steps_small(dtype, rule):
+    """Prefill then token-by-token steps equal one causal pass over all tokens."""
+    B, T0, steps, Hq, Hkv, D = 3, 40, 9, 4, 2, 64
+    fmap, norm = ("elu_plus_one", True) if rule == "linear" else ("none", False)
+    T = T0 + steps
+    q = rand((B, T, Hq, D), 31, dtype, 0.5)
+    k = rand((B, T, Hkv, D), 32, dtype, 0.5)
+    v = rand((B, T, Hkv, D), 33, dtype)
+    decay = None
+    if rule == "gated":
+        decay = torch.nn.functional.logsigmoid(rand((B, T, Hkv), 34, torch.float32) + 3.0).to(dtype)
+    kw = dict(q_heads=Hq, kv_heads=Hkv, feature_map=fmap, use_normalizer=norm, update_rule=rule,
+              out_dtype=torch.float32)
+    _, (S, Z) = la.la_forward_causal(q[:, :T0].contiguous(), k[:, :T0].contiguous(),
+                                     v[:, :T0].contiguous(), return_state=True,
+                                     decay=None if decay is None else decay[:, :T0].contiguous(), **kw)
+    ys = []
+    for t in range(T0, T):
+        ys.append(la.la_decode_step(q[:, t:t + 1].contiguous(), k[:, t:t + 1].contiguous(),
+                                    v[:, t:t + 1].contiguous(), S, Z,
+                                    decay=None if decay is None else decay[:, t:t + 1].contiguous(), **kw))
+    torch.cuda.synchronize()
+    yr, Sr, Zr = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map=fmap,
+                               use_normalizer=norm, rule=rule, decay=decay)
+    tol = tol_for(dtype, torch.float32)
+    assert_close(to64(torch.cat(ys, 1)), yr[:, T0:], tol, "decode y")
+    assert_close(to64(S), Sr, tol_for(dtype, torch.float32), "decode S")
+    if norm:
+        assert_close(to64(Z), Zr, 1e-5, "decode Z")
+
+
+def test_invalid_call_raises_and_launches_nothing():
+    q = torch.zeros(1, 4, 3, 16, dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros(1, 4, 2, 16, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(la.LinearAttentionError) as e:
+        la.la_forward_causal(q, k, k, q_heads=3, kv_heads=2)
+    assert e.value.status == la.LA_ERR_INVALID_ARG
