@@ -145,6 +145,12 @@ const char* la_last_error(void);
 /* LINATTN_ABI_VERSION of the loaded library. */
 int la_abi_version(void);
 
+/* Error word of the tensor-core kernels on the current device: 0 when no
+ * kernel gave up on a bounded wait (each pipeline wait ends with an error
+ * bit instead of hanging); a nonzero value names the wait sites that timed
+ * out.  Synchronous (device-to-host copy).  reset != 0 clears it. */
+unsigned la_device_error(int reset);
+
 /* Number of CUDA kernels this library has enqueued in this process so far
  * (memsets and copies are not counted).  For accounting in benchmarks. */
 uint64_t la_launch_count(void);

@@ -55,6 +55,7 @@ _SIGNATURES = {
     "la_last_error": (ctypes.c_char_p, []),
     "la_abi_version": (ctypes.c_int, []),
     "la_launch_count": (ctypes.c_uint64, []),
+    "la_device_error": (ctypes.c_uint, [ctypes.c_int]),
 }
 
 _lib = None
@@ -213,6 +214,11 @@ def la_decode_step(q, k, v, S, Z=None, *, q_heads, kv_heads, feature_map="elu_pl
 def la_launch_count() -> int:
     """Kernels the library has enqueued in this process so far."""
     return int(lib().la_launch_count())
+
+
+def la_device_error(reset: bool = True) -> int:
+    """Error word of the bounded pipeline waits on the current device (0 = none)."""
+    return int(lib().la_device_error(int(bool(reset))))
 
 
 def resolve_scale(scale: float, key_dim: int) -> float:

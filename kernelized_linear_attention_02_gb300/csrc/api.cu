@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/linattn.h: argument checks,
 // workspace sizing and kernel selection.  Every entry point validates all of
 // its arguments before it enqueues anything.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -92,8 +93,9 @@ size_t state_bytes(const la::Problem& P) { return sizeof(float) * (size_t)P.B * 
 size_t key_state_bytes(const la::Problem& P) { return sizeof(float) * (size_t)P.B * P.Hkv * P.Dk; }
 
 size_t workspace_bytes(const la::Problem& P, bool causal) {
-    if (causal) return 0;
-    return round_up(state_bytes(P)) + round_up(key_state_bytes(P));
+    const size_t rec = causal ? 0 : round_up(state_bytes(P)) + round_up(key_state_bytes(P));
+    if (!la::chunk_supported(P)) return rec;
+    return std::max(rec, la::chunk_workspace_bytes(P, causal));
 }
 
 la_status check_ws(const la::Problem& P, bool causal, void* ws, size_t ws_bytes) {
@@ -113,6 +115,8 @@ extern "C" {
 int la_abi_version(void) { return LINATTN_ABI_VERSION; }
 
 uint64_t la_launch_count(void) { return la::g_launches.load(std::memory_order_relaxed); }
+
+unsigned la_device_error(int reset) { return la::chunk_device_error(reset != 0); }
 
 const char* la_last_error(void) { return g_last_error.c_str(); }
 
@@ -169,7 +173,11 @@ la_status la_forward_causal(const la_params* p, const void* q, const void* k, co
     if (!q || !k || !v || !y) return fail(LA_ERR_INVALID_ARG, "q, k, v and y are required when seq_len > 0");
     if (P.gated && !decay) return fail(LA_ERR_INVALID_ARG, "the gated rule needs decay");
     if ((st = check_ws(P, true, ws, ws_bytes)) != LA_OK) return st;
-    cudaError_t e = la::recurrent_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, s);
+    cudaError_t e;
+    if (la::chunk_supported(P) && la::chunk_pointers_ok(q, k, v, y))
+        e = la::chunk_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, ws, s);
+    else
+        e = la::recurrent_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, s);
     if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal");
     g_last_error.clear();
     return LA_OK;
@@ -187,9 +195,14 @@ la_status la_forward_noncausal(const la_params* p, const void* q, const void* k,
     if (!q || !k || !v || !y) return fail(LA_ERR_INVALID_ARG, "q, k, v and y are required when seq_len > 0");
     if ((st = check_ws(P, false, ws, ws_bytes)) != LA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    float* S_ws = static_cast<float*>(ws);
-    float* Z_ws = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(state_bytes(P)));
-    cudaError_t e = la::recurrent_noncausal(P, q, k, v, y, S_ws, Z_ws, s);
+    cudaError_t e;
+    if (la::chunk_supported(P) && la::chunk_pointers_ok(q, k, v, y)) {
+        e = la::chunk_noncausal(P, q, k, v, y, ws, s);
+    } else {
+        float* S_ws = static_cast<float*>(ws);
+        float* Z_ws = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(state_bytes(P)));
+        e = la::recurrent_noncausal(P, q, k, v, y, S_ws, Z_ws, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "la_forward_noncausal");
     g_last_error.clear();
     return LA_OK;

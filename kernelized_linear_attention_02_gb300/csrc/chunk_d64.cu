@@ -1,0 +1,6 @@
+// chunk_d64.cu -- tensor-core chunk kernel, head size 64.
+#include "chunk_launch.cuh"
+
+namespace la {
+cudaError_t chunk_run_d64(const chunk::Launch& L, cudaStream_t st) { return chunk::run_d<64>(L, st); }
+}  // namespace la

@@ -1,0 +1,306 @@
+// chunk_host.cu -- host orchestration of the tensor-core path: sequence
+// segmentation, workspace layout, tensor maps, and the two small CUDA-core
+// kernels between the passes (segment-state scan for the causal form,
+// segment-state sum for the non-causal form).
+//
+// Causal, sequence split into P segments per (batch, kv head):
+//   pass 1 (state mode, segments 0..P-2): dS_p, dZ_p, log decay of segment p
+//   scan: start state of segment p = decay-weighted prefix of dS over p' < p,
+//         starting from the caller's initial state
+//   pass 2 (causal mode, all segments): outputs, final state from segment P-1
+// Non-causal: pass 1 over all segments, sum, then the read-out pass.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "chunk_args.h"
+#include "kernels.h"
+#include "tma_host.h"
+
+namespace la {
+
+__device__ unsigned int g_chunk_err = 0;
+
+namespace {
+
+constexpr int kMaxDev = 64;
+constexpr size_t kAlign = 256;
+size_t round_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+struct DevInfo {
+    int sms = 0;
+    unsigned* err = nullptr;
+};
+
+bool dev_info(DevInfo* out) {
+    static std::mutex mu;
+    static DevInfo info[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!info[dev].err) {
+        int sms = 0;
+        void* p = nullptr;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        if (cudaGetSymbolAddress(&p, g_chunk_err) != cudaSuccess) return false;
+        info[dev].sms = sms;
+        info[dev].err = static_cast<unsigned*>(p);
+    }
+    *out = info[dev];
+    return true;
+}
+
+struct Plan {
+    int nseg, cps;
+};
+
+// Enough (batch, kv head, segment) tiles for one CTA per SM, never more
+// segments than chunks.
+Plan plan_segments(int64_t BH, int nchunks, int sms) {
+    int nseg = BH >= sms ? 1 : std::max<int>(1, static_cast<int>(sms / BH));
+    nseg = std::min(nseg, nchunks);
+    const int cps = (nchunks + nseg - 1) / nseg;
+    return {(nchunks + cps - 1) / cps, cps};
+}
+
+struct WsLayout {
+    size_t S_seg = 0, Z_seg = 0, G_seg = 0, S_tot = 0, Z_tot = 0, total = 0;
+};
+
+WsLayout ws_layout(const Problem& P, bool causal, int nseg) {
+    WsLayout w;
+    const size_t BH = static_cast<size_t>(P.B) * P.Hkv;
+    const size_t D = P.Dk;
+    size_t off = 0;
+    if (causal && nseg <= 1) return w;
+    w.S_seg = off;
+    off += round_up(BH * nseg * D * D * sizeof(float));
+    w.Z_seg = off;
+    off += round_up(BH * nseg * D * sizeof(float));
+    w.G_seg = off;
+    off += round_up(BH * nseg * sizeof(float));
+    if (!causal) {
+        w.S_tot = off;
+        off += round_up(BH * D * D * sizeof(float));
+        w.Z_tot = off;
+        off += round_up(BH * D * sizeof(float));
+    }
+    w.total = off;
+    return w;
+}
+
+// Start state of every segment, in place over the per-segment increments:
+// slot p holds dS_p on entry and S_start(p) on exit.
+__global__ void segment_scan_kernel(float* S_seg, float* Z_seg, const float* G_seg, const float* S0, const float* Z0,
+                                    int nseg, int D, int norm, int gated) {
+    const int64_t bh = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int DD = D * D;
+    if (e < DD) {
+        float run = S0 ? S0[bh * DD + e] : 0.f;
+        for (int p = 0; p < nseg; ++p) {
+            float* slot = S_seg + (bh * nseg + p) * DD + e;
+            const float d = p < nseg - 1 ? *slot : 0.f;
+            *slot = run;
+            if (p < nseg - 1) run = (gated ? expf(G_seg[bh * nseg + p]) : 1.f) * run + d;
+        }
+    }
+    if (norm && blockIdx.x == 0 && threadIdx.x < D) {
+        const int k = threadIdx.x;
+        float run = Z0 ? Z0[bh * D + k] : 0.f;
+        for (int p = 0; p < nseg; ++p) {
+            float* slot = Z_seg + (bh * nseg + p) * D + k;
+            const float d = p < nseg - 1 ? *slot : 0.f;
+            *slot = run;
+            run += d;
+        }
+    }
+}
+
+// Global state of the non-causal form: sum of the per-segment states in a
+// fixed order (deterministic).
+__global__ void segment_sum_kernel(const float* S_seg, const float* Z_seg, float* S_tot, float* Z_tot, int nseg,
+                                   int D, int norm) {
+    const int64_t bh = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int DD = D * D;
+    if (e < DD) {
+        float acc = 0.f;
+        for (int p = 0; p < nseg; ++p) acc += S_seg[(bh * nseg + p) * DD + e];
+        S_tot[bh * DD + e] = acc;
+    }
+    if (norm && blockIdx.x == 0 && threadIdx.x < D) {
+        float acc = 0.f;
+        for (int p = 0; p < nseg; ++p) acc += Z_seg[(bh * nseg + p) * D + threadIdx.x];
+        Z_tot[bh * D + threadIdx.x] = acc;
+    }
+}
+
+// (D, H, T, B) view of an activation; loads use 64 x 64 boxes with the
+// 128-byte swizzle, stores a plain (D, 1, 64, 1) box.
+bool act_map(CUtensorMap* m, const void* base, int D, int H, int64_t T, int64_t B, bool store, bool f32) {
+    const uint64_t es = f32 ? 4 : 2;
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t str[3] = {D * es, (uint64_t)H * D * es, (uint64_t)T * H * D * es};
+    const uint32_t box_load[4] = {64, 1, 64, 1};
+    const uint32_t box_store[4] = {(uint32_t)D, 1, 64, 1};
+    return make_tensor_map(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, 4, dims,
+                           str, store ? box_store : box_load,
+                           store ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+cudaError_t run(const chunk::Launch& L, int D, cudaStream_t st) {
+    return D == 64 ? chunk_run_d64(L, st) : chunk_run_d128(L, st);
+}
+
+chunk::Launch base_launch(const Problem& P, int mode, const DevInfo& di) {
+    chunk::Launch L;
+    memset(&L, 0, sizeof(L));
+    L.mode = mode;
+    L.norm = P.norm != 0;
+    L.gated = P.gated != 0;
+    L.splitk = P.gated || P.fmap == LA_FMAP_ELU_PLUS_ONE;
+    L.out_bf16 = P.out_bf16 != 0;
+    chunk::Args& a = L.args;
+    a.B = (int)P.B;
+    a.T = (int)P.T;
+    a.Hq = P.Hq;
+    a.Hkv = P.Hkv;
+    a.G = P.G;
+    a.fmap = P.fmap;
+    a.eps = P.eps;
+    a.scale = P.scale;
+    a.err = di.err;
+    return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+bool chunk_supported(const Problem& P) {
+    if (!P.io_bf16 || P.Dk != P.Dv || (P.Dk != 64 && P.Dk != 128)) return false;
+    if (P.T < 1 || P.T > 0x7fffffffLL - 64 || P.B > 0x7fffffffLL) return false;
+    DevInfo di;
+    return dev_info(&di);
+}
+
+bool chunk_pointers_ok(const void* q, const void* k, const void* v, const void* y) {
+    return aligned16(q) && aligned16(k) && aligned16(v) && aligned16(y);
+}
+
+size_t chunk_workspace_bytes(const Problem& P, bool causal) {
+    DevInfo di;
+    if (!dev_info(&di)) return 0;
+    const int nchunks = (int)((P.T + 63) / 64);
+    const Plan pl = plan_segments((int64_t)P.B * P.Hkv, nchunks, di.sms);
+    return ws_layout(P, causal, pl.nseg).total;
+}
+
+cudaError_t chunk_causal(const Problem& P, const void* q, const void* k, const void* v, const void* decay,
+                         const float* S0, const float* Z0, void* y, float* S_out, float* Z_out, void* ws,
+                         cudaStream_t st) {
+    DevInfo di;
+    if (!dev_info(&di)) return cudaErrorInvalidDevice;
+    const int D = P.Dk;
+    const int64_t BH = (int64_t)P.B * P.Hkv;
+    const int nchunks = (int)((P.T + 63) / 64);
+    const Plan pl = plan_segments(BH, nchunks, di.sms);
+    const WsLayout wl = ws_layout(P, true, pl.nseg);
+    char* w = static_cast<char*>(ws);
+
+    chunk::Launch L = base_launch(P, chunk::kCausal, di);
+    L.args.cps = pl.cps;
+    L.args.nseg = pl.nseg;
+    L.args.decay = static_cast<const __nv_bfloat16*>(decay);
+    if (!act_map(&L.mq, q, D, P.Hq, P.T, P.B, false, false) || !act_map(&L.mk, k, D, P.Hkv, P.T, P.B, false, false) ||
+        !act_map(&L.mv, v, D, P.Hkv, P.T, P.B, false, false) ||
+        !act_map(&L.my, y, D, P.Hq, P.T, P.B, true, !P.out_bf16))
+        return cudaErrorInvalidValue;
+
+    if (pl.nseg > 1) {
+        float* S_seg = reinterpret_cast<float*>(w + wl.S_seg);
+        float* Z_seg = reinterpret_cast<float*>(w + wl.Z_seg);
+        float* G_seg = reinterpret_cast<float*>(w + wl.G_seg);
+        chunk::Launch Ls = L;
+        Ls.mode = chunk::kState;
+        Ls.grid = dim3((unsigned)BH, (unsigned)(pl.nseg - 1));
+        Ls.args.S_dst = S_seg;
+        Ls.args.Z_dst = P.norm ? Z_seg : nullptr;
+        Ls.args.G_dst = G_seg;
+        cudaError_t e = run(Ls, D, st);
+        if (e != cudaSuccess) return e;
+        const int DD = D * D;
+        segment_scan_kernel<<<dim3((DD + 255) / 256, (unsigned)BH), 256, 0, st>>>(S_seg, Z_seg, G_seg, S0, Z0, pl.nseg,
+                                                                                D, P.norm, P.gated);
+        note_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        L.args.S_seg = S_seg;
+        L.args.Z_seg = P.norm ? Z_seg : nullptr;
+    } else {
+        L.args.S_init = S0;
+        L.args.Z_init = P.norm ? Z0 : nullptr;
+    }
+    L.grid = dim3((unsigned)BH, (unsigned)pl.nseg);
+    L.args.S_dst = S_out;
+    L.args.Z_dst = P.norm ? Z_out : nullptr;
+    return run(L, D, st);
+}
+
+cudaError_t chunk_noncausal(const Problem& P, const void* q, const void* k, const void* v, void* y, void* ws,
+                            cudaStream_t st) {
+    DevInfo di;
+    if (!dev_info(&di)) return cudaErrorInvalidDevice;
+    const int D = P.Dk;
+    const int64_t BH = (int64_t)P.B * P.Hkv;
+    const int nchunks = (int)((P.T + 63) / 64);
+    const Plan pl = plan_segments(BH, nchunks, di.sms);
+    const WsLayout wl = ws_layout(P, false, pl.nseg);
+    char* w = static_cast<char*>(ws);
+    float* S_seg = reinterpret_cast<float*>(w + wl.S_seg);
+    float* Z_seg = reinterpret_cast<float*>(w + wl.Z_seg);
+    float* S_tot = reinterpret_cast<float*>(w + wl.S_tot);
+    float* Z_tot = reinterpret_cast<float*>(w + wl.Z_tot);
+
+    chunk::Launch L = base_launch(P, chunk::kState, di);
+    L.gated = false;
+    L.args.cps = pl.cps;
+    L.args.nseg = pl.nseg;
+    if (!act_map(&L.mq, q, D, P.Hq, P.T, P.B, false, false) || !act_map(&L.mk, k, D, P.Hkv, P.T, P.B, false, false) ||
+        !act_map(&L.mv, v, D, P.Hkv, P.T, P.B, false, false) ||
+        !act_map(&L.my, y, D, P.Hq, P.T, P.B, true, !P.out_bf16))
+        return cudaErrorInvalidValue;
+    L.grid = dim3((unsigned)BH, (unsigned)pl.nseg);
+    L.args.S_dst = S_seg;
+    L.args.Z_dst = P.norm ? Z_seg : nullptr;
+    cudaError_t e = run(L, D, st);
+    if (e != cudaSuccess) return e;
+    const int DD = D * D;
+    segment_sum_kernel<<<dim3((DD + 255) / 256, (unsigned)BH), 256, 0, st>>>(S_seg, Z_seg, S_tot, Z_tot, pl.nseg, D,
+                                                                           P.norm);
+    note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    chunk::Launch La = L;
+    La.mode = chunk::kApply;
+    La.args.S_init = S_tot;
+    La.args.Z_init = P.norm ? Z_tot : nullptr;
+    La.args.S_dst = nullptr;
+    La.args.Z_dst = nullptr;
+    La.grid = dim3((unsigned)BH, (unsigned)pl.nseg);
+    return run(La, D, st);
+}
+
+unsigned chunk_device_error(bool reset) {
+    DevInfo di;
+    if (!dev_info(&di)) return 0;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, di.err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ~0u;
+    if (reset && v) {
+        unsigned z = 0;
+        cudaMemcpy(di.err, &z, sizeof(z), cudaMemcpyHostToDevice);
+    }
+    return v;
+}
+
+}  // namespace la

@@ -15,6 +15,18 @@ cudaError_t recurrent_causal(const Problem& P, const void* q, const void* k, con
 cudaError_t recurrent_noncausal(const Problem& P, const void* q, const void* k, const void* v,
                                 void* y, float* S_ws, float* Z_ws, cudaStream_t st);
 
+// Tensor-core chunk path (chunk_host.cu): bf16 inputs, Dk == Dv in {64, 128}.
+bool chunk_supported(const Problem& P);
+bool chunk_pointers_ok(const void* q, const void* k, const void* v, const void* y);
+size_t chunk_workspace_bytes(const Problem& P, bool causal);
+cudaError_t chunk_causal(const Problem& P, const void* q, const void* k, const void* v, const void* decay,
+                         const float* S0, const float* Z0, void* y, float* S_out, float* Z_out, void* ws,
+                         cudaStream_t st);
+cudaError_t chunk_noncausal(const Problem& P, const void* q, const void* k, const void* v, void* y, void* ws,
+                            cudaStream_t st);
+// Reads (and optionally clears) the error word of the bounded waits; 0 = none.
+unsigned chunk_device_error(bool reset);
+
 // Decode step (decode.cu).
 bool decode_supported(const Problem& P);
 cudaError_t decode_step(const Problem& P, const void* q, const void* k, const void* v,

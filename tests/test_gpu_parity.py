@@ -28,6 +28,9 @@ def _built():
     from kernelized_linear_attention_02_gb300 import build
     build.build()
     la.lib()
+    la.la_device_error(reset=True)
+    yield
+    assert la.la_device_error(reset=True) == 0, "a tensor-core kernel gave up on a bounded wait"
 
 
 def rand(shape, seed, dtype, std=1.0):
