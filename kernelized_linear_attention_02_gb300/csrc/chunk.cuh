@@ -29,8 +29,16 @@
 // Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-5 operand converters (feature map, hi/lo splits, Z, state
 // hi/lo in TMEM), warps 6-9 epilogue (masking of the scores, output
-// normalisation, TMA store).  Every wait is bounded (mbar_wait) and reports
-// a code in *err instead of hanging.
+// normalisation and store).  Every wait is bounded and reports a code in
+// *err instead of hanging.
+//
+// Pipeline per chunk i (G query heads per kv head):
+//   converter: S(i) [state hi/lo, after the update of chunk i-1], the query
+//              heads of chunk i beyond the ring depth, then the feature maps
+//              of chunk i+1 (keys, first query heads) ahead of time;
+//   MMA:       per head: scores, read-out with S_prev; after the last
+//              head's read-out the state update, then the intra term;
+// so the only loop-carried chain is S(i) -> read-out(i) -> update(i) -> S(i+1).
 //
 // Modes: kCausal (outputs + carried state), kState (only the state update
 // over a segment, for the two-pass sequence split and the non-causal
@@ -39,6 +47,7 @@
 
 #include "chunk_args.h"
 #include "common.cuh"
+#include "trace.cuh"
 #include "umma.cuh"
 
 namespace la {
@@ -49,16 +58,14 @@ using namespace umma;
 constexpr int kC = 64;  // tokens per chunk
 constexpr int kThreads = 320;
 constexpr int kConvWarp0 = 2, kEpiWarp0 = 6;
-constexpr int kBarConv = 1, kBarEpi = 2;  // named barriers (0 is __syncthreads)
 
 template <int D, int MODE, bool NORM, bool SPLITK, bool GATED, bool OUT_BF16>
 struct Cfg {
     static constexpr bool kHasKV = MODE != kApply;
     static constexpr bool kHasQ = MODE != kState;
     static constexpr int kTile = D * 128;  // 64 rows x D bf16 (D/64 swizzled blocks of 8 KB)
-    static constexpr int kZr = D * 16;     // 8 rows x D bf16
-    static constexpr int kOutBytes = OUT_BF16 ? 2 : 4;
-    // per KV stage: Kb | Kd (gated) | Klo (split) | Vb | Zr | G (256 B, padded)
+    static constexpr int kZr = D * 16;     // 8 rows x D bf16: [Z_hi; Z_lo; 0 x 6]
+    // per KV stage: Kb | Kd (gated) | Klo (split) | Vb | Zr (normalizer) | G (256 B, padded)
     static constexpr int kOffKd = kTile;
     static constexpr int kOffKlo = kOffKd + (GATED ? kTile : 0);
     static constexpr int kOffVb = kOffKlo + (SPLITK ? kTile : 0);
@@ -66,18 +73,16 @@ struct Cfg {
     static constexpr int kOffG = kOffZr + (NORM ? kZr : 0);
     static constexpr int kKvStage = kHasKV ? kOffG + 1024 : 0;
     static constexpr int kQStage = kHasQ ? kTile * (GATED ? 2 : 1) : 0;
-    static constexpr int kAT = MODE == kCausal ? 2 * 8192 : 0;  // hi + lo, one 64 x 64 block each
-    static constexpr int kYStage = kHasQ ? kC * D * kOutBytes : 0;
-    static constexpr int kZrApply = MODE == kApply ? kZr : 0;
-    static constexpr int kMisc = 4096;  // den, partial Z sums, barriers
-    static constexpr int bytes(int nkv, int nq, int ny) {
-        return 1024 + nkv * kKvStage + nq * kQStage + 2 * kAT + ny * kYStage + kZrApply + kMisc;
+    static constexpr int kAT = MODE == kCausal ? 2 * 8192 : 0;  // masked scores hi + lo, 64 x 64 each
+    static constexpr int kZrApply = (MODE == kApply && NORM) ? kZr : 0;
+    static constexpr int kMisc = 12 * 1024;  // 1/den ring, partial Z sums, barriers
+    static constexpr int bytes(int nkv, int nq) {
+        return 1024 + nkv * kKvStage + nq * kQStage + kAT + kZrApply + kMisc;
     }
     static constexpr int kLimit = 227 * 1024;
-    static constexpr int kNKV = kHasKV ? (bytes(2, kHasQ ? 1 : 0, kHasQ ? 1 : 0) <= kLimit ? 2 : 1) : 0;
-    static constexpr int kNY = kHasQ ? (bytes(kNKV, 2, 2) <= kLimit ? 2 : 1) : 0;
-    static constexpr int kNQ = kHasQ ? (bytes(kNKV, 2, kNY) <= kLimit ? 2 : 1) : 0;
-    static constexpr int kSmem = bytes(kNKV, kNQ, kNY);
+    static constexpr int kNKV = kHasKV ? (bytes(2, kHasQ ? 1 : 0) <= kLimit ? 2 : 1) : 0;
+    static constexpr int kNQ = kHasQ ? (bytes(kNKV, 2) <= kLimit ? 2 : 1) : 0;
+    static constexpr int kSmem = bytes(kNKV, kNQ);
     static_assert(kSmem <= kLimit, "shared memory budget");
     // TMEM columns
     static constexpr uint32_t kColS = 0;           // S^T fp32: D columns, lanes = value rows
@@ -87,25 +92,42 @@ struct Cfg {
     static constexpr uint32_t kColY = 2 * D + 160; // Y^T: 64 columns
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kColY + 64 <= kTmemCols, "TMEM budget");
+    // vectorised tile passes: 16-byte chunks, 128 threads
+    static constexpr int kCPR = D / 8;           // chunks per 64 x D tile row
+    static constexpr int kRowStep = 128 / kCPR;  // rows covered by one pass of 128 threads
+    static constexpr int kPer = 64 / kRowStep;   // chunks per thread per tile
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// element (row, k) of a [64 rows][D] K-major swizzled bf16 tile
-template <int D>
-__device__ __forceinline__ uint32_t tile_off(int row, int k) {
-    return static_cast<uint32_t>((k >> 6) * 8192) + sw128_offset(row, (k & 63) * 2);
+__device__ __forceinline__ void bf8_to_f(const uint4& u, float (&f)[8]) {
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __bfloat1622float2(p[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
 }
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ uint4 f_to_bf8(const float (&f)[8]) {
+    return make_uint4(bf2_bits(__floats2bfloat162_rn(f[0], f[1])), bf2_bits(__floats2bfloat162_rn(f[2], f[3])),
+                      bf2_bits(__floats2bfloat162_rn(f[4], f[5])), bf2_bits(__floats2bfloat162_rn(f[6], f[7])));
 }
-__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-    hi = __float2bfloat16_rn(x);
-    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), for a pair
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    hi = bf2_bits(h);
+    lo = bf2_bits(__floats2bfloat162_rn(x0 - hf.x, x1 - hf.y));
+}
+__device__ __forceinline__ void split8(const float (&f)[8], uint4& hi, uint4& lo) {
+    split2(f[0], f[1], hi.x, lo.x);
+    split2(f[2], f[3], hi.y, lo.y);
+    split2(f[4], f[5], hi.z, lo.z);
+    split2(f[6], f[7], hi.w, lo.w);
 }
 __device__ __forceinline__ __nv_bfloat16& bf_at(uint8_t* base, uint32_t off) {
     return *reinterpret_cast<__nv_bfloat16*>(base + off);
@@ -113,21 +135,21 @@ __device__ __forceinline__ __nv_bfloat16& bf_at(uint8_t* base, uint32_t off) {
 
 template <int D, int MODE, bool NORM, bool SPLITK, bool GATED, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_kernel(const Args a, const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                 const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapY) {
+    chunk_kernel(const __grid_constant__ Args a, const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                 const __grid_constant__ CUtensorMap mapV) {
     using Cf = Cfg<D, MODE, NORM, SPLITK, GATED, OUT_BF16>;
-    constexpr int NKV = Cf::kNKV, NQ = Cf::kNQ, NY = Cf::kNY;
+    constexpr int NKV = Cf::kNKV, NQ = Cf::kNQ;
+    constexpr int NKV1 = NKV ? NKV : 1, NQ1 = NQ ? NQ : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* kv_base = sm;
     uint8_t* q_base = kv_base + NKV * Cf::kKvStage;
     uint8_t* at_base = q_base + NQ * Cf::kQStage;
-    uint8_t* y_base = at_base + 2 * Cf::kAT;
-    uint8_t* zr_apply = y_base + NY * Cf::kYStage;
+    uint8_t* zr_apply = at_base + Cf::kAT;
     float* misc = reinterpret_cast<float*>(zr_apply + Cf::kZrApply);
-    float* den_s = misc;             // [2][64]
-    float* zpart = misc + 128;       // [2][128]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + 512);
+    float* inv_den = misc;           // [4][64] scale / den of the last four items
+    float* zpart = misc + 256;       // [2][1024] partial column sums of phi(K)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + 256 + 2048);
     uint64_t* full_kv = bars;        // [2]
     uint64_t* empty_kv = bars + 2;   // [2]
     uint64_t* conv_kv = bars + 4;    // [2]
@@ -136,24 +158,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* conv_q = bars + 10;    // [2]
     uint64_t* a_full = bars + 12;    // [2]
     uint64_t* a_empty = bars + 14;   // [2]
-    uint64_t* at_full = bars + 16;   // [2]
-    uint64_t* at_empty = bars + 18;  // [2]
-    uint64_t* y_full = bars + 20;
-    uint64_t* y_empty = bars + 21;
-    uint64_t* state_ready = bars + 22;
-    uint64_t* state_done = bars + 23;
-    uint64_t* conv_group = bars + 24;  // barrier among the four converter warps
-    uint64_t* epi_group = bars + 25;   // barrier among the four epilogue warps
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
+    uint64_t* at_full = bars + 16;
+    uint64_t* at_empty = bars + 17;
+    uint64_t* y_full = bars + 18;
+    uint64_t* y_empty = bars + 19;
+    uint64_t* state_ready = bars + 20;
+    uint64_t* state_done = bars + 21;
+    uint64_t* conv_group = bars + 22;  // barrier among the four converter warps
+    uint64_t* epi_group = bars + 23;   // barrier among the four epilogue warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+#ifdef LA_TRACE
+    unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 25);
+    if (threadIdx.x < 4) la_trace_ctr[threadIdx.x] = 0;
+#endif
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x;
     const int seg = blockIdx.y;
-    const int b = bh / a.Hkv, hk = bh - b * a.Hkv;
-    const int nchunks = (a.T + kC - 1) / kC;
+    // Argument fields in registers: the role code below runs in lambdas that
+    // capture by reference, and reading the parameter block through its
+    // address inside hot loops would be a long-latency load per use.
+    const int T = a.T, Hq = a.Hq, Hkv = a.Hkv, G = a.G, nseg = a.nseg;
+    const int fmap = a.fmap;
+    const float eps = a.eps, scale = a.scale;
+    const __nv_bfloat16* __restrict__ decay = a.decay;
+    void* const yout = a.y;
+    const int b = bh / Hkv, hk = bh - b * Hkv;
+    const int nchunks = (T + kC - 1) / kC;
     const int c_begin = seg * a.cps;
     const int nck = min(nchunks, c_begin + a.cps) - c_begin;
-    const int G = a.G;
 
     auto Kb = [&](int s) { return kv_base + s * Cf::kKvStage; };
     auto Kd = [&](int s) { return kv_base + s * Cf::kKvStage + Cf::kOffKd; };
@@ -163,9 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto Gc = [&](int s) { return reinterpret_cast<float*>(kv_base + s * Cf::kKvStage + Cf::kOffG); };
     auto Qb = [&](int s) { return q_base + s * Cf::kQStage; };
     auto Qd = [&](int s) { return q_base + s * Cf::kQStage + Cf::kTile; };
-    auto ATh = [&](int s) { return at_base + s * Cf::kAT; };
-    auto ATl = [&](int s) { return at_base + s * Cf::kAT + 8192; };
-    auto Ys = [&](int s) { return y_base + s * Cf::kYStage; };
+    uint8_t* ATh = at_base;
+    uint8_t* ATl = at_base + 8192;
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -177,9 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&conv_q[i], 4);
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], 4);
-            mbar_init(&at_full[i], 4);
-            mbar_init(&at_empty[i], 1);
         }
+        mbar_init(at_full, 4);
+        mbar_init(at_empty, 1);
         mbar_init(y_full, 1);
         mbar_init(y_empty, 4);
         mbar_init(state_ready, 4);
@@ -198,24 +230,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch(&mapK);
             tma_prefetch(&mapV);
         }
-        if (Cf::kHasQ) tma_prefetch(&mapY);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) LA_TR(0, 0, 0);
     const uint32_t tmem = *tmem_slot;
     unsigned* err = a.err;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // loads in the order the converters consume: K/V of chunk i, then its heads
         if (lane == 0) {
             bool ok = true;
             for (int i = 0; i < nck && ok; ++i) {
                 const int t0 = (c_begin + i) * kC;
                 if (Cf::kHasKV) {
-                    const int s = NKV ? i % NKV : 0;
-                    if (i >= NKV) ok = mbar_wait(&empty_kv[s], ((i / (NKV ? NKV : 1)) & 1) ^ 1, err, kErrEmptyKV);
+                    const int s = i % NKV1;
+                    if (i >= NKV) ok = mbar_wait(&empty_kv[s], ((i / NKV1) & 1) ^ 1, err, kErrEmptyKV);
                     if (!ok) break;
+                    LA_TR(0, 1, i);
                     mbar_arrive_expect_tx(&full_kv[s], 2 * Cf::kTile);
                     for (int kb = 0; kb < D / 64; ++kb) {
                         tma_load_4d(Kb(s) + kb * 8192, &mapK, &full_kv[s], kb * 64, hk, t0, b);
@@ -224,9 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (Cf::kHasQ) {
                     for (int r = 0; r < G && ok; ++r) {
-                        const int n = i * G + r, s = n % (NQ ? NQ : 1);
-                        if (n >= NQ) ok = mbar_wait(&empty_q[s], ((n / (NQ ? NQ : 1)) & 1) ^ 1, err, kErrEmptyQ);
+                        const int n = i * G + r, s = n % NQ1;
+                        if (n >= NQ) ok = mbar_wait(&empty_q[s], ((n / NQ1) & 1) ^ 1, err, kErrEmptyQ);
                         if (!ok) break;
+                        LA_TR(0, 2, n);
                         mbar_arrive_expect_tx(&full_q[s], Cf::kTile);
                         for (int kb = 0; kb < D / 64; ++kb)
                             tma_load_4d(Qb(s) + kb * 8192, &mapQ, &full_q[s], kb * 64, hk * G + r, t0, b);
@@ -245,331 +280,396 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t id_state = idesc_bf16(D, D, true, true);
             const uint32_t tS = tmem + Cf::kColS, tHi = tmem + Cf::kColHi, tLo = tmem + Cf::kColLo;
             const uint32_t tY = tmem + Cf::kColY;
+
+            // state update of chunk i: S^T += V^T . Kd (+ V^T . Kd_lo)
+            auto issue_state_update = [&](int s) {
+                uint8_t* khi = GATED ? Kd(s) : Kb(s);
+                for (int ks = 0; ks < kC / 16; ++ks) {
+                    const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
+                    mma_ss(tS, av, sdesc_sw128(smem_u32(khi + ks * 2048), 8192, 1024), id_state, 1);
+                    if (SPLITK) mma_ss(tS, av, sdesc_sw128(smem_u32(Klo(s) + ks * 2048), 8192, 1024), id_state, 1);
+                }
+            };
+
             for (int i = 0; i < nck && ok; ++i) {
-                const int s = NKV ? i % NKV : 0;
+                const int s = i % NKV1;
                 if (Cf::kHasKV) {
-                    ok = mbar_wait(&conv_kv[s], (i / (NKV ? NKV : 1)) & 1, err, kErrConvKV);
+                    ok = mbar_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
                     if (!ok) break;
                     tc_fence_after();
+                    LA_TR(1, 1, i);
                 }
-                if (Cf::kHasQ) {
-                    for (int r = 0; r < G && ok; ++r) {
-                        const int n = i * G + r, sq = n % (NQ ? NQ : 1), ab = n & 1;
-                        ok = mbar_wait(&conv_q[sq], (n / (NQ ? NQ : 1)) & 1, err, kErrConvQ);
-                        if (!ok) break;
-                        tc_fence_after();
-                        uint8_t* qop = GATED ? Qd(sq) : Qb(sq);  // operand of the inter read-out
-                        const uint32_t tA = tmem + Cf::kColA + 80 * ab;
-                        if (MODE == kCausal || NORM) {
-                            if (n >= 2) {
-                                ok = mbar_wait(&a_empty[ab], ((n >> 1) & 1) ^ 1, err, kErrAEmpty);
-                                if (!ok) break;
-                                tc_fence_after();
-                            }
-                            if (MODE == kCausal) {
-                                for (int ks = 0; ks < D / 16; ++ks) {
-                                    const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
-                                    mma_ss(tA, sdesc_sw128(smem_u32(Qb(sq) + ko), 16, 1024),
-                                           sdesc_sw128(smem_u32(Kb(s) + ko), 16, 1024), id_scores, ks > 0);
-                                }
-                            }
-                            if (NORM) {
-                                for (int ks = 0; ks < D / 16; ++ks) {
-                                    const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
-                                    const uint32_t zo = (ks >> 2) * 1024 + (ks & 3) * 32;
-                                    mma_ss(tA + 64, sdesc_sw128(smem_u32(Qb(sq) + ko), 16, 1024),
-                                           sdesc_sw128(smem_u32(Zr(s) + zo), 16, 1024), id_qz, ks > 0);
-                                }
-                            }
-                            mma_commit(&a_full[ab]);
-                        }
-                        if (r == 0 && (MODE == kCausal || i == 0)) {
-                            ok = mbar_wait(state_ready, MODE == kCausal ? (i & 1) : 0, err, kErrStateReady);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        if (n >= 1) {
-                            ok = mbar_wait(y_empty, (n - 1) & 1, err, kErrYEmpty);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        // inter: Y^T = S_prev^T(hi + lo) . Q^T
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
-                            const uint64_t bq = sdesc_sw128(smem_u32(qop + ko), 16, 1024);
-                            mma_ts(tY, tHi + ks * 8, bq, id_inter, ks > 0);
-                            mma_ts(tY, tLo + ks * 8, bq, id_inter, 1);
-                        }
-                        mma_commit(&empty_q[sq]);
-                        if (MODE == kCausal) {
-                            ok = mbar_wait(&at_full[ab], (n >> 1) & 1, err, kErrATFull);
-                            if (!ok) break;
-                            tc_fence_after();
-                            // intra: Y^T += V^T . A^T (hi + lo)
-                            for (int ks = 0; ks < kC / 16; ++ks) {
-                                const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                                mma_ss(tY, av, sdesc_sw128(smem_u32(ATh(ab) + ks * 32), 16, 1024), id_intra, 1);
-                                mma_ss(tY, av, sdesc_sw128(smem_u32(ATl(ab) + ks * 32), 16, 1024), id_intra, 1);
-                            }
-                            mma_commit(&at_empty[ab]);
-                        }
-                        mma_commit(y_full);
-                    }
-                    if (!ok) break;
-                }
-                if (Cf::kHasKV) {
-                    if (MODE == kState && (GATED || i == 0)) {
-                        // state mode: the converters publish the (decayed) state before each update
+                if (MODE == kState) {
+                    if (GATED || i == 0) {
+                        // the converters publish the (decayed) state before each update
                         ok = mbar_wait(state_ready, i & 1, err, kErrStateReady);
                         if (!ok) break;
                         tc_fence_after();
                     }
-                    // state update: S^T += V^T . Kd (+ V^T . Kd_lo)
-                    uint8_t* khi = GATED ? Kd(s) : Kb(s);
-                    for (int ks = 0; ks < kC / 16; ++ks) {
-                        const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                        mma_ss(tS, av, sdesc_sw128(smem_u32(khi + ks * 2048), 8192, 1024), id_state, 1);
-                        if (SPLITK)
-                            mma_ss(tS, av, sdesc_sw128(smem_u32(Klo(s) + ks * 2048), 8192, 1024), id_state, 1);
-                    }
+                    issue_state_update(s);
                     // the non-gated state pass has no per-chunk hand-off: one phase at the end
-                    if (MODE == kCausal || GATED || i == nck - 1) mma_commit(state_done);
+                    if (GATED || i == nck - 1) mma_commit(state_done);
                     mma_commit(&empty_kv[s]);
+                    continue;
                 }
+                for (int r = 0; r < G && ok; ++r) {
+                    const int n = i * G + r, sq = n % NQ1, ab = n & 1;
+                    ok = mbar_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ);
+                    if (!ok) break;
+                    tc_fence_after();
+                    LA_TR(1, 2, n);
+                    uint8_t* qop = GATED ? Qd(sq) : Qb(sq);  // operand of the inter read-out
+                    const uint32_t tA = tmem + Cf::kColA + 80 * ab;
+                    if (MODE == kCausal || NORM) {
+                        if (n >= 2) {
+                            ok = mbar_wait(&a_empty[ab], ((n >> 1) & 1) ^ 1, err, kErrAEmpty);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        if (MODE == kCausal) {
+                            for (int ks = 0; ks < D / 16; ++ks) {
+                                const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
+                                mma_ss(tA, sdesc_sw128(smem_u32(Qb(sq) + ko), 16, 1024),
+                                       sdesc_sw128(smem_u32(Kb(s) + ko), 16, 1024), id_scores, ks > 0);
+                            }
+                        }
+                        if (NORM) {
+                            for (int ks = 0; ks < D / 16; ++ks) {
+                                const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
+                                const uint32_t zo = (ks >> 2) * 1024 + (ks & 3) * 32;
+                                mma_ss(tA + 64, sdesc_sw128(smem_u32(Qb(sq) + ko), 16, 1024),
+                                       sdesc_sw128(smem_u32(Zr(s) + zo), 16, 1024), id_qz, ks > 0);
+                            }
+                        }
+                        mma_commit(&a_full[ab]);
+                        LA_TR(1, 3, n);
+                    }
+                    if (r == 0 && (MODE == kCausal || i == 0)) {
+                        ok = mbar_wait(state_ready, MODE == kCausal ? (i & 1) : 0, err, kErrStateReady);
+                        if (!ok) break;
+                        tc_fence_after();
+                        LA_TR(1, 4, i);
+                    }
+                    if (n >= 1) {
+                        ok = mbar_wait(y_empty, (n - 1) & 1, err, kErrYEmpty);
+                        if (!ok) break;
+                        tc_fence_after();
+                        LA_TR(1, 5, n);
+                    }
+                    // inter: Y^T = S_prev^T(hi + lo) . Q^T
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
+                        const uint64_t bq = sdesc_sw128(smem_u32(qop + ko), 16, 1024);
+                        mma_ts(tY, tHi + ks * 8, bq, id_inter, ks > 0);
+                        mma_ts(tY, tLo + ks * 8, bq, id_inter, 1);
+                    }
+                    mma_commit(&empty_q[sq]);
+                    LA_TR(1, 6, n);
+                    if (MODE == kCausal) {
+                        if (r == G - 1) {
+                            // every read-out of this chunk is issued: update the state now
+                            issue_state_update(s);
+                            mma_commit(state_done);
+                            LA_TR(1, 9, i);
+                        }
+                        ok = mbar_wait(at_full, n & 1, err, kErrATFull);
+                        if (!ok) break;
+                        tc_fence_after();
+                        LA_TR(1, 7, n);
+                        // intra: Y^T += V^T . A^T (hi + lo)
+                        for (int ks = 0; ks < kC / 16; ++ks) {
+                            const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
+                            mma_ss(tY, av, sdesc_sw128(smem_u32(ATh + ks * 32), 16, 1024), id_intra, 1);
+                            mma_ss(tY, av, sdesc_sw128(smem_u32(ATl + ks * 32), 16, 1024), id_intra, 1);
+                        }
+                        mma_commit(at_empty);
+                    }
+                    mma_commit(y_full);
+                    LA_TR(1, 8, n);
+                }
+                if (!ok) break;
+                if (Cf::kHasKV) mma_commit(&empty_kv[s]);
             }
         }
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------------ converters
+        constexpr int kCPR = Cf::kCPR, kRowStep = Cf::kRowStep, kPer = Cf::kPer;
         const int ct = tid - kConvWarp0 * 32;  // 0..127
         const int quad = warp & 3;             // TMEM lane quadrant of this warp
-        const int kcol = ct % D;               // feature column handled in tile passes
-        const int rgrp = ct / D;               // row group (D = 64: two groups of 32 rows)
-        constexpr int kRows = 64 * D / 128;    // rows per thread in tile passes
-        const int row0 = rgrp * kRows;
+        const int cc = ct % kCPR;              // 16-byte chunk column: features 8cc..8cc+7
+        const int rbase = ct / kCPR;           // rows rbase + kRowStep * m
+        const bool m64 = D == 64;
+        const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);  // value row of S^T in this lane
+        const bool vrow_ok = m64 ? lane < 16 : true;
         bool ok = true;
         uint32_t gphase = 0;
+        int zbuf = 0;
+        auto chunk_off = [&](int m) -> uint32_t {
+            const int row = rbase + kRowStep * m;
+            return static_cast<uint32_t>((cc >> 3) * 8192 + row * 128 + ((((cc & 7) ^ (row & 7))) << 4));
+        };
+        auto zr_off = [&](int row, int k) -> uint32_t {
+            return static_cast<uint32_t>((k >> 6) * 1024) + sw128_offset(row, (k & 63) * 2);
+        };
 
         // zero the constant rows 2..7 of every Z-row block
         if (NORM) {
             const int nzr = MODE == kApply ? 1 : NKV;
             for (int z = 0; z < nzr; ++z)
-                for (int e = ct; e < D * 8; e += 128) {
-                    const int row = e / D, k = e % D;
-                    if (row >= 2) bf_at(Zr(z), (k >> 6) * 1024 + sw128_offset(row, (k & 63) * 2)) = __float2bfloat16(0.f);
-                }
+                for (int e = ct; e < D * 6; e += 128) bf_at(Zr(z), zr_off(2 + e / D, e % D)) = __float2bfloat16(0.f);
         }
-        // start state -> S^T (fp32) in TMEM; Z in a register of thread k (rgrp 0)
-        const float* S_start = nullptr;
-        const float* Z_start = nullptr;
-        if (MODE == kCausal && a.S_seg) {
-            S_start = a.S_seg + ((size_t)bh * a.nseg + seg) * D * D;
-            Z_start = a.Z_seg ? a.Z_seg + ((size_t)bh * a.nseg + seg) * D : nullptr;
-        } else if (MODE != kState) {
-            S_start = a.S_init ? a.S_init + (size_t)bh * D * D : nullptr;
-            Z_start = a.Z_init ? a.Z_init + (size_t)bh * D : nullptr;
-        }
-        // TMEM row of this thread for a D-row accumulator (M = D): value index
-        const bool m64 = D == 64;
-        const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);
-        const bool vrow_ok = m64 ? lane < 16 : true;
+
+        // ---- start state -> S^T (fp32) in TMEM, Z -> register of thread k < D.
+        // Causal segment s > 0 folds the increments of segments 0..s-1 (from
+        // the state pass) onto the initial state, decay-weighted for gated.
+        const bool fold = MODE == kCausal && a.S_seg && seg > 0;
+        const float* S_start = MODE == kState ? nullptr : a.S_init;
         for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t r[32];
 #pragma unroll
-            for (int x = 0; x < 32; ++x)
-                r[x] = __float_as_uint((S_start && vrow_ok) ? S_start[(size_t)(c0 + x) * D + vrow] : 0.f);
+            for (int x = 0; x < 32; ++x) {
+                const size_t e = (size_t)(c0 + x) * D + vrow;
+                float run = (S_start && vrow_ok) ? S_start[(size_t)bh * D * D + e] : 0.f;
+                if (fold && vrow_ok)
+                    for (int p = 0; p < seg; ++p) {
+                        const float dS = a.S_seg[((size_t)bh * nseg + p) * D * D + e];
+                        run = GATED ? fmaf(__expf(a.G_seg[(size_t)bh * nseg + p]), run, dS) : run + dS;
+                    }
+                r[x] = __float_as_uint(run);
+            }
             tmem_st32(tmem_addr(tmem + Cf::kColS, quad * 32, c0), r);
         }
         tmem_st_wait();
-        float zreg = (NORM && Z_start && rgrp == 0) ? Z_start[kcol] : 0.f;
-        float gsum = 0.f;  // gated, state mode: total log decay of the segment
+        float zreg = 0.f;
+        if (NORM && ct < D && MODE != kState) {
+            zreg = a.Z_init ? a.Z_init[(size_t)bh * D + ct] : 0.f;
+            if (fold && a.Z_seg)
+                for (int p = 0; p < seg; ++p) zreg += a.Z_seg[((size_t)bh * nseg + p) * D + ct];
+        }
+        float gsum = 0.f;      // gated, state mode: total log decay of the segment
+        float gtot_cur = 0.f;  // gated: log decay of the chunk processed last by process_kv
 
-        // state hi/lo conversion (and, gated, decay of the fp32 state in place)
+        // ---- state hi/lo (and, gated, the decay of the fp32 state in place)
         auto convert_state = [&](float decay_mul, bool write_back) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem_addr(tmem + Cf::kColS, quad * 32, c0), r);
+            for (int c0 = 0; c0 < D; c0 += 64) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem_addr(tmem + Cf::kColS, quad * 32, c0), r0);
+                tmem_ld32(tmem_addr(tmem + Cf::kColS, quad * 32, c0 + 32), r1);
                 tmem_ld_wait();
-                reg_fence(r);
+                reg_fence(r0);
+                reg_fence(r1);
                 if (MODE != kState) {
-                    uint32_t hi[16], lo[16];
+                    uint32_t h0[16], l0[16], h1[16], l1[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
-                        const float f0 = __uint_as_float(r[2 * x]), f1 = __uint_as_float(r[2 * x + 1]);
-                        __nv_bfloat16 h0, l0, h1, l1;
-                        split_bf16(f0, h0, l0);
-                        split_bf16(f1, h1, l1);
-                        __nv_bfloat162 hh, ll;
-                        hh.x = h0; hh.y = h1;
-                        ll.x = l0; ll.y = l1;
-                        hi[x] = *reinterpret_cast<uint32_t*>(&hh);
-                        lo[x] = *reinterpret_cast<uint32_t*>(&ll);
+                        split2(__uint_as_float(r0[2 * x]), __uint_as_float(r0[2 * x + 1]), h0[x], l0[x]);
+                        split2(__uint_as_float(r1[2 * x]), __uint_as_float(r1[2 * x + 1]), h1[x], l1[x]);
                     }
-                    tmem_st16(tmem_addr(tmem + Cf::kColHi, quad * 32, c0 / 2), hi);
-                    tmem_st16(tmem_addr(tmem + Cf::kColLo, quad * 32, c0 / 2), lo);
+                    tmem_st16(tmem_addr(tmem + Cf::kColHi, quad * 32, c0 / 2), h0);
+                    tmem_st16(tmem_addr(tmem + Cf::kColHi, quad * 32, c0 / 2 + 16), h1);
+                    tmem_st16(tmem_addr(tmem + Cf::kColLo, quad * 32, c0 / 2), l0);
+                    tmem_st16(tmem_addr(tmem + Cf::kColLo, quad * 32, c0 / 2 + 16), l1);
                 }
                 if (write_back) {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * decay_mul);
-                    tmem_st32(tmem_addr(tmem + Cf::kColS, quad * 32, c0), r);
+                    for (int x = 0; x < 32; ++x) {
+                        r0[x] = __float_as_uint(__uint_as_float(r0[x]) * decay_mul);
+                        r1[x] = __float_as_uint(__uint_as_float(r1[x]) * decay_mul);
+                    }
+                    tmem_st32(tmem_addr(tmem + Cf::kColS, quad * 32, c0), r0);
+                    tmem_st32(tmem_addr(tmem + Cf::kColS, quad * 32, c0 + 32), r1);
                 }
             }
             tmem_st_wait();
         };
 
+        // ---- keys of chunk i: feature map (+ lo part), decayed keys, Z rows and sums
+        auto process_kv = [&](int i) -> bool {
+            const int s = i % NKV1;
+            const int t0 = (c_begin + i) * kC;
+            const int valid = min(kC, T - t0);
+            if (!warp_wait(&full_kv[s], (i / NKV1) & 1, err, kErrFullKV)) return false;
+            if (ct == 0) LA_TR(2, 1, i);
+            float* gc = Gc(s);
+            float gtot = 0.f;
+            if (GATED) {
+                // inclusive cumulative log decay inside the chunk (first converter warp)
+                if (ct < 32) {
+                    float g0 = 0.f, g1 = 0.f;
+                    const int j0 = 2 * ct, j1 = 2 * ct + 1;
+                    if (j0 < valid) g0 = __bfloat162float(decay[((size_t)b * T + t0 + j0) * Hkv + hk]);
+                    if (j1 < valid) g1 = __bfloat162float(decay[((size_t)b * T + t0 + j1) * Hkv + hk]);
+                    const float sum = g0 + g1;
+                    float incl = sum;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float t = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    gc[j0] = incl - sum + g0;
+                    gc[j1] = incl;
+                }
+                if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
+                gtot = gc[kC - 1];
+            }
+            const bool touch = GATED || SPLITK || NORM || fmap != LA_FMAP_NONE;
+            if (ct == 0) LA_TR(2, 7, i);
+            if (touch) {
+                uint4 in[kPer];
+#pragma unroll
+                for (int m = 0; m < kPer; ++m) in[m] = *reinterpret_cast<const uint4*>(Kb(s) + chunk_off(m));
+                float colsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int m = 0; m < kPer; ++m) {
+                    const int row = rbase + kRowStep * m;
+                    float f[8];
+                    bf8_to_f(in[m], f);
+                    uint4 hi, lo;
+                    if (GATED) {
+                        const float w = __expf(gtot - gc[row]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] *= w;
+                        split8(f, hi, lo);
+                        *reinterpret_cast<uint4*>(Kd(s) + chunk_off(m)) = hi;
+                        *reinterpret_cast<uint4*>(Klo(s) + chunk_off(m)) = lo;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = phi<true>(fmap, f[e], eps);
+                        if (fmap != LA_FMAP_NONE || SPLITK) {
+                            split8(f, hi, lo);
+                            if (fmap != LA_FMAP_NONE) *reinterpret_cast<uint4*>(Kb(s) + chunk_off(m)) = hi;
+                            if (SPLITK) *reinterpret_cast<uint4*>(Klo(s) + chunk_off(m)) = lo;
+                        }
+                        if (NORM && row < valid)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) colsum[e] += f[e];
+                    }
+                }
+                if (ct == 0) LA_TR(2, 8, i);
+                if (NORM) {
+                    // Z rows of this chunk hold Z_prev (hi, lo); then Z += column sums
+                    float* zp = zpart + zbuf * 1024;
+                    *reinterpret_cast<float4*>(zp + rbase * D + 8 * cc) =
+                        make_float4(colsum[0], colsum[1], colsum[2], colsum[3]);
+                    *reinterpret_cast<float4*>(zp + rbase * D + 8 * cc + 4) =
+                        make_float4(colsum[4], colsum[5], colsum[6], colsum[7]);
+                    if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
+                    if (ct == 0) LA_TR(2, 9, i);
+                    if (ct < D) {
+                        if (MODE != kState) {
+                            const __nv_bfloat16 h = __float2bfloat16_rn(zreg);
+                            bf_at(Zr(s), zr_off(0, ct)) = h;
+                            bf_at(Zr(s), zr_off(1, ct)) = __float2bfloat16_rn(zreg - __bfloat162float(h));
+                        }
+                        float add = 0.f;
+#pragma unroll
+                        for (int g = 0; g < kRowStep; ++g) add += zp[g * D + ct];
+                        zreg += add;
+                    }
+                    zbuf ^= 1;
+                }
+            }
+            gtot_cur = gtot;
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv_kv[s]);
+            if (ct == 0) LA_TR(2, 2, i);
+            return true;
+        };
+
+        // ---- query head item n (chunk i): feature map in place, or the decayed copy
+        auto process_q = [&](int i, int n) -> bool {
+            const int sq = n % NQ1;
+            if (!warp_wait(&full_q[sq], (n / NQ1) & 1, err, kErrFullQ)) return false;
+            if (ct == 0) LA_TR(2, 3, n);
+            if (fmap != LA_FMAP_NONE || GATED) {
+                const float* gc = Gc(i % NKV1);
+                uint4 in[kPer];
+#pragma unroll
+                for (int m = 0; m < kPer; ++m) in[m] = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(m));
+#pragma unroll
+                for (int m = 0; m < kPer; ++m) {
+                    float f[8];
+                    bf8_to_f(in[m], f);
+                    if (GATED) {
+                        const float w = __expf(gc[rbase + kRowStep * m]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] *= w;
+                        *reinterpret_cast<uint4*>(Qd(sq) + chunk_off(m)) = f_to_bf8(f);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = phi<true>(fmap, f[e], eps);
+                        *reinterpret_cast<uint4*>(Qb(sq) + chunk_off(m)) = f_to_bf8(f);
+                    }
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv_q[sq]);
+            if (ct == 0) LA_TR(2, 4, n);
+            return true;
+        };
+
+        auto publish_state = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(state_ready);
+        };
+
+        const int nq_ahead = MODE == kState ? 0 : min(G, NQ);  // query items converted one chunk ahead
         if (MODE == kApply) {
             // fixed global state: hi/lo once; Z rows from the global key state
             tc_fence_after();
             convert_state(1.f, false);
-            if (NORM && rgrp == 0) {
-                __nv_bfloat16 h, l;
-                split_bf16(zreg, h, l);
-                bf_at(Zr(0), (kcol >> 6) * 1024 + sw128_offset(0, (kcol & 63) * 2)) = h;
-                bf_at(Zr(0), (kcol >> 6) * 1024 + sw128_offset(1, (kcol & 63) * 2)) = l;
+            if (NORM && ct < D) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(zreg);
+                bf_at(Zr(0), zr_off(0, ct)) = h;
+                bf_at(Zr(0), zr_off(1, ct)) = __float2bfloat16_rn(zreg - __bfloat162float(h));
             }
             fence_proxy_async();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(state_ready);
-        }
-
-        for (int i = 0; i < nck && ok; ++i) {
-            const int t0 = (c_begin + i) * kC;
-            const int valid = min(kC, a.T - t0);
-            const int s = NKV ? i % NKV : 0;
-            float gtot = 0.f;
-            if (Cf::kHasKV) {
-                ok = warp_wait(&full_kv[s], (i / (NKV ? NKV : 1)) & 1, err, kErrFullKV);
-                if (!ok) break;
-                float* gc = Gc(s);
-                if (GATED) {
-                    // inclusive cumulative log decay inside the chunk (first converter warp)
-                    if (ct < 32) {
-                        float g0 = 0.f, g1 = 0.f;
-                        const int j0 = 2 * ct, j1 = 2 * ct + 1;
-                        if (j0 < valid) g0 = __bfloat162float(a.decay[((size_t)b * a.T + t0 + j0) * a.Hkv + hk]);
-                        if (j1 < valid) g1 = __bfloat162float(a.decay[((size_t)b * a.T + t0 + j1) * a.Hkv + hk]);
-                        float sum = g0 + g1, incl = sum;
-#pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const float t = __shfl_up_sync(0xffffffffu, incl, o);
-                            if (lane >= o) incl += t;
-                        }
-                        const float excl = incl - sum;
-                        gc[j0] = excl + g0;
-                        gc[j1] = excl + sum;
-                    }
-                    ok = group_sync(conv_group, gphase, err, kErrStateReady);
-                    if (!ok) break;
-                    gtot = gc[kC - 1];
-                }
-                // feature map of the keys in place (+ lo part), decayed keys, Z column sums
-                float colsum = 0.f;
-#pragma unroll 4
-                for (int jj = 0; jj < kRows; ++jj) {
-                    const int j = row0 + jj;
-                    const uint32_t off = tile_off<D>(j, kcol);
-                    const float x = __bfloat162float(bf_at(Kb(s), off));
-                    if (GATED) {
-                        const float w = __expf(gtot - gc[j]);
-                        __nv_bfloat16 h, l;
-                        split_bf16(x * w, h, l);
-                        bf_at(Kd(s), off) = h;
-                        bf_at(Klo(s), off) = l;
-                    } else {
-                        const float f = phi<true>(a.fmap, x, a.eps);
-                        if (a.fmap != LA_FMAP_NONE) {
-                            __nv_bfloat16 h, l;
-                            split_bf16(f, h, l);
-                            bf_at(Kb(s), off) = h;
-                            if (SPLITK) bf_at(Klo(s), off) = l;
-                        } else if (SPLITK) {
-                            bf_at(Klo(s), off) = __float2bfloat16(0.f);
-                        }
-                        if (NORM && j < valid) colsum += f;
-                    }
-                }
-                if (NORM) {
-                    // Z rows of this chunk hold Z_prev (hi, lo); then Z += column sums
-                    if (D == 128) {
-                        __nv_bfloat16 h, l;
-                        split_bf16(zreg, h, l);
-                        bf_at(Zr(s), (kcol >> 6) * 1024 + sw128_offset(0, (kcol & 63) * 2)) = h;
-                        bf_at(Zr(s), (kcol >> 6) * 1024 + sw128_offset(1, (kcol & 63) * 2)) = l;
-                        zreg += colsum;
-                    } else {
-                        zpart[rgrp * 128 + kcol] = colsum;
-                        ok = group_sync(conv_group, gphase, err, kErrStateReady);
-                        if (!ok) break;
-                        if (rgrp == 0) {
-                            __nv_bfloat16 h, l;
-                            split_bf16(zreg, h, l);
-                            bf_at(Zr(s), (kcol >> 6) * 1024 + sw128_offset(0, (kcol & 63) * 2)) = h;
-                            bf_at(Zr(s), (kcol >> 6) * 1024 + sw128_offset(1, (kcol & 63) * 2)) = l;
-                            zreg += zpart[kcol] + zpart[128 + kcol];
-                        }
-                        ok = group_sync(conv_group, gphase, err, kErrStateReady);  // zpart reuse
+            publish_state();
+            for (int n = 0; n < nck * G && ok; ++n) ok = process_q(n / G, n);
+        } else {
+            // prologue: chunk 0 ahead of the loop
+            if (nck > 0) ok = process_kv(0);
+            for (int r = 0; r < nq_ahead && ok; ++r) ok = process_q(0, r);
+            if (MODE == kState && !GATED) publish_state();  // the zero state is in place
+            float gtot_next = gtot_cur;  // decay of the next chunk whose state is converted
+            for (int i = 0; i < nck && ok; ++i) {
+                const float gtot_i = gtot_next;
+                if (MODE == kCausal || GATED) {
+                    // S(i): after the update of chunk i-1 (and every read-out that used S_prev)
+                    if (i > 0) {
+                        ok = warp_wait(state_done, (i - 1) & 1, err, kErrStateDone);
                         if (!ok) break;
                     }
+                    tc_fence_after();
+                    if (ct == 0) LA_TR(2, 5, i);
+                    convert_state(GATED ? __expf(gtot_i) : 1.f, GATED);
+                    publish_state();
+                    if (ct == 0) LA_TR(2, 6, i);
+                    if (MODE == kState) gsum += gtot_i;
                 }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&conv_kv[s]);
-            }
-            // state for this chunk, before the query heads (the read-out of head 0
-            // needs it, and later heads' loads wait on head 0's read-out):
-            // hi/lo of S_prev for the read-out; decay (gated) before the update
-            if (MODE == kCausal || (MODE == kState && GATED)) {
-                if (i > 0) {
-                    ok = warp_wait(state_done, (i - 1) & 1, err, kErrStateDone);
-                    if (!ok) break;
-                }
-                tc_fence_after();
-                convert_state(GATED ? __expf(gtot) : 1.f, GATED);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(state_ready);
-            } else if (MODE == kState && i == 0) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(state_ready);
-            }
-            if (Cf::kHasQ) {
-                const float* gc = Gc(s);
-                for (int r = 0; r < G && ok; ++r) {
-                    const int n = i * G + r, sq = n % (NQ ? NQ : 1);
-                    ok = warp_wait(&full_q[sq], (n / (NQ ? NQ : 1)) & 1, err, kErrFullQ);
-                    if (!ok) break;
-                    if (a.fmap != LA_FMAP_NONE || GATED) {
-#pragma unroll 4
-                        for (int jj = 0; jj < kRows; ++jj) {
-                            const int j = row0 + jj;
-                            const uint32_t off = tile_off<D>(j, kcol);
-                            const float x = __bfloat162float(bf_at(Qb(sq), off));
-                            if (GATED) {
-                                bf_at(Qd(sq), off) = __float2bfloat16_rn(x * __expf(gc[j]));
-                            } else {
-                                bf_at(Qb(sq), off) = __float2bfloat16_rn(phi<true>(a.fmap, x, a.eps));
-                            }
-                        }
-                    }
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&conv_q[sq]);
-                }
+                for (int r = nq_ahead; r < G && ok && MODE == kCausal; ++r) ok = process_q(i, i * G + r);
                 if (!ok) break;
+                if (i + 1 < nck) {
+                    ok = process_kv(i + 1);
+                    gtot_next = gtot_cur;
+                    for (int r = 0; r < nq_ahead && ok; ++r) ok = process_q(i + 1, (i + 1) * G + r);
+                }
             }
-            if (MODE == kState && GATED) gsum += gtot;
         }
 
-        // final state out: causal (last segment) or every segment in state mode
-        const bool write_state = ok && ((MODE == kCausal && seg == a.nseg - 1 && a.S_dst) || MODE == kState);
+        // ---- final state out: causal (last segment) or every segment in state mode
+        const bool write_state =
+            ok && nck > 0 && ((MODE == kCausal && seg == nseg - 1 && a.S_dst) || MODE == kState);
         if (write_state) {
             // causal: phase nck-1 (one per chunk); non-gated state pass: its single phase
             ok = warp_wait(state_done, (MODE == kState && !GATED) ? 0 : ((nck - 1) & 1), err, kErrStateDone);
             tc_fence_after();
             if (ok) {
-                float* Sd = MODE == kState ? a.S_dst + ((size_t)bh * a.nseg + seg) * D * D : a.S_dst + (size_t)bh * D * D;
+                float* Sd = MODE == kState ? a.S_dst + ((size_t)bh * nseg + seg) * D * D : a.S_dst + (size_t)bh * D * D;
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t r[32];
@@ -580,107 +680,95 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int x = 0; x < 32; ++x) Sd[(size_t)(c0 + x) * D + vrow] = __uint_as_float(r[x]);
                 }
-                if (NORM && rgrp == 0 && a.Z_dst) {
-                    float* Zd = MODE == kState ? a.Z_dst + ((size_t)bh * a.nseg + seg) * D : a.Z_dst + (size_t)bh * D;
-                    Zd[kcol] = zreg;
-                }
-                if (MODE == kState && GATED && ct == 0) a.G_dst[(size_t)bh * a.nseg + seg] = gsum;
+                if (NORM && ct < D && a.Z_dst)
+                    (MODE == kState ? a.Z_dst + ((size_t)bh * nseg + seg) * D : a.Z_dst + (size_t)bh * D)[ct] = zreg;
+                if (MODE == kState && GATED && ct == 0) a.G_dst[(size_t)bh * nseg + seg] = gsum;
             }
         }
     } else {
         // -------------------------------------------------------------- epilogue
-        const int et = tid - kEpiWarp0 * 32;  // 0..127
         const int quad = warp & 3;
         const bool m64 = D == 64;
-        const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);  // value index of Y^T row
+        const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);  // value index of this Y^T lane
         const bool vrow_ok = m64 ? lane < 16 : true;
-        const int arow = quad * 16 + lane;  // score row (M = 64 layout)
+        const int arow = quad * 16 + lane;  // score row (M = 64 layout: lanes 0-15 of each quadrant)
         const bool arow_ok = lane < 16;
         const int n_total = Cf::kHasQ ? nck * G : 0;
         bool ok = true;
         uint32_t gphase = 0;
         for (int n = 0; n <= n_total && ok; ++n) {
-            if (n < n_total && (MODE == kCausal || NORM)) {
-                // -------- scores of item n: mask, decay, hi/lo split, normaliser
+            if (n < n_total) {
+                // -------- scores of item n: mask, decay, hi/lo split, 1/den
                 const int ab = n & 1;
-                const int i_chunk = n / G;
-                const int s = NKV ? i_chunk % NKV : 0;
-                ok = warp_wait(&a_full[ab], (n >> 1) & 1, err, kErrAFull);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t tA = tmem + Cf::kColA + 80 * ab;
-                uint32_t r[32], r2[32], z[16];
-                if (MODE == kCausal) {
-                    tmem_ld32(tmem_addr(tA, quad * 32, 0), r);
-                    tmem_ld32(tmem_addr(tA, quad * 32, 32), r2);
-                }
-                if (NORM) tmem_ld16(tmem_addr(tA, quad * 32, 64), z);
-                tmem_ld_wait();
-                if (MODE == kCausal) {
-                    reg_fence(r);
-                    reg_fence(r2);
-                }
-                if (NORM) reg_fence(z);
-                float den = 0.f;
-                if (NORM) den = __uint_as_float(z[0]) + __uint_as_float(z[1]) + a.eps;
-                if (MODE == kCausal) {
-                    if (n >= 2) {
-                        ok = warp_wait(&at_empty[ab], ((n >> 1) & 1) ^ 1, err, kErrATEmpty);
-                        if (!ok) break;
+                const int s = (n / G) % NKV1;
+                float den = 1.f;
+                if (MODE == kCausal || NORM) {
+                    ok = warp_wait(&a_full[ab], (n >> 1) & 1, err, kErrAFull);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 1, n);
+                    const uint32_t tA = tmem + Cf::kColA + 80 * ab;
+                    uint32_t r[32], r2[32], z[16];
+                    if (MODE == kCausal) {
+                        tmem_ld32(tmem_addr(tA, quad * 32, 0), r);
+                        tmem_ld32(tmem_addr(tA, quad * 32, 32), r2);
                     }
-                    if (arow_ok) {
-                        const float* gc = reinterpret_cast<const float*>(Gc(s));
-                        const float gi = GATED ? gc[arow] : 0.f;
-                        uint8_t* hb = ATh(ab);
-                        uint8_t* lb = ATl(ab);
-#pragma unroll
-                        for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
-                            uint32_t hv[4], lv[4];
-#pragma unroll
-                            for (int x = 0; x < 4; ++x) {
-                                float v2[2];
-#pragma unroll
-                                for (int y = 0; y < 2; ++y) {
-                                    const int j = cch * 8 + 2 * x + y;
-                                    float v = j < 32 ? __uint_as_float(r[j]) : __uint_as_float(r2[j - 32]);
-                                    v = (j <= arow) ? v : 0.f;
-                                    if (NORM) den += v;
-                                    if (GATED && j <= arow) v *= __expf(gi - gc[j]);
-                                    v2[y] = v;
-                                }
-                                __nv_bfloat16 h0, l0, h1, l1;
-                                split_bf16(v2[0], h0, l0);
-                                split_bf16(v2[1], h1, l1);
-                                __nv_bfloat162 hh, ll;
-                                hh.x = h0; hh.y = h1;
-                                ll.x = l0; ll.y = l1;
-                                hv[x] = *reinterpret_cast<uint32_t*>(&hh);
-                                lv[x] = *reinterpret_cast<uint32_t*>(&ll);
-                            }
-                            const uint32_t off = sw128_offset(arow, cch * 16);
-                            *reinterpret_cast<uint4*>(hb + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                            *reinterpret_cast<uint4*>(lb + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+                    if (NORM) tmem_ld16(tmem_addr(tA, quad * 32, 64), z);
+                    tmem_ld_wait();
+                    if (MODE == kCausal) {
+                        reg_fence(r);
+                        reg_fence(r2);
+                    }
+                    if (NORM) reg_fence(z);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_empty[ab]);  // TMEM scores read out
+                    if (NORM) den = __uint_as_float(z[0]) + __uint_as_float(z[1]) + eps;
+                    if (MODE == kCausal) {
+                        if (n >= 1) {
+                            ok = warp_wait(at_empty, (n - 1) & 1, err, kErrATEmpty);
+                            if (!ok) break;
                         }
+                        if (arow_ok) {
+                            const float* gc = reinterpret_cast<const float*>(Gc(s));
+                            const float gi = GATED ? gc[arow] : 0.f;
+#pragma unroll
+                            for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
+                                float v[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const int j = cch * 8 + e;
+                                    float x = j < 32 ? __uint_as_float(r[j]) : __uint_as_float(r2[j - 32]);
+                                    x = (j <= arow) ? x : 0.f;
+                                    if (NORM) den += x;
+                                    if (GATED && j <= arow) x *= __expf(gi - gc[j]);
+                                    v[e] = x;
+                                }
+                                uint4 hv, lv;
+                                split8(v, hv, lv);
+                                const uint32_t off = sw128_offset(arow, cch * 16);
+                                *reinterpret_cast<uint4*>(ATh + off) = hv;
+                                *reinterpret_cast<uint4*>(ATl + off) = lv;
+                            }
+                        }
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(at_full);
+                        if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 2, n);
                     }
-                    fence_proxy_async();
                 }
-                if (NORM && arow_ok) den_s[ab * 64 + arow] = den;
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&a_empty[ab]);
-                    if (MODE == kCausal) mbar_arrive(&at_full[ab]);
-                }
+                if (arow_ok) inv_den[(n & 3) * 64 + arow] = NORM ? scale / den : scale;
             }
             if (n >= 1) {
-                // -------- output of item m = n - 1
+                // -------- output of item m = n - 1, stored straight to global memory
                 const int m = n - 1;
-                const int ab = m & 1;
                 const int i_chunk = m / G, r_head = m - i_chunk * G;
                 const int t0 = (c_begin + i_chunk) * kC;
+                const int valid = min(kC, T - t0);
                 ok = warp_wait(y_full, m & 1, err, kErrYFull);
                 if (!ok) break;
                 tc_fence_after();
+                if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 3, m);
                 uint32_t y0[32], y1[32];
                 tmem_ld32(tmem_addr(tmem + Cf::kColY, quad * 32, 0), y0);
                 tmem_ld32(tmem_addr(tmem + Cf::kColY, quad * 32, 32), y1);
@@ -690,37 +778,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(y_empty);
-                ok = group_sync(epi_group, gphase, err, kErrYFull);  // den_s of item m complete; staging free
-                if (!ok) break;
-                uint8_t* ys = Ys(m % (NY ? NY : 1));
-                if (vrow_ok) {
-#pragma unroll
-                    for (int x = 0; x < 64; ++x) {
-                        float v = x < 32 ? __uint_as_float(y0[x]) : __uint_as_float(y1[x - 32]);
-                        if (NORM) v = v / den_s[ab * 64 + x];
-                        v *= a.scale;
-                        if (OUT_BF16)
-                            reinterpret_cast<__nv_bfloat16*>(ys)[x * D + vrow] = __float2bfloat16_rn(v);
-                        else
-                            reinterpret_cast<float*>(ys)[x * D + vrow] = v;
-                    }
-                }
-                fence_proxy_async();
+                // 1/den of item m was written by all four warps one iteration ago
                 ok = group_sync(epi_group, gphase, err, kErrYFull);
                 if (!ok) break;
-                if (et == 0) {
-                    tma_store_4d(&mapY, ys, 0, hk * G + r_head, t0, b);
-                    bulk_commit_group();
-                    if (NY == 1) bulk_wait_group_read<0>();
-                    else bulk_wait_group_read<1>();
+                if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 4, m);
+                const float* idn = inv_den + (m & 3) * 64;
+                if (vrow_ok) {
+                    const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
+                    const size_t tstride = (size_t)Hq * D;
+#pragma unroll
+                    for (int x = 0; x < 64; ++x) {
+                        if (x < valid) {
+                            const float v = (x < 32 ? __uint_as_float(y0[x]) : __uint_as_float(y1[x - 32])) * idn[x];
+                            if (OUT_BF16)
+                                reinterpret_cast<__nv_bfloat16*>(yout)[base + x * tstride] = __float2bfloat16_rn(v);
+                            else
+                                reinterpret_cast<float*>(yout)[base + x * tstride] = v;
+                        }
+                    }
                 }
             }
         }
-        if (et == 0) bulk_wait_group<0>();
     }
 
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) LA_TR(0, 9, 0);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, Cf::kTmemCols);

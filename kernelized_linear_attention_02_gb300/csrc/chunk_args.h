@@ -24,14 +24,16 @@ struct Args {
     int nseg;  // segments per (b, kv head)
     int fmap;
     float eps, scale;
-    const float* S_init;  // (B*Hkv, Dk, Dv) start state of segment 0, or the global state (apply); may be null
+    const float* S_init;  // (B*Hkv, Dk, Dv) initial state (causal) or the global state (apply); may be null
     const float* Z_init;  // (B*Hkv, Dk)
-    const float* S_seg;   // causal, nseg > 1: (B*Hkv, nseg, Dk, Dv); entry s is the start state of segment s
-    const float* Z_seg;   // (B*Hkv, nseg, Dk)
+    const float* S_seg;   // causal, nseg > 1: (B*Hkv, nseg, Dk, Dv) state increment of each segment
+    const float* Z_seg;   // (B*Hkv, nseg, Dk) key-sum increment of each segment
+    const float* G_seg;   // (B*Hkv, nseg) log decay of each segment (gated)
     float* S_dst;         // causal: final state (B*Hkv, Dk, Dv) from the last segment; state: (B*Hkv, nseg, Dk, Dv)
     float* Z_dst;
     float* G_dst;                 // state + gated: (B*Hkv, nseg) log decay of each segment
     const __nv_bfloat16* decay;   // (B, T, Hkv)
+    void* y;                      // (B, T, Hq, Dv) output, bf16 or fp32
     unsigned* err;
 };
 
@@ -41,7 +43,7 @@ struct Launch {
     bool norm, splitk, gated, out_bf16;
     dim3 grid;
     Args args;
-    CUtensorMap mq, mk, mv, my;
+    CUtensorMap mq, mk, mv;
 };
 
 }  // namespace chunk

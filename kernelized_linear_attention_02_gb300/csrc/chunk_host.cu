@@ -1,13 +1,13 @@
 // chunk_host.cu -- host orchestration of the tensor-core path: sequence
-// segmentation, workspace layout, tensor maps, and the two small CUDA-core
-// kernels between the passes (segment-state scan for the causal form,
-// segment-state sum for the non-causal form).
+// segmentation, workspace layout, tensor maps, and the small CUDA-core
+// kernel that sums the per-segment states of the non-causal form.
 //
 // Causal, sequence split into P segments per (batch, kv head):
 //   pass 1 (state mode, segments 0..P-2): dS_p, dZ_p, log decay of segment p
-//   scan: start state of segment p = decay-weighted prefix of dS over p' < p,
-//         starting from the caller's initial state
-//   pass 2 (causal mode, all segments): outputs, final state from segment P-1
+//   pass 2 (causal mode, all segments): each CTA folds dS_0..dS_{s-1} onto
+//          the initial state (decay-weighted) to get the start state of its
+//          segment, then produces its outputs; the last segment writes the
+//          final state
 // Non-causal: pass 1 over all segments, sum, then the read-out pass.
 #include <algorithm>
 #include <cstring>
@@ -66,6 +66,9 @@ Plan plan_segments(int64_t BH, int nchunks, int sms) {
 struct WsLayout {
     size_t S_seg = 0, Z_seg = 0, G_seg = 0, S_tot = 0, Z_tot = 0, total = 0;
 };
+// Causal with several segments: S_tot / Z_tot hold a copy of the initial
+// state when the caller streams in place (S_out == S0), because the last
+// segment writes the final state while other segments may still read S0.
 
 WsLayout ws_layout(const Problem& P, bool causal, int nseg) {
     WsLayout w;
@@ -79,7 +82,7 @@ WsLayout ws_layout(const Problem& P, bool causal, int nseg) {
     off += round_up(BH * nseg * D * sizeof(float));
     w.G_seg = off;
     off += round_up(BH * nseg * sizeof(float));
-    if (!causal) {
+    {
         w.S_tot = off;
         off += round_up(BH * D * D * sizeof(float));
         w.Z_tot = off;
@@ -87,34 +90,6 @@ WsLayout ws_layout(const Problem& P, bool causal, int nseg) {
     }
     w.total = off;
     return w;
-}
-
-// Start state of every segment, in place over the per-segment increments:
-// slot p holds dS_p on entry and S_start(p) on exit.
-__global__ void segment_scan_kernel(float* S_seg, float* Z_seg, const float* G_seg, const float* S0, const float* Z0,
-                                    int nseg, int D, int norm, int gated) {
-    const int64_t bh = blockIdx.y;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    const int DD = D * D;
-    if (e < DD) {
-        float run = S0 ? S0[bh * DD + e] : 0.f;
-        for (int p = 0; p < nseg; ++p) {
-            float* slot = S_seg + (bh * nseg + p) * DD + e;
-            const float d = p < nseg - 1 ? *slot : 0.f;
-            *slot = run;
-            if (p < nseg - 1) run = (gated ? expf(G_seg[bh * nseg + p]) : 1.f) * run + d;
-        }
-    }
-    if (norm && blockIdx.x == 0 && threadIdx.x < D) {
-        const int k = threadIdx.x;
-        float run = Z0 ? Z0[bh * D + k] : 0.f;
-        for (int p = 0; p < nseg; ++p) {
-            float* slot = Z_seg + (bh * nseg + p) * D + k;
-            const float d = p < nseg - 1 ? *slot : 0.f;
-            *slot = run;
-            run += d;
-        }
-    }
 }
 
 // Global state of the non-causal form: sum of the per-segment states in a
@@ -214,32 +189,40 @@ cudaError_t chunk_causal(const Problem& P, const void* q, const void* k, const v
     L.args.nseg = pl.nseg;
     L.args.decay = static_cast<const __nv_bfloat16*>(decay);
     if (!act_map(&L.mq, q, D, P.Hq, P.T, P.B, false, false) || !act_map(&L.mk, k, D, P.Hkv, P.T, P.B, false, false) ||
-        !act_map(&L.mv, v, D, P.Hkv, P.T, P.B, false, false) ||
-        !act_map(&L.my, y, D, P.Hq, P.T, P.B, true, !P.out_bf16))
+        !act_map(&L.mv, v, D, P.Hkv, P.T, P.B, false, false))
         return cudaErrorInvalidValue;
+    L.args.y = y;
+    L.args.S_init = S0;
+    L.args.Z_init = P.norm ? Z0 : nullptr;
 
     if (pl.nseg > 1) {
         float* S_seg = reinterpret_cast<float*>(w + wl.S_seg);
         float* Z_seg = reinterpret_cast<float*>(w + wl.Z_seg);
         float* G_seg = reinterpret_cast<float*>(w + wl.G_seg);
+        cudaError_t e;
+        if (S0 && S0 == S_out) {  // in-place streaming: read the initial state from a copy
+            float* S_copy = reinterpret_cast<float*>(w + wl.S_tot);
+            e = cudaMemcpyAsync(S_copy, S0, (size_t)BH * D * D * sizeof(float), cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) return e;
+            L.args.S_init = S_copy;
+        }
+        if (P.norm && Z0 && Z0 == Z_out) {
+            float* Z_copy = reinterpret_cast<float*>(w + wl.Z_tot);
+            e = cudaMemcpyAsync(Z_copy, Z0, (size_t)BH * D * sizeof(float), cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) return e;
+            L.args.Z_init = Z_copy;
+        }
         chunk::Launch Ls = L;
         Ls.mode = chunk::kState;
         Ls.grid = dim3((unsigned)BH, (unsigned)(pl.nseg - 1));
         Ls.args.S_dst = S_seg;
         Ls.args.Z_dst = P.norm ? Z_seg : nullptr;
         Ls.args.G_dst = G_seg;
-        cudaError_t e = run(Ls, D, st);
+        e = run(Ls, D, st);
         if (e != cudaSuccess) return e;
-        const int DD = D * D;
-        segment_scan_kernel<<<dim3((DD + 255) / 256, (unsigned)BH), 256, 0, st>>>(S_seg, Z_seg, G_seg, S0, Z0, pl.nseg,
-                                                                                D, P.norm, P.gated);
-        note_launch();
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         L.args.S_seg = S_seg;
         L.args.Z_seg = P.norm ? Z_seg : nullptr;
-    } else {
-        L.args.S_init = S0;
-        L.args.Z_init = P.norm ? Z0 : nullptr;
+        L.args.G_seg = G_seg;
     }
     L.grid = dim3((unsigned)BH, (unsigned)pl.nseg);
     L.args.S_dst = S_out;
@@ -267,9 +250,9 @@ cudaError_t chunk_noncausal(const Problem& P, const void* q, const void* k, cons
     L.args.cps = pl.cps;
     L.args.nseg = pl.nseg;
     if (!act_map(&L.mq, q, D, P.Hq, P.T, P.B, false, false) || !act_map(&L.mk, k, D, P.Hkv, P.T, P.B, false, false) ||
-        !act_map(&L.mv, v, D, P.Hkv, P.T, P.B, false, false) ||
-        !act_map(&L.my, y, D, P.Hq, P.T, P.B, true, !P.out_bf16))
+        !act_map(&L.mv, v, D, P.Hkv, P.T, P.B, false, false))
         return cudaErrorInvalidValue;
+    L.args.y = y;
     L.grid = dim3((unsigned)BH, (unsigned)pl.nseg);
     L.args.S_dst = S_seg;
     L.args.Z_dst = P.norm ? Z_seg : nullptr;

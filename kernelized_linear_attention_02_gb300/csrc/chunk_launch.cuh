@@ -13,9 +13,16 @@ template <int D, int MODE, bool NORM, bool SPLITK, bool GATED, bool OUTBF>
 cudaError_t run_one(const Launch& L, cudaStream_t st) {
     using Cf = Cfg<D, MODE, NORM, SPLITK, GATED, OUTBF>;
     auto kern = chunk_kernel<D, MODE, NORM, SPLITK, GATED, OUTBF>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
+    static int configured = -1;  // device on which the shared-memory limit was raised
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    kern<<<L.grid, kThreads, Cf::kSmem, st>>>(L.args, L.mq, L.mk, L.mv, L.my);
+    if (configured != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
+        if (e != cudaSuccess) return e;
+        configured = dev;
+    }
+    kern<<<L.grid, kThreads, Cf::kSmem, st>>>(L.args, L.mq, L.mk, L.mv);
     note_launch();
     return cudaGetLastError();
 }
@@ -49,3 +56,19 @@ cudaError_t run_d(const Launch& L, cudaStream_t st) {
 
 }  // namespace chunk
 }  // namespace la
+
+#ifdef LA_TRACE
+// Trace builds only: copy out (and reset) this unit's event buffer.
+#define LA_TRACE_DUMP(NAME)                                                                              \
+    extern "C" int NAME(unsigned* count, unsigned long long* times, unsigned* tags) {                   \
+        using namespace la::trace;                                                                      \
+        if (cudaDeviceSynchronize() != cudaSuccess) return -1;                                          \
+        cudaMemcpyFromSymbol(count, g_count, sizeof(unsigned) * kTraceCtas);                            \
+        cudaMemcpyFromSymbol(times, g_time, sizeof(unsigned long long) * kTraceCtas * kTraceEvents);    \
+        cudaMemcpyFromSymbol(tags, g_tag, sizeof(unsigned) * kTraceCtas * kTraceEvents);                \
+        unsigned long long zt[kTraceEvents] = {};                                                        \
+        for (int c = 0; c < kTraceCtas; ++c)                                                             \
+            cudaMemcpyToSymbol(g_time, zt, sizeof(zt), sizeof(zt) * c);                                  \
+        return 0;                                                                                       \
+    }
+#endif
