@@ -26,19 +26,18 @@
 // decayed key) is not exactly representable in bf16.  All accumulation is
 // fp32 in tensor memory.
 //
-// Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-5 operand converters (feature map, hi/lo splits, Z, state
-// hi/lo in TMEM), warps 6-9 epilogue (masking of the scores, output
-// normalisation and store).  Every wait is bounded and reports a code in
+// Roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2-5 state (hi/lo copy of the carried state in TMEM, gated
+// decay), warps 6-9 epilogue (masking of the scores, output normalisation
+// and store), warps 10-13 feature maps (phi of keys and queries, hi/lo
+// splits, Z rows and sums).  Every wait is bounded and reports a code in
 // *err instead of hanging.
 //
-// Pipeline per chunk i (G query heads per kv head):
-//   converter: S(i) [state hi/lo, after the update of chunk i-1], the query
-//              heads of chunk i beyond the ring depth, then the feature maps
-//              of chunk i+1 (keys, first query heads) ahead of time;
-//   MMA:       per head: scores, read-out with S_prev; after the last
-//              head's read-out the state update, then the intra term;
-// so the only loop-carried chain is S(i) -> read-out(i) -> update(i) -> S(i+1).
+// Pipeline per chunk i (G query heads per kv head): the feature warps run
+// ahead of the tensor core, limited only by the load rings; the MMA issues
+// per head the scores and the read-out with S_prev, after the last head's
+// read-out the state update, then the intra term; so the only loop-carried
+// chain is state hi/lo(i) -> read-out(i) -> update(i) -> state hi/lo(i+1).
 //
 // Modes: kCausal (outputs + carried state), kState (only the state update
 // over a segment, for the two-pass sequence split and the non-causal
@@ -56,21 +55,28 @@ namespace chunk {
 using namespace umma;
 
 constexpr int kC = 64;  // tokens per chunk
-constexpr int kThreads = 320;
-constexpr int kConvWarp0 = 2, kEpiWarp0 = 6;
+constexpr int kThreads = 448;
+constexpr int kStateWarp0 = 2, kEpiWarp0 = 6, kFeatWarp0 = 10;
 
-template <int D, int MODE, bool NORM, bool SPLITK, bool GATED, bool OUT_BF16>
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16>
 struct Cfg {
+    // the state update needs a lo part of its key operand when phi(k) (elu+1)
+    // or the decayed key (gated) is not exactly representable in bf16
+    static constexpr bool kSplitK = GATED || FMAP == LA_FMAP_ELU_PLUS_ONE;
     static constexpr bool kHasKV = MODE != kApply;
     static constexpr bool kHasQ = MODE != kState;
     static constexpr int kTile = D * 128;  // 64 rows x D bf16 (D/64 swizzled blocks of 8 KB)
     static constexpr int kZr = D * 16;     // 8 rows x D bf16: [Z_hi; Z_lo; 0 x 6]
-    // per KV stage: Kb | Kd (gated) | Klo (split) | Vb | Zr (normalizer) | G (256 B, padded)
-    static constexpr int kOffKd = kTile;
+    // key tile: per 64-feature block, 64 token rows followed (causal with the
+    // normalizer) by 8 Z rows, so one N = 72 MMA gives the scores and phi(q).Z
+    static constexpr int kKRows = (NORM && MODE == kCausal) ? 72 : 64;
+    static constexpr int kKBlk = kKRows * 128;  // bytes per 64-feature block of the key tile
+    static constexpr int kKTile = (D / 64) * kKBlk;
+    // per KV stage: Kb (+ Z rows) | Kd (gated) | Klo (split) | Vb | G (256 B, padded)
+    static constexpr int kOffKd = ((kKTile + 1023) / 1024) * 1024;
     static constexpr int kOffKlo = kOffKd + (GATED ? kTile : 0);
-    static constexpr int kOffVb = kOffKlo + (SPLITK ? kTile : 0);
-    static constexpr int kOffZr = kOffVb + kTile;
-    static constexpr int kOffG = kOffZr + (NORM ? kZr : 0);
+    static constexpr int kOffVb = kOffKlo + (kSplitK ? kTile : 0);
+    static constexpr int kOffG = kOffVb + kTile;
     static constexpr int kKvStage = kHasKV ? kOffG + 1024 : 0;
     static constexpr int kQStage = kHasQ ? kTile * (GATED ? 2 : 1) : 0;
     static constexpr int kAT = MODE == kCausal ? 2 * 8192 : 0;  // masked scores hi + lo, 64 x 64 each
@@ -85,21 +91,26 @@ struct Cfg {
     static constexpr int kSmem = bytes(kNKV, kNQ);
     static_assert(kSmem <= kLimit, "shared memory budget");
     // TMEM columns
+    static constexpr int kNA = D == 64 ? 2 : 1;    // score buffers (64 + 8 columns for phi(q).Z each)
+    static constexpr int kNY = 2;                  // Y^T buffers (64 columns each)
     static constexpr uint32_t kColS = 0;           // S^T fp32: D columns, lanes = value rows
     static constexpr uint32_t kColHi = D;          // S^T hi bf16 pairs: D/2 columns
     static constexpr uint32_t kColLo = D + D / 2;  // S^T lo
-    static constexpr uint32_t kColA = 2 * D;       // two score buffers of 80 columns (64 + 8 for phi(q).Z)
-    static constexpr uint32_t kColY = 2 * D + 160; // Y^T: 64 columns
+    static constexpr uint32_t kColA = 2 * D;       // score buffers, 80 columns apart
+    static constexpr uint32_t kColY = 2 * D + 80 * kNA;
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(kColY + 64 <= kTmemCols, "TMEM budget");
+    static_assert(kColY + 64 * kNY <= kTmemCols, "TMEM budget");
     // vectorised tile passes: 16-byte chunks, 128 threads
     static constexpr int kCPR = D / 8;           // chunks per 64 x D tile row
     static constexpr int kRowStep = 128 / kCPR;  // rows covered by one pass of 128 threads
     static constexpr int kPer = 64 / kRowStep;   // chunks per thread per tile
 };
 
+// Rounds a shared-memory pointer up to 1024 bytes by pointer arithmetic (not
+// through an integer), so the compiler still knows it addresses shared memory
+// and emits shared loads/stores instead of generic ones.
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
 __device__ __forceinline__ void bf8_to_f(const uint4& u, float (&f)[8]) {
@@ -133,11 +144,13 @@ __device__ __forceinline__ __nv_bfloat16& bf_at(uint8_t* base, uint32_t off) {
     return *reinterpret_cast<__nv_bfloat16*>(base + off);
 }
 
-template <int D, int MODE, bool NORM, bool SPLITK, bool GATED, bool OUT_BF16>
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_kernel(const __grid_constant__ Args a, const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                  const __grid_constant__ CUtensorMap mapV) {
-    using Cf = Cfg<D, MODE, NORM, SPLITK, GATED, OUT_BF16>;
+    using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>;
+    constexpr bool SPLITK = Cf::kSplitK;
+    constexpr int NA = Cf::kNA, NY = Cf::kNY;
     constexpr int NKV = Cf::kNKV, NQ = Cf::kNQ;
     constexpr int NKV1 = NKV ? NKV : 1, NQ1 = NQ ? NQ : 1;
     extern __shared__ uint8_t smem_raw[];
@@ -159,16 +172,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* a_full = bars + 12;    // [2]
     uint64_t* a_empty = bars + 14;   // [2]
     uint64_t* at_full = bars + 16;
-    uint64_t* at_empty = bars + 17;
-    uint64_t* y_full = bars + 18;
-    uint64_t* y_empty = bars + 19;
-    uint64_t* state_ready = bars + 20;
-    uint64_t* state_done = bars + 21;
-    uint64_t* conv_group = bars + 22;  // barrier among the four converter warps
-    uint64_t* epi_group = bars + 23;   // barrier among the four epilogue warps
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+    uint64_t* y_full = bars + 17;    // [2]
+    uint64_t* y_empty = bars + 19;   // [2]
+    uint64_t* state_ready = bars + 21;
+    uint64_t* state_done = bars + 22;
+    uint64_t* conv_group = bars + 23;  // barrier among the four converter warps
+    uint64_t* epi_group = bars + 24;   // barrier among the four epilogue warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 25);
 #ifdef LA_TRACE
-    unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 25);
+    unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 26);
     if (threadIdx.x < 4) la_trace_ctr[threadIdx.x] = 0;
 #endif
 
@@ -179,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // capture by reference, and reading the parameter block through its
     // address inside hot loops would be a long-latency load per use.
     const int T = a.T, Hq = a.Hq, Hkv = a.Hkv, G = a.G, nseg = a.nseg;
-    const int fmap = a.fmap;
+    constexpr int fmap = FMAP;
     const float eps = a.eps, scale = a.scale;
     const __nv_bfloat16* __restrict__ decay = a.decay;
     void* const yout = a.y;
@@ -192,7 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto Kd = [&](int s) { return kv_base + s * Cf::kKvStage + Cf::kOffKd; };
     auto Klo = [&](int s) { return kv_base + s * Cf::kKvStage + Cf::kOffKlo; };
     auto Vb = [&](int s) { return kv_base + s * Cf::kKvStage + Cf::kOffVb; };
-    auto Zr = [&](int s) { return MODE == kApply ? zr_apply : kv_base + s * Cf::kKvStage + Cf::kOffZr; };
+    // Z rows [Z_hi; Z_lo; 0 x 6]: behind the key rows of each 64-feature block
+    // (causal), or one standalone 8-row block per feature block (read-out pass)
+    auto zr_at = [&](int s, int kb) -> uint8_t* {
+        return MODE == kApply ? zr_apply + kb * 1024 : kv_base + s * Cf::kKvStage + kb * Cf::kKBlk + 64 * 128;
+    };
     auto Gc = [&](int s) { return reinterpret_cast<float*>(kv_base + s * Cf::kKvStage + Cf::kOffG); };
     auto Qb = [&](int s) { return q_base + s * Cf::kQStage; };
     auto Qd = [&](int s) { return q_base + s * Cf::kQStage + Cf::kTile; };
@@ -209,11 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&conv_q[i], 4);
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], 4);
+            mbar_init(&y_full[i], 1);
+            mbar_init(&y_empty[i], 4);
         }
         mbar_init(at_full, 4);
-        mbar_init(at_empty, 1);
-        mbar_init(y_full, 1);
-        mbar_init(y_empty, 4);
         mbar_init(state_ready, 4);
         mbar_init(state_done, 1);
         mbar_init(conv_group, 4);
@@ -252,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     LA_TR(0, 1, i);
                     mbar_arrive_expect_tx(&full_kv[s], 2 * Cf::kTile);
                     for (int kb = 0; kb < D / 64; ++kb) {
-                        tma_load_4d(Kb(s) + kb * 8192, &mapK, &full_kv[s], kb * 64, hk, t0, b);
+                        tma_load_4d(Kb(s) + kb * Cf::kKBlk, &mapK, &full_kv[s], kb * 64, hk, t0, b);
                         tma_load_4d(Vb(s) + kb * 8192, &mapV, &full_kv[s], kb * 64, hk, t0, b);
                     }
                 }
@@ -273,20 +288,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             bool ok = true;
-            constexpr uint32_t id_scores = idesc_bf16(64, 64, false, false);
+            constexpr uint32_t id_scores = idesc_bf16(64, Cf::kKRows, false, false);
             constexpr uint32_t id_qz = idesc_bf16(64, 8, false, false);
             constexpr uint32_t id_inter = idesc_bf16(D, 64, false, false);
             constexpr uint32_t id_intra = idesc_bf16(D, 64, true, false);
             constexpr uint32_t id_state = idesc_bf16(D, D, true, true);
             const uint32_t tS = tmem + Cf::kColS, tHi = tmem + Cf::kColHi, tLo = tmem + Cf::kColLo;
-            const uint32_t tY = tmem + Cf::kColY;
 
             // state update of chunk i: S^T += V^T . Kd (+ V^T . Kd_lo)
             auto issue_state_update = [&](int s) {
                 uint8_t* khi = GATED ? Kd(s) : Kb(s);
+                const uint32_t khi_lbo = GATED ? 8192u : (uint32_t)Cf::kKBlk;  // stride of 64-feature blocks
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                    mma_ss(tS, av, sdesc_sw128(smem_u32(khi + ks * 2048), 8192, 1024), id_state, 1);
+                    mma_ss(tS, av, sdesc_sw128(smem_u32(khi + ks * 2048), khi_lbo, 1024), id_state, 1);
                     if (SPLITK) mma_ss(tS, av, sdesc_sw128(smem_u32(Klo(s) + ks * 2048), 8192, 1024), id_state, 1);
                 }
             };
@@ -313,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
                 for (int r = 0; r < G && ok; ++r) {
-                    const int n = i * G + r, sq = n % NQ1, ab = n & 1;
+                    const int n = i * G + r, sq = n % NQ1, ab = n % NA, yb = n % NY;
                     ok = mbar_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ);
                     if (!ok) break;
                     tc_fence_after();
@@ -321,24 +336,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* qop = GATED ? Qd(sq) : Qb(sq);  // operand of the inter read-out
                     const uint32_t tA = tmem + Cf::kColA + 80 * ab;
                     if (MODE == kCausal || NORM) {
-                        if (n >= 2) {
-                            ok = mbar_wait(&a_empty[ab], ((n >> 1) & 1) ^ 1, err, kErrAEmpty);
+                        if (n >= NA) {
+                            ok = mbar_wait(&a_empty[ab], ((n / NA) & 1) ^ 1, err, kErrAEmpty);
                             if (!ok) break;
                             tc_fence_after();
                         }
                         if (MODE == kCausal) {
+                            // scores, and in columns 64..71 phi(q).[Z_hi; Z_lo] from the Z rows
                             for (int ks = 0; ks < D / 16; ++ks) {
-                                const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
-                                mma_ss(tA, sdesc_sw128(smem_u32(Qb(sq) + ko), 16, 1024),
+                                const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
+                                const uint32_t ko = (ks >> 2) * Cf::kKBlk + (ks & 3) * 32;
+                                mma_ss(tA, sdesc_sw128(smem_u32(Qb(sq) + qo), 16, 1024),
                                        sdesc_sw128(smem_u32(Kb(s) + ko), 16, 1024), id_scores, ks > 0);
                             }
-                        }
-                        if (NORM) {
+                        } else {
                             for (int ks = 0; ks < D / 16; ++ks) {
-                                const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
-                                const uint32_t zo = (ks >> 2) * 1024 + (ks & 3) * 32;
-                                mma_ss(tA + 64, sdesc_sw128(smem_u32(Qb(sq) + ko), 16, 1024),
-                                       sdesc_sw128(smem_u32(Zr(s) + zo), 16, 1024), id_qz, ks > 0);
+                                const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
+                                mma_ss(tA + 64, sdesc_sw128(smem_u32(Qb(sq) + qo), 16, 1024),
+                                       sdesc_sw128(smem_u32(zr_at(0, ks >> 2) + (ks & 3) * 32), 16, 1024), id_qz,
+                                       ks > 0);
                             }
                         }
                         mma_commit(&a_full[ab]);
@@ -350,13 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         LA_TR(1, 4, i);
                     }
-                    if (n >= 1) {
-                        ok = mbar_wait(y_empty, (n - 1) & 1, err, kErrYEmpty);
+                    if (n >= NY) {
+                        ok = mbar_wait(&y_empty[yb], ((n / NY) & 1) ^ 1, err, kErrYEmpty);
                         if (!ok) break;
                         tc_fence_after();
                         LA_TR(1, 5, n);
                     }
                     // inter: Y^T = S_prev^T(hi + lo) . Q^T
+                    const uint32_t tY = tmem + Cf::kColY + 64 * yb;
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
                         const uint64_t bq = sdesc_sw128(smem_u32(qop + ko), 16, 1024);
@@ -376,15 +393,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         tc_fence_after();
                         LA_TR(1, 7, n);
-                        // intra: Y^T += V^T . A^T (hi + lo)
+                        // intra: Y^T += V^T . A^T (hi + lo).  The masked-score buffer is
+                        // free again for item n + 1 once its scores complete, because
+                        // tensor-core operations complete in issue order.
                         for (int ks = 0; ks < kC / 16; ++ks) {
                             const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
                             mma_ss(tY, av, sdesc_sw128(smem_u32(ATh + ks * 32), 16, 1024), id_intra, 1);
                             mma_ss(tY, av, sdesc_sw128(smem_u32(ATl + ks * 32), 16, 1024), id_intra, 1);
                         }
-                        mma_commit(at_empty);
                     }
-                    mma_commit(y_full);
+                    mma_commit(&y_full[yb]);
                     LA_TR(1, 8, n);
                 }
                 if (!ok) break;
@@ -392,36 +410,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp < kEpiWarp0) {
-        // ------------------------------------------------------------ converters
-        constexpr int kCPR = Cf::kCPR, kRowStep = Cf::kRowStep, kPer = Cf::kPer;
-        const int ct = tid - kConvWarp0 * 32;  // 0..127
-        const int quad = warp & 3;             // TMEM lane quadrant of this warp
-        const int cc = ct % kCPR;              // 16-byte chunk column: features 8cc..8cc+7
-        const int rbase = ct / kCPR;           // rows rbase + kRowStep * m
+        // -------------------------------------------------------- state warps
+        // Own the carried state in TMEM: the start state, its bf16 hi/lo copy
+        // for each chunk's read-out (the only loop-carried hand-off), the
+        // per-chunk decay of the gated rule, and the final state.
+        const int quad = warp & 3;  // TMEM lane quadrant of this warp
+        const int st_t = tid - kStateWarp0 * 32;
         const bool m64 = D == 64;
         const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);  // value row of S^T in this lane
         const bool vrow_ok = m64 ? lane < 16 : true;
         bool ok = true;
-        uint32_t gphase = 0;
-        int zbuf = 0;
-        auto chunk_off = [&](int m) -> uint32_t {
-            const int row = rbase + kRowStep * m;
-            return static_cast<uint32_t>((cc >> 3) * 8192 + row * 128 + ((((cc & 7) ^ (row & 7))) << 4));
-        };
-        auto zr_off = [&](int row, int k) -> uint32_t {
-            return static_cast<uint32_t>((k >> 6) * 1024) + sw128_offset(row, (k & 63) * 2);
-        };
 
-        // zero the constant rows 2..7 of every Z-row block
-        if (NORM) {
-            const int nzr = MODE == kApply ? 1 : NKV;
-            for (int z = 0; z < nzr; ++z)
-                for (int e = ct; e < D * 6; e += 128) bf_at(Zr(z), zr_off(2 + e / D, e % D)) = __float2bfloat16(0.f);
-        }
-
-        // ---- start state -> S^T (fp32) in TMEM, Z -> register of thread k < D.
-        // Causal segment s > 0 folds the increments of segments 0..s-1 (from
-        // the state pass) onto the initial state, decay-weighted for gated.
+        // ---- start state -> S^T (fp32) in TMEM.  Causal segment s > 0 folds
+        // the increments of segments 0..s-1 (from the state pass) onto the
+        // initial state, decay-weighted for gated.
         const bool fold = MODE == kCausal && a.S_seg && seg > 0;
         const float* S_start = MODE == kState ? nullptr : a.S_init;
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -440,14 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tmem_addr(tmem + Cf::kColS, quad * 32, c0), r);
         }
         tmem_st_wait();
-        float zreg = 0.f;
-        if (NORM && ct < D && MODE != kState) {
-            zreg = a.Z_init ? a.Z_init[(size_t)bh * D + ct] : 0.f;
-            if (fold && a.Z_seg)
-                for (int p = 0; p < seg; ++p) zreg += a.Z_seg[((size_t)bh * nseg + p) * D + ct];
-        }
-        float gsum = 0.f;      // gated, state mode: total log decay of the segment
-        float gtot_cur = 0.f;  // gated: log decay of the chunk processed last by process_kv
+        float gsum = 0.f;  // gated, state mode: total log decay of the segment
 
         // ---- state hi/lo (and, gated, the decay of the fp32 state in place)
         auto convert_state = [&](float decay_mul, bool write_back) {
@@ -483,6 +478,221 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_st_wait();
         };
+        auto publish_state = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(state_ready);
+        };
+
+        if (MODE == kApply) {
+            // fixed global state: hi/lo once
+            tc_fence_after();
+            convert_state(1.f, false);
+            publish_state();
+        } else if (MODE == kState && !GATED) {
+            publish_state();  // the zero state is in place; updates accumulate without hand-offs
+        } else {
+            for (int i = 0; i < nck && ok; ++i) {
+                // S(i): after the update of chunk i-1 and every read-out that used S_prev
+                if (i > 0) {
+                    ok = warp_wait(state_done, (i - 1) & 1, err, kErrStateDone);
+                    if (!ok) break;
+                }
+                float gtot = 0.f;
+                if (GATED) {
+                    // the decay of chunk i comes with its converted keys
+                    const int s = i % NKV1;
+                    ok = warp_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
+                    if (!ok) break;
+                    gtot = Gc(s)[kC - 1];
+                }
+                tc_fence_after();
+                if (st_t == 0) LA_TR(2, 5, i);
+                convert_state(GATED ? __expf(gtot) : 1.f, GATED);
+                publish_state();
+                if (st_t == 0) LA_TR(2, 6, i);
+                if (MODE == kState) gsum += gtot;
+            }
+        }
+
+        // ---- final state out: causal (last segment) or every segment in state mode
+        const bool write_state =
+            ok && nck > 0 && ((MODE == kCausal && seg == nseg - 1 && a.S_dst) || MODE == kState);
+        if (write_state) {
+            // causal: phase nck-1 (one per chunk); non-gated state pass: its single phase
+            ok = warp_wait(state_done, (MODE == kState && !GATED) ? 0 : ((nck - 1) & 1), err, kErrStateDone);
+            tc_fence_after();
+            if (ok) {
+                float* Sd = MODE == kState ? a.S_dst + ((size_t)bh * nseg + seg) * D * D : a.S_dst + (size_t)bh * D * D;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem_addr(tmem + Cf::kColS, quad * 32, c0), r);
+                    tmem_ld_wait();
+                    reg_fence(r);
+                    if (vrow_ok)
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) Sd[(size_t)(c0 + x) * D + vrow] = __uint_as_float(r[x]);
+                }
+                if (MODE == kState && GATED && st_t == 0) a.G_dst[(size_t)bh * nseg + seg] = gsum;
+            }
+        }
+    } else if (warp < kFeatWarp0) {
+        // -------------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const bool m64 = D == 64;
+        const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);  // value index of this Y^T lane
+        const bool vrow_ok = m64 ? lane < 16 : true;
+        const int arow = quad * 16 + lane;  // score row (M = 64 layout: lanes 0-15 of each quadrant)
+        const bool arow_ok = lane < 16;
+        const int n_total = Cf::kHasQ ? nck * G : 0;
+        bool ok = true;
+        uint32_t gphase = 0;
+        for (int n = 0; n <= n_total && ok; ++n) {
+            if (n < n_total) {
+                // -------- scores of item n: mask, decay, hi/lo split, 1/den
+                const int ab = n % NA;
+                const int s = (n / G) % NKV1;
+                float den = 1.f;
+                if (MODE == kCausal || NORM) {
+                    ok = warp_wait(&a_full[ab], (n / NA) & 1, err, kErrAFull);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 1, n);
+                    const uint32_t tA = tmem + Cf::kColA + 80 * ab;
+                    uint32_t r[32], r2[32], z[16];
+                    if (MODE == kCausal) {
+                        tmem_ld32(tmem_addr(tA, quad * 32, 0), r);
+                        tmem_ld32(tmem_addr(tA, quad * 32, 32), r2);
+                    }
+                    if (NORM) tmem_ld16(tmem_addr(tA, quad * 32, 64), z);
+                    tmem_ld_wait();
+                    if (MODE == kCausal) {
+                        reg_fence(r);
+                        reg_fence(r2);
+                    }
+                    if (NORM) reg_fence(z);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_empty[ab]);  // TMEM scores read out
+                    if (NORM) den = __uint_as_float(z[0]) + __uint_as_float(z[1]) + eps;
+                    if (MODE == kCausal) {
+                        // the masked-score buffer is free: the intra product of item n - 1
+                        // was issued before the scores of item n and has completed with them
+                        if (arow_ok) {
+                            const float* gc = reinterpret_cast<const float*>(Gc(s));
+                            const float gi = GATED ? gc[arow] : 0.f;
+#pragma unroll
+                            for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
+                                const uint32_t off = sw128_offset(arow, cch * 16);
+                                if (cch * 8 > arow) {  // entirely above the diagonal
+                                    *reinterpret_cast<uint4*>(ATh + off) = make_uint4(0, 0, 0, 0);
+                                    *reinterpret_cast<uint4*>(ATl + off) = make_uint4(0, 0, 0, 0);
+                                    continue;
+                                }
+                                float v[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const int j = cch * 8 + e;
+                                    float x = j < 32 ? __uint_as_float(r[j]) : __uint_as_float(r2[j - 32]);
+                                    x = (j <= arow) ? x : 0.f;
+                                    if (NORM) den += x;
+                                    if (GATED && j <= arow) x *= __expf(gi - gc[j]);
+                                    v[e] = x;
+                                }
+                                uint4 hv, lv;
+                                split8(v, hv, lv);
+                                *reinterpret_cast<uint4*>(ATh + off) = hv;
+                                *reinterpret_cast<uint4*>(ATl + off) = lv;
+                            }
+                        }
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(at_full);
+                        if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 2, n);
+                    }
+                }
+                if (arow_ok) inv_den[(n & 3) * 64 + arow] = NORM ? scale / den : scale;
+            }
+            if (n >= 1) {
+                // -------- output of item m = n - 1, stored straight to global memory
+                const int m = n - 1;
+                const int i_chunk = m / G, r_head = m - i_chunk * G;
+                const int t0 = (c_begin + i_chunk) * kC;
+                const int valid = min(kC, T - t0);
+                const int yb = m % NY;
+                ok = warp_wait(&y_full[yb], (m / NY) & 1, err, kErrYFull);
+                if (!ok) break;
+                tc_fence_after();
+                if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 3, m);
+                uint32_t y0[32], y1[32];
+                tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 0), y0);
+                tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 32), y1);
+                tmem_ld_wait();
+                reg_fence(y0);
+                reg_fence(y1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&y_empty[yb]);
+                // 1/den of item m was written by all four warps one iteration ago
+                ok = group_sync(epi_group, gphase, err, kErrYFull);
+                if (!ok) break;
+                if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 4, m);
+                const float* idn = inv_den + (m & 3) * 64;
+                if (vrow_ok) {
+                    const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
+                    const size_t tstride = (size_t)Hq * D;
+#pragma unroll
+                    for (int x = 0; x < 64; ++x) {
+                        if (x < valid) {
+                            const float v = (x < 32 ? __uint_as_float(y0[x]) : __uint_as_float(y1[x - 32])) * idn[x];
+                            if (OUT_BF16)
+                                reinterpret_cast<__nv_bfloat16*>(yout)[base + x * tstride] = __float2bfloat16_rn(v);
+                            else
+                                reinterpret_cast<float*>(yout)[base + x * tstride] = v;
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------ feature warps
+        // Feature maps of keys and queries in shared memory (bf16 hi, lo part
+        // of the keys for the state update), decayed copies for the gated
+        // rule, the Z rows of every chunk and the running key sum Z.  Runs
+        // ahead of the state chain, limited only by the load rings.
+        constexpr int kCPR = Cf::kCPR, kRowStep = Cf::kRowStep, kPer = Cf::kPer;
+        const int ct = tid - kFeatWarp0 * 32;  // 0..127
+        const int cc = ct % kCPR;              // 16-byte chunk column: features 8cc..8cc+7
+        const int rbase = ct / kCPR;           // rows rbase + kRowStep * m
+        bool ok = true;
+        uint32_t gphase = 0;
+        int zbuf = 0;
+        // 16-byte chunk m of this thread in a swizzled 64 x D tile whose
+        // 64-feature blocks are `blk` bytes apart
+        auto chunk_off = [&](int m, int blk = 8192) -> uint32_t {
+            const int row = rbase + kRowStep * m;
+            return static_cast<uint32_t>((cc >> 3) * blk + row * 128 + ((((cc & 7) ^ (row & 7))) << 4));
+        };
+        // element (Z row r, feature k) of the Z rows of stage s
+        auto zr_elem = [&](int s, int r, int k) -> __nv_bfloat16& {
+            return bf_at(zr_at(s, k >> 6), sw128_offset(r, (k & 63) * 2));
+        };
+
+        // zero the constant rows 2..7 of every Z-row block
+        if (NORM && MODE != kState) {
+            const int nzr = MODE == kApply ? 1 : NKV;
+            for (int z = 0; z < nzr; ++z)
+                for (int e = ct; e < D * 6; e += 128) zr_elem(z, 2 + e / D, e % D) = __float2bfloat16(0.f);
+        }
+        // running key sum Z in a register of thread k < D (state pass: the increment)
+        float zreg = 0.f;
+        if (NORM && ct < D && MODE != kState) {
+            const bool fold = MODE == kCausal && a.S_seg && seg > 0;
+            zreg = a.Z_init ? a.Z_init[(size_t)bh * D + ct] : 0.f;
+            if (fold && a.Z_seg)
+                for (int p = 0; p < seg; ++p) zreg += a.Z_seg[((size_t)bh * nseg + p) * D + ct];
+        }
 
         // ---- keys of chunk i: feature map (+ lo part), decayed keys, Z rows and sums
         auto process_kv = [&](int i) -> bool {
@@ -518,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (touch) {
                 uint4 in[kPer];
 #pragma unroll
-                for (int m = 0; m < kPer; ++m) in[m] = *reinterpret_cast<const uint4*>(Kb(s) + chunk_off(m));
+                for (int m = 0; m < kPer; ++m) in[m] = *reinterpret_cast<const uint4*>(Kb(s) + chunk_off(m, Cf::kKBlk));
                 float colsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int m = 0; m < kPer; ++m) {
@@ -538,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 8; ++e) f[e] = phi<true>(fmap, f[e], eps);
                         if (fmap != LA_FMAP_NONE || SPLITK) {
                             split8(f, hi, lo);
-                            if (fmap != LA_FMAP_NONE) *reinterpret_cast<uint4*>(Kb(s) + chunk_off(m)) = hi;
+                            if (fmap != LA_FMAP_NONE) *reinterpret_cast<uint4*>(Kb(s) + chunk_off(m, Cf::kKBlk)) = hi;
                             if (SPLITK) *reinterpret_cast<uint4*>(Klo(s) + chunk_off(m)) = lo;
                         }
                         if (NORM && row < valid)
@@ -559,8 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ct < D) {
                         if (MODE != kState) {
                             const __nv_bfloat16 h = __float2bfloat16_rn(zreg);
-                            bf_at(Zr(s), zr_off(0, ct)) = h;
-                            bf_at(Zr(s), zr_off(1, ct)) = __float2bfloat16_rn(zreg - __bfloat162float(h));
+                            zr_elem(s, 0, ct) = h;
+                            zr_elem(s, 1, ct) = __float2bfloat16_rn(zreg - __bfloat162float(h));
                         }
                         float add = 0.f;
 #pragma unroll
@@ -570,7 +780,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     zbuf ^= 1;
                 }
             }
-            gtot_cur = gtot;
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&conv_kv[s]);
@@ -611,193 +820,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        auto publish_state = [&]() {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(state_ready);
-        };
 
-        const int nq_ahead = MODE == kState ? 0 : min(G, NQ);  // query items converted one chunk ahead
         if (MODE == kApply) {
-            // fixed global state: hi/lo once; Z rows from the global key state
-            tc_fence_after();
-            convert_state(1.f, false);
+            // Z rows from the global key sum; then every query item in order
             if (NORM && ct < D) {
                 const __nv_bfloat16 h = __float2bfloat16_rn(zreg);
-                bf_at(Zr(0), zr_off(0, ct)) = h;
-                bf_at(Zr(0), zr_off(1, ct)) = __float2bfloat16_rn(zreg - __bfloat162float(h));
+                zr_elem(0, 0, ct) = h;
+                zr_elem(0, 1, ct) = __float2bfloat16_rn(zreg - __bfloat162float(h));
             }
             fence_proxy_async();
-            publish_state();
             for (int n = 0; n < nck * G && ok; ++n) ok = process_q(n / G, n);
         } else {
-            // prologue: chunk 0 ahead of the loop
-            if (nck > 0) ok = process_kv(0);
-            for (int r = 0; r < nq_ahead && ok; ++r) ok = process_q(0, r);
-            if (MODE == kState && !GATED) publish_state();  // the zero state is in place
-            float gtot_next = gtot_cur;  // decay of the next chunk whose state is converted
+            // keys of chunk i, then its query heads, chunk after chunk
             for (int i = 0; i < nck && ok; ++i) {
-                const float gtot_i = gtot_next;
-                if (MODE == kCausal || GATED) {
-                    // S(i): after the update of chunk i-1 (and every read-out that used S_prev)
-                    if (i > 0) {
-                        ok = warp_wait(state_done, (i - 1) & 1, err, kErrStateDone);
-                        if (!ok) break;
-                    }
-                    tc_fence_after();
-                    if (ct == 0) LA_TR(2, 5, i);
-                    convert_state(GATED ? __expf(gtot_i) : 1.f, GATED);
-                    publish_state();
-                    if (ct == 0) LA_TR(2, 6, i);
-                    if (MODE == kState) gsum += gtot_i;
-                }
-                for (int r = nq_ahead; r < G && ok && MODE == kCausal; ++r) ok = process_q(i, i * G + r);
-                if (!ok) break;
-                if (i + 1 < nck) {
-                    ok = process_kv(i + 1);
-                    gtot_next = gtot_cur;
-                    for (int r = 0; r < nq_ahead && ok; ++r) ok = process_q(i + 1, (i + 1) * G + r);
-                }
+                ok = process_kv(i);
+                if (MODE == kCausal)
+                    for (int r = 0; r < G && ok; ++r) ok = process_q(i, i * G + r);
             }
-        }
-
-        // ---- final state out: causal (last segment) or every segment in state mode
-        const bool write_state =
-            ok && nck > 0 && ((MODE == kCausal && seg == nseg - 1 && a.S_dst) || MODE == kState);
-        if (write_state) {
-            // causal: phase nck-1 (one per chunk); non-gated state pass: its single phase
-            ok = warp_wait(state_done, (MODE == kState && !GATED) ? 0 : ((nck - 1) & 1), err, kErrStateDone);
-            tc_fence_after();
-            if (ok) {
-                float* Sd = MODE == kState ? a.S_dst + ((size_t)bh * nseg + seg) * D * D : a.S_dst + (size_t)bh * D * D;
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem_addr(tmem + Cf::kColS, quad * 32, c0), r);
-                    tmem_ld_wait();
-                    reg_fence(r);
-                    if (vrow_ok)
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) Sd[(size_t)(c0 + x) * D + vrow] = __uint_as_float(r[x]);
-                }
-                if (NORM && ct < D && a.Z_dst)
-                    (MODE == kState ? a.Z_dst + ((size_t)bh * nseg + seg) * D : a.Z_dst + (size_t)bh * D)[ct] = zreg;
-                if (MODE == kState && GATED && ct == 0) a.G_dst[(size_t)bh * nseg + seg] = gsum;
-            }
-        }
-    } else {
-        // -------------------------------------------------------------- epilogue
-        const int quad = warp & 3;
-        const bool m64 = D == 64;
-        const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);  // value index of this Y^T lane
-        const bool vrow_ok = m64 ? lane < 16 : true;
-        const int arow = quad * 16 + lane;  // score row (M = 64 layout: lanes 0-15 of each quadrant)
-        const bool arow_ok = lane < 16;
-        const int n_total = Cf::kHasQ ? nck * G : 0;
-        bool ok = true;
-        uint32_t gphase = 0;
-        for (int n = 0; n <= n_total && ok; ++n) {
-            if (n < n_total) {
-                // -------- scores of item n: mask, decay, hi/lo split, 1/den
-                const int ab = n & 1;
-                const int s = (n / G) % NKV1;
-                float den = 1.f;
-                if (MODE == kCausal || NORM) {
-                    ok = warp_wait(&a_full[ab], (n >> 1) & 1, err, kErrAFull);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 1, n);
-                    const uint32_t tA = tmem + Cf::kColA + 80 * ab;
-                    uint32_t r[32], r2[32], z[16];
-                    if (MODE == kCausal) {
-                        tmem_ld32(tmem_addr(tA, quad * 32, 0), r);
-                        tmem_ld32(tmem_addr(tA, quad * 32, 32), r2);
-                    }
-                    if (NORM) tmem_ld16(tmem_addr(tA, quad * 32, 64), z);
-                    tmem_ld_wait();
-                    if (MODE == kCausal) {
-                        reg_fence(r);
-                        reg_fence(r2);
-                    }
-                    if (NORM) reg_fence(z);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_empty[ab]);  // TMEM scores read out
-                    if (NORM) den = __uint_as_float(z[0]) + __uint_as_float(z[1]) + eps;
-                    if (MODE == kCausal) {
-                        if (n >= 1) {
-                            ok = warp_wait(at_empty, (n - 1) & 1, err, kErrATEmpty);
-                            if (!ok) break;
-                        }
-                        if (arow_ok) {
-                            const float* gc = reinterpret_cast<const float*>(Gc(s));
-                            const float gi = GATED ? gc[arow] : 0.f;
-#pragma unroll
-                            for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
-                                float v[8];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const int j = cch * 8 + e;
-                                    float x = j < 32 ? __uint_as_float(r[j]) : __uint_as_float(r2[j - 32]);
-                                    x = (j <= arow) ? x : 0.f;
-                                    if (NORM) den += x;
-                                    if (GATED && j <= arow) x *= __expf(gi - gc[j]);
-                                    v[e] = x;
-                                }
-                                uint4 hv, lv;
-                                split8(v, hv, lv);
-                                const uint32_t off = sw128_offset(arow, cch * 16);
-                                *reinterpret_cast<uint4*>(ATh + off) = hv;
-                                *reinterpret_cast<uint4*>(ATl + off) = lv;
-                            }
-                        }
-                        fence_proxy_async();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(at_full);
-                        if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 2, n);
-                    }
-                }
-                if (arow_ok) inv_den[(n & 3) * 64 + arow] = NORM ? scale / den : scale;
-            }
-            if (n >= 1) {
-                // -------- output of item m = n - 1, stored straight to global memory
-                const int m = n - 1;
-                const int i_chunk = m / G, r_head = m - i_chunk * G;
-                const int t0 = (c_begin + i_chunk) * kC;
-                const int valid = min(kC, T - t0);
-                ok = warp_wait(y_full, m & 1, err, kErrYFull);
-                if (!ok) break;
-                tc_fence_after();
-                if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 3, m);
-                uint32_t y0[32], y1[32];
-                tmem_ld32(tmem_addr(tmem + Cf::kColY, quad * 32, 0), y0);
-                tmem_ld32(tmem_addr(tmem + Cf::kColY, quad * 32, 32), y1);
-                tmem_ld_wait();
-                reg_fence(y0);
-                reg_fence(y1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(y_empty);
-                // 1/den of item m was written by all four warps one iteration ago
-                ok = group_sync(epi_group, gphase, err, kErrYFull);
-                if (!ok) break;
-                if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 4, m);
-                const float* idn = inv_den + (m & 3) * 64;
-                if (vrow_ok) {
-                    const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
-                    const size_t tstride = (size_t)Hq * D;
-#pragma unroll
-                    for (int x = 0; x < 64; ++x) {
-                        if (x < valid) {
-                            const float v = (x < 32 ? __uint_as_float(y0[x]) : __uint_as_float(y1[x - 32])) * idn[x];
-                            if (OUT_BF16)
-                                reinterpret_cast<__nv_bfloat16*>(yout)[base + x * tstride] = __float2bfloat16_rn(v);
-                            else
-                                reinterpret_cast<float*>(yout)[base + x * tstride] = v;
-                        }
-                    }
-                }
-            }
+            // key sum: final (causal, last segment) or this segment's increment (state pass)
+            const bool write_z = ok && nck > 0 && NORM && ct < D && a.Z_dst &&
+                                 ((MODE == kCausal && seg == nseg - 1) || MODE == kState);
+            if (write_z)
+                (MODE == kState ? a.Z_dst + ((size_t)bh * nseg + seg) * D : a.Z_dst + (size_t)bh * D)[ct] = zreg;
         }
     }
 

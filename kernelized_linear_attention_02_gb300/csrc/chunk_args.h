@@ -40,7 +40,7 @@ struct Args {
 // One launch of the chunk kernel: variant selectors, grid, arguments, tensor maps.
 struct Launch {
     int mode;
-    bool norm, splitk, gated, out_bf16;
+    bool norm, gated, out_bf16;
     dim3 grid;
     Args args;
     CUtensorMap mq, mk, mv;
@@ -48,7 +48,11 @@ struct Launch {
 
 }  // namespace chunk
 
-cudaError_t chunk_run_d64(const chunk::Launch& L, cudaStream_t st);
-cudaError_t chunk_run_d128(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_causal_d64_bf16(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_causal_d64_f32(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_causal_d128_bf16(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_causal_d128_f32(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_other_d64(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_other_d128(const chunk::Launch& L, cudaStream_t st);
 
 }  // namespace la

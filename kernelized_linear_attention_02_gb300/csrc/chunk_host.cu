@@ -125,7 +125,11 @@ bool act_map(CUtensorMap* m, const void* base, int D, int H, int64_t T, int64_t 
 }
 
 cudaError_t run(const chunk::Launch& L, int D, cudaStream_t st) {
-    return D == 64 ? chunk_run_d64(L, st) : chunk_run_d128(L, st);
+    if (L.mode == chunk::kCausal) {
+        if (D == 64) return L.out_bf16 ? chunk_run_causal_d64_bf16(L, st) : chunk_run_causal_d64_f32(L, st);
+        return L.out_bf16 ? chunk_run_causal_d128_bf16(L, st) : chunk_run_causal_d128_f32(L, st);
+    }
+    return D == 64 ? chunk_run_other_d64(L, st) : chunk_run_other_d128(L, st);
 }
 
 chunk::Launch base_launch(const Problem& P, int mode, const DevInfo& di) {
@@ -134,7 +138,6 @@ chunk::Launch base_launch(const Problem& P, int mode, const DevInfo& di) {
     L.mode = mode;
     L.norm = P.norm != 0;
     L.gated = P.gated != 0;
-    L.splitk = P.gated || P.fmap == LA_FMAP_ELU_PLUS_ONE;
     L.out_bf16 = P.out_bf16 != 0;
     chunk::Args& a = L.args;
     a.B = (int)P.B;

@@ -1,6 +1,6 @@
 // chunk_launch.cuh -- instantiates the tensor-core chunk kernel for one head
-// size D (included by chunk_d64.cu and chunk_d128.cu, so the two sizes
-// compile in parallel).
+// size D and one group of modes (included by chunk_d{64,128}_{causal,other}.cu,
+// so the variants compile in parallel translation units).
 #pragma once
 
 #include "chunk.cuh"
@@ -9,10 +9,10 @@
 namespace la {
 namespace chunk {
 
-template <int D, int MODE, bool NORM, bool SPLITK, bool GATED, bool OUTBF>
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUTBF>
 cudaError_t run_one(const Launch& L, cudaStream_t st) {
-    using Cf = Cfg<D, MODE, NORM, SPLITK, GATED, OUTBF>;
-    auto kern = chunk_kernel<D, MODE, NORM, SPLITK, GATED, OUTBF>;
+    using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUTBF>;
+    auto kern = chunk_kernel<D, MODE, NORM, FMAP, GATED, OUTBF>;
     static int configured = -1;  // device on which the shared-memory limit was raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -27,32 +27,27 @@ cudaError_t run_one(const Launch& L, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <int D, int MODE, bool NORM, bool SPLITK, bool GATED>
-cudaError_t run_out(const Launch& L, cudaStream_t st) {
-    if (MODE == kState) return run_one<D, MODE, NORM, SPLITK, GATED, true>(L, st);
-    return L.out_bf16 ? run_one<D, MODE, NORM, SPLITK, GATED, true>(L, st)
-                      : run_one<D, MODE, NORM, SPLITK, GATED, false>(L, st);
-}
-
-template <int D, int MODE>
-cudaError_t run_mode(const Launch& L, cudaStream_t st) {
-    if (MODE == kApply) {
-        return L.norm ? run_out<D, MODE, true, false, false>(L, st) : run_out<D, MODE, false, false, false>(L, st);
+// OUT: 1 = bf16 output, 0 = float32 output (the state pass writes no output)
+template <int D, int MODE, int OUT>
+struct Dispatch {
+    template <bool NORM, int FMAP, bool GATED>
+    static cudaError_t one(const Launch& L, cudaStream_t st) {
+        return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1>(L, st);
     }
-    if (L.gated) return run_out<D, MODE, false, true, true>(L, st);
-    if (L.norm)
-        return L.splitk ? run_out<D, MODE, true, true, false>(L, st) : run_out<D, MODE, true, false, false>(L, st);
-    return L.splitk ? run_out<D, MODE, false, true, false>(L, st) : run_out<D, MODE, false, false, false>(L, st);
-}
-
-template <int D>
-cudaError_t run_d(const Launch& L, cudaStream_t st) {
-    switch (L.mode) {
-    case kCausal: return run_mode<D, kCausal>(L, st);
-    case kState: return run_mode<D, kState>(L, st);
-    default: return run_mode<D, kApply>(L, st);
+    template <bool NORM>
+    static cudaError_t fmap(const Launch& L, cudaStream_t st) {
+        switch (L.args.fmap) {
+        case LA_FMAP_ELU_PLUS_ONE: return one<NORM, LA_FMAP_ELU_PLUS_ONE, false>(L, st);
+        case LA_FMAP_RELU_EPS: return one<NORM, LA_FMAP_RELU_EPS, false>(L, st);
+        default: return one<NORM, LA_FMAP_NONE, false>(L, st);
+        }
     }
-}
+    static cudaError_t run(const Launch& L, cudaStream_t st) {
+        // the gated rule is defined without a feature map or normalizer
+        if (MODE != kApply && L.gated) return one<false, LA_FMAP_NONE, true>(L, st);
+        return L.norm ? fmap<true>(L, st) : fmap<false>(L, st);
+    }
+};
 
 }  // namespace chunk
 }  // namespace la
