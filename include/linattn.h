@@ -121,6 +121,40 @@ la_status la_forward_causal(const la_params* p, const void* q, const void* k, co
                             float* S_out, float* Z_out, void* ws, size_t ws_bytes,
                             la_stream_t stream);
 
+/* Size of the scratch built into the library for la_forward_causal_noalloc:
+ * 16 MiB of device memory, reserved once per device when the library's
+ * device code is loaded there. */
+#define LA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* la_forward_causal without a caller workspace.  The methods on the pages
+ * have no counterpart to this call: it exists for callers that cannot hand
+ * the library device memory -- for example a plug-in inside a host program
+ * that owns every device allocation and offers no scratch, or a
+ * latency-critical loop that must not call cudaMalloc (which can synchronize
+ * the device) or an allocator between steps.
+ *
+ * Arguments, results and numerics are those of la_forward_causal; the
+ * scratch that call would take from `ws` comes from one buffer of
+ * LA_NOALLOC_SCRATCH_BYTES compiled into the library (one per device).
+ *  - No device memory is allocated or freed by this call, and it calls no
+ *    library routine that allocates.
+ *  - The first call on a device, made with that device current, looks up the
+ *    buffer's address (cudaGetSymbolAddress) and configures the kernels;
+ *    make that first call before any stream capture starts on the device.
+ *  - Nothing in the buffer has to start at zero: every byte a call reads
+ *    was written earlier in the same call.
+ *  - The buffer is shared by all calls on one device: two calls that may run
+ *    at the same time (different streams, or different host threads without
+ *    ordering between them) race on it and give wrong results.  Calls issued
+ *    one after another on one stream are safe.
+ *  - LA_ERR_WORKSPACE when the problem needs more scratch than
+ *    LA_NOALLOC_SCRATCH_BYTES (la_workspace_bytes(p, 1) tells how much);
+ *    use la_forward_causal with a caller workspace for those.  On a GPU with
+ *    at most 152 SMs every causal problem fits. */
+la_status la_forward_causal_noalloc(const la_params* p, const void* q, const void* k, const void* v,
+                                    const void* decay, const float* S0, const float* Z0, void* y,
+                                    float* S_out, float* Z_out, la_stream_t stream);
+
 /* Non-causal attention with the global state (Keras request, Mathematical
  * definition / Non-causal).  No state in or out ("Non-causal attention does
  * not expose streaming state").  Only the linear rule. */

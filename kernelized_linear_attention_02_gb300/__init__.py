@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "liblinattn.so")
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA = range(5)
 LA_F32, LA_BF16 = 0, 1
+LA_NOALLOC_SCRATCH_BYTES = 16 << 20  # built-in scratch of la_forward_causal_noalloc
 FEATURE_MAPS = {"none": 0, "elu_plus_one": 1, "relu": 2}
 UPDATE_RULES = {"linear": 0, "gated": 1}
 _DTYPES = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
@@ -49,6 +50,7 @@ _SIGNATURES = {
     "la_get_initial_state": (ctypes.c_int, [ctypes.POINTER(la_params), _vp, _vp, _vp]),
     "la_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(la_params), ctypes.c_int]),
     "la_forward_causal": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 10 + [ctypes.c_size_t, _vp]),
+    "la_forward_causal_noalloc": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 10),
     "la_forward_noncausal": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 5 + [ctypes.c_size_t, _vp]),
     "la_decode_step": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 8),
     "la_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -180,6 +182,25 @@ def la_forward_causal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one",
                                    _ptr(Z0), _ptr(y), _ptr(S), _ptr(Z), _ptr(ws), ws_bytes,
                                    _stream(stream)))
     return (y, (S, Z)) if return_state else y
+
+
+def la_forward_causal_noalloc(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one",
+                              use_normalizer=True, epsilon=1e-6, scale=1.0, update_rule="linear", decay=None,
+                              initial_state=None, out, state_out=None, stream=None):
+    """la_forward_causal on the library's built-in scratch: the caller passes
+    every output buffer (``out`` and, to get the final state, ``state_out``),
+    so neither this wrapper nor the library allocates device memory.  Calls
+    that may overlap on one device race on the shared scratch."""
+    q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=out.dtype, feature_map=feature_map,
+                       use_normalizer=use_normalizer, epsilon=epsilon, scale=scale,
+                       update_rule=update_rule)
+    if decay is not None and (not decay.is_cuda or not decay.is_contiguous() or decay.dtype != q.dtype):
+        raise ValueError("decay must be a contiguous CUDA tensor of the io dtype")
+    S0, Z0 = initial_state if initial_state is not None else (None, None)
+    S, Z = state_out if state_out is not None else (None, None)
+    _check(lib().la_forward_causal_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(S0),
+                                           _ptr(Z0), _ptr(out), _ptr(S), _ptr(Z), _stream(stream)))
+    return out
 
 
 def la_forward_noncausal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one", use_normalizer=True,

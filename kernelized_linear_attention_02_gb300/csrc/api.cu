@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "kernels.h"
@@ -108,6 +109,32 @@ la_status check_ws(const la::Problem& P, bool causal, void* ws, size_t ws_bytes)
     return LA_OK;
 }
 
+// Scratch of la_forward_causal_noalloc: one buffer per device, part of the
+// library's device image, so using it needs no allocation at call time.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_noalloc_scratch on the current device, looked up on
+// the first call per device and cached.
+cudaError_t noalloc_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = ptr;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -181,6 +208,28 @@ la_status la_forward_causal(const la_params* p, const void* q, const void* k, co
     if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal");
     g_last_error.clear();
     return LA_OK;
+}
+
+la_status la_forward_causal_noalloc(const la_params* p, const void* q, const void* k, const void* v,
+                                    const void* decay, const float* S0, const float* Z0, void* y,
+                                    float* S_out, float* Z_out, la_stream_t stream) {
+    la::Problem P;
+    la_status st = make_problem(p, Call::kCausal, &P);
+    if (st != LA_OK) return st;
+    if (P.T == 0) return la_forward_causal(p, q, k, v, decay, S0, Z0, y, S_out, Z_out, nullptr, 0, stream);
+    const size_t need = workspace_bytes(P, true);
+    if (need > LA_NOALLOC_SCRATCH_BYTES)
+        return fail(LA_ERR_WORKSPACE,
+                    "la_forward_causal_noalloc: this problem needs %zu bytes of scratch, more than the %zu "
+                    "built in; call la_forward_causal with a workspace instead",
+                    need, (size_t)LA_NOALLOC_SCRATCH_BYTES);
+    void* ws = nullptr;
+    if (need > 0) {
+        cudaError_t e = noalloc_scratch(&ws);
+        if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal_noalloc: scratch address");
+    }
+    return la_forward_causal(p, q, k, v, decay, S0, Z0, y, S_out, Z_out, ws, need > 0 ? LA_NOALLOC_SCRATCH_BYTES : 0,
+                             stream);
 }
 
 la_status la_forward_noncausal(const la_params* p, const void* q, const void* k, const void* v, void* y,
