@@ -19,25 +19,30 @@
 // exp(G_i - G_j) (<= 1), and the carry is S <- exp(G_C) S + sum_j
 // exp(G_C - G_j) k_j v_j^T.
 //
-// Precision: phi(Q) and phi(K) enter the tensor cores as bf16; the masked
-// score matrix and the carried state are split into bf16 hi + lo parts, so
-// that both reach the tensor cores with ~16 significant bits; the state
-// update uses a hi + lo split of the key operand whenever phi(k) (or the
-// decayed key) is not exactly representable in bf16.  All accumulation is
-// fp32 in tensor memory.
+// Precision: phi(Q) and phi(K) enter the score product as bf16; the masked
+// score matrix is split into bf16 hi + lo parts (~16 significant bits); the
+// read-out with the carried state uses the fp32 state in tensor memory
+// directly at tf32 precision (linear rule) or a bf16 hi + lo copy of it
+// (gated rule, whose state is rescaled every chunk); the state update uses a
+// hi + lo split of the key operand whenever phi(k) (or the decayed key) is
+// not exactly representable in bf16.  All accumulation is fp32 in tensor
+// memory.
 //
 // Roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-5 state (hi/lo copy of the carried state in TMEM, gated
-// decay), warps 6-9 epilogue (masking of the scores, output normalisation
-// and store), warps 10-13 feature maps (phi of keys and queries, hi/lo
-// splits, Z rows and sums).  Every wait is bounded and reports a code in
+// owner, warps 2-5 state (start and final state; gated rule: hi/lo copy of
+// the carried state and its decay; linear rule: the output stage), warps
+// 6-9 epilogue (masking of the scores, 1/den; gated rule: also the output
+// stage), warps 10-13 feature maps (phi of keys and queries, Z rows and
+// sums).  Every wait is bounded and reports a code in
 // *err instead of hanging.
 //
 // Pipeline per chunk i (G query heads per kv head): the feature warps run
 // ahead of the tensor core, limited only by the load rings; the MMA issues
 // per head the scores and the read-out with S_prev, after the last head's
-// read-out the state update, then the intra term; so the only loop-carried
-// chain is state hi/lo(i) -> read-out(i) -> update(i) -> state hi/lo(i+1).
+// read-out the state update, then the intra term.  Linear rule: the only
+// loop-carried chain is read-out(i) -> update(i) -> read-out(i+1), ordered by
+// the MMA issuer alone; gated rule: state hi/lo(i) -> read-out(i) ->
+// update(i) -> state hi/lo(i+1) through the state warps.
 //
 // Modes: kCausal (outputs + carried state), kState (only the state update
 // over a segment, for the two-pass sequence split and the non-causal
@@ -60,9 +65,10 @@ constexpr int kStateWarp0 = 2, kEpiWarp0 = 6, kFeatWarp0 = 10;
 
 template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16>
 struct Cfg {
-    // the state update needs a lo part of its key operand when phi(k) (elu+1)
-    // or the decayed key (gated) is not exactly representable in bf16
-    static constexpr bool kSplitK = GATED || FMAP == LA_FMAP_ELU_PLUS_ONE;
+    // the gated state update takes its decayed keys as bf16 hi + lo; the
+    // linear rule's keys enter as bf16 alone (phi(k) of elu+1 is rounded: its
+    // effect on the output stays near 1e-4 relative)
+    static constexpr bool kSplitK = GATED;
     static constexpr bool kHasKV = MODE != kApply;
     static constexpr bool kHasQ = MODE != kState;
     static constexpr int kTile = D * 128;  // 64 rows x D bf16 (D/64 swizzled blocks of 8 KB)
@@ -78,8 +84,17 @@ struct Cfg {
     static constexpr int kOffVb = kOffKlo + (kSplitK ? kTile : 0);
     static constexpr int kOffG = kOffVb + kTile;
     static constexpr int kKvStage = kHasKV ? kOffG + 1024 : 0;
-    static constexpr int kQStage = kHasQ ? kTile * (GATED ? 2 : 1) : 0;
-    static constexpr int kAT = MODE == kCausal ? 2 * 8192 : 0;  // masked scores hi + lo, 64 x 64 each
+    // linear rule: the read-out with the carried state runs as kind::tf32
+    // with the fp32 state straight from TMEM as A, against an fp32 copy of
+    // phi(Q) (64 x D, D/32 swizzled blocks of 8 KB); the gated rule, whose
+    // state is rescaled every chunk anyway, reads a bf16 hi/lo copy of it
+    static constexpr bool kTf32 = !GATED;
+    static constexpr int kQf = (kHasQ && kTf32) ? 2 * kTile : 0;
+    static constexpr int kQStage = kHasQ ? kTile * (GATED ? 2 : 1) + kQf : 0;
+    // masked scores as bf16 hi + lo (one bf16 part suffices without the
+    // normalizer, where its rounding stays within ~5e-4 of the output)
+    static constexpr bool kALo = NORM || GATED;
+    static constexpr int kAT = MODE == kCausal ? 2 * 8192 : 0;  // hi, lo: 64 x 64 each
     static constexpr int kZrApply = (MODE == kApply && NORM) ? kZr : 0;
     static constexpr int kMisc = 12 * 1024;  // 1/den ring, partial Z sums, barriers
     static constexpr int bytes(int nkv, int nq) {
@@ -150,6 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap mapV) {
     using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>;
     constexpr bool SPLITK = Cf::kSplitK;
+    constexpr bool TF32 = Cf::kTf32;
+    constexpr bool ALO = Cf::kALo;
     constexpr int NA = Cf::kNA, NY = Cf::kNY;
     constexpr int NKV = Cf::kNKV, NQ = Cf::kNQ;
     constexpr int NKV1 = NKV ? NKV : 1, NQ1 = NQ ? NQ : 1;
@@ -176,12 +193,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* y_empty = bars + 19;   // [2]
     uint64_t* state_ready = bars + 21;
     uint64_t* state_done = bars + 22;
-    uint64_t* conv_group = bars + 23;  // barrier among the four converter warps
-    uint64_t* epi_group = bars + 24;   // barrier among the four epilogue warps
+    uint64_t* conv_group = bars + 23;  // barrier among the four feature warps
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 25);
+    uint64_t* inter_done = bars + 28;  // tf32 read-outs of a chunk complete (state may be updated)
+    uint64_t* final_done = bars + 29;  // every tensor-core operation of the CTA complete
+    // [4] scale/den of item n in inv_den[n & 3] (normalizer only).  Four
+    // phases in flight at most: the scores of item n + 4 are issued only
+    // after the output stage has read item n + 1 out of TMEM.
+    uint64_t* den_full = bars + 30;
 #ifdef LA_TRACE
-    unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 26);
-    if (threadIdx.x < 4) la_trace_ctr[threadIdx.x] = 0;
+    unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 40);
+    if (threadIdx.x < 8) la_trace_ctr[threadIdx.x] = 0;
 #endif
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -212,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto Gc = [&](int s) { return reinterpret_cast<float*>(kv_base + s * Cf::kKvStage + Cf::kOffG); };
     auto Qb = [&](int s) { return q_base + s * Cf::kQStage; };
     auto Qd = [&](int s) { return q_base + s * Cf::kQStage + Cf::kTile; };
+    auto Qf = [&](int s) { return q_base + s * Cf::kQStage + Cf::kTile; };  // fp32 phi(Q) (linear rule)
     uint8_t* ATh = at_base;
     uint8_t* ATl = at_base + 8192;
 
@@ -232,7 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(state_ready, 4);
         mbar_init(state_done, 1);
         mbar_init(conv_group, 4);
-        mbar_init(epi_group, 4);
+        for (int i = 0; i < 4; ++i) mbar_init(&den_full[i], 4);
+        mbar_init(inter_done, 1);
+        mbar_init(final_done, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -252,6 +277,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) LA_TR(0, 0, 0);
     const uint32_t tmem = *tmem_slot;
     unsigned* err = a.err;
+
+    // Output of item m (query head m % G of chunk m / G): Y^T from TMEM times
+    // scale/den, stored to global memory.  Run by four warps, one per TMEM lane
+    // quadrant: the state warps (linear rule) or the epilogue warps (gated).
+    auto emit_y = [&](int m) -> bool {
+        const int quad = warp & 3;
+        const bool m64 = D == 64;
+        const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);  // value index of this Y^T lane
+        const bool vrow_ok = m64 ? lane < 16 : true;
+        const int i_chunk = m / G, r_head = m - i_chunk * G;
+        const int t0 = (c_begin + i_chunk) * kC;
+        const int valid = min(kC, T - t0);
+        const int yb = m % NY;
+        if (!warp_wait(&y_full[yb], (m / NY) & 1, err, kErrYFull)) return false;
+        tc_fence_after();
+        if (quad == 0 && lane == 0) LA_TR(4, 3, m);
+        uint32_t y0[32], y1[32];
+        tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 0), y0);
+        tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 32), y1);
+        tmem_ld_wait();
+        reg_fence(y0);
+        reg_fence(y1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&y_empty[yb]);
+        // scale/den of item m, written by the four score warps
+        if (NORM && !warp_wait(&den_full[m & 3], (m >> 2) & 1, err, kErrYFull)) return false;
+        if (quad == 0 && lane == 0) LA_TR(4, 4, m);
+        if (vrow_ok) {
+            // all 64 factors into registers first: a shared load placed
+            // after a global store could not be moved ahead of it
+            float f[64];
+            const float4* idn4 = reinterpret_cast<const float4*>(inv_den + (m & 3) * 64);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                const float4 t = NORM ? idn4[x] : make_float4(scale, scale, scale, scale);
+                f[4 * x] = t.x;
+                f[4 * x + 1] = t.y;
+                f[4 * x + 2] = t.z;
+                f[4 * x + 3] = t.w;
+            }
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                f[x] *= __uint_as_float(y0[x]);
+                f[x + 32] *= __uint_as_float(y1[x]);
+            }
+            const size_t tstride = (size_t)Hq * D;
+            const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
+            if (OUT_BF16) {
+                __nv_bfloat16* yp = reinterpret_cast<__nv_bfloat16*>(yout) + base;
+                if (valid == kC) {
+#pragma unroll
+                    for (int x = 0; x < 64; ++x) yp[x * tstride] = __float2bfloat16_rn(f[x]);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 64; ++x)
+                        if (x < valid) yp[x * tstride] = __float2bfloat16_rn(f[x]);
+                }
+            } else {
+                float* yp = reinterpret_cast<float*>(yout) + base;
+                if (valid == kC) {
+#pragma unroll
+                    for (int x = 0; x < 64; ++x) yp[x * tstride] = f[x];
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 64; ++x)
+                        if (x < valid) yp[x * tstride] = f[x];
+                }
+            }
+        }
+        if (quad == 0 && lane == 0) LA_TR(4, 5, m);
+        return true;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -286,11 +384,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop, so that every operand is warp-uniform
+        // (descriptors stay in uniform registers); lane 0 alone issues the
+        // tensor-core instructions through their predicate.
+        {
+            const uint32_t lead = lane == 0;
             bool ok = true;
             constexpr uint32_t id_scores = idesc_bf16(64, Cf::kKRows, false, false);
             constexpr uint32_t id_qz = idesc_bf16(64, 8, false, false);
             constexpr uint32_t id_inter = idesc_bf16(D, 64, false, false);
+            constexpr uint32_t id_inter_tf32 = idesc_tf32(D, 64);
             constexpr uint32_t id_intra = idesc_bf16(D, 64, true, false);
             constexpr uint32_t id_state = idesc_bf16(D, D, true, true);
             const uint32_t tS = tmem + Cf::kColS, tHi = tmem + Cf::kColHi, tLo = tmem + Cf::kColLo;
@@ -301,113 +404,142 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t khi_lbo = GATED ? 8192u : (uint32_t)Cf::kKBlk;  // stride of 64-feature blocks
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                    mma_ss(tS, av, sdesc_sw128(smem_u32(khi + ks * 2048), khi_lbo, 1024), id_state, 1);
-                    if (SPLITK) mma_ss(tS, av, sdesc_sw128(smem_u32(Klo(s) + ks * 2048), 8192, 1024), id_state, 1);
+                    mma_ss(tS, av, sdesc_sw128(smem_u32(khi + ks * 2048), khi_lbo, 1024), id_state, 1, lead);
+                    if (SPLITK) mma_ss(tS, av, sdesc_sw128(smem_u32(Klo(s) + ks * 2048), 8192, 1024), id_state, 1, lead);
                 }
             };
 
             for (int i = 0; i < nck && ok; ++i) {
                 const int s = i % NKV1;
                 if (Cf::kHasKV) {
-                    ok = mbar_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
+                    ok = warp_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
                     if (!ok) break;
                     tc_fence_after();
-                    LA_TR(1, 1, i);
+                    if (lead) LA_TR(1, 1, i);
                 }
                 if (MODE == kState) {
                     if (GATED || i == 0) {
                         // the converters publish the (decayed) state before each update
-                        ok = mbar_wait(state_ready, i & 1, err, kErrStateReady);
+                        ok = warp_wait(state_ready, i & 1, err, kErrStateReady);
                         if (!ok) break;
                         tc_fence_after();
                     }
                     issue_state_update(s);
                     // the non-gated state pass has no per-chunk hand-off: one phase at the end
-                    if (GATED || i == nck - 1) mma_commit(state_done);
-                    mma_commit(&empty_kv[s]);
+                    if (GATED || i == nck - 1) mma_commit(state_done, lead);
+                    mma_commit(&empty_kv[s], lead);
                     continue;
                 }
                 for (int r = 0; r < G && ok; ++r) {
                     const int n = i * G + r, sq = n % NQ1, ab = n % NA, yb = n % NY;
-                    ok = mbar_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ);
+                    ok = warp_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ);
                     if (!ok) break;
                     tc_fence_after();
-                    LA_TR(1, 2, n);
+                    if (lead) LA_TR(1, 2, n);
                     uint8_t* qop = GATED ? Qd(sq) : Qb(sq);  // operand of the inter read-out
                     const uint32_t tA = tmem + Cf::kColA + 80 * ab;
                     if (MODE == kCausal || NORM) {
                         if (n >= NA) {
-                            ok = mbar_wait(&a_empty[ab], ((n / NA) & 1) ^ 1, err, kErrAEmpty);
+                            ok = warp_wait(&a_empty[ab], ((n / NA) & 1) ^ 1, err, kErrAEmpty);
                             if (!ok) break;
                             tc_fence_after();
                         }
+                        if (lead) LA_TR(1, 10, n);
                         if (MODE == kCausal) {
                             // scores, and in columns 64..71 phi(q).[Z_hi; Z_lo] from the Z rows
                             for (int ks = 0; ks < D / 16; ++ks) {
                                 const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
                                 const uint32_t ko = (ks >> 2) * Cf::kKBlk + (ks & 3) * 32;
                                 mma_ss(tA, sdesc_sw128(smem_u32(Qb(sq) + qo), 16, 1024),
-                                       sdesc_sw128(smem_u32(Kb(s) + ko), 16, 1024), id_scores, ks > 0);
+                                       sdesc_sw128(smem_u32(Kb(s) + ko), 16, 1024), id_scores, ks > 0, lead);
                             }
                         } else {
                             for (int ks = 0; ks < D / 16; ++ks) {
                                 const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
                                 mma_ss(tA + 64, sdesc_sw128(smem_u32(Qb(sq) + qo), 16, 1024),
                                        sdesc_sw128(smem_u32(zr_at(0, ks >> 2) + (ks & 3) * 32), 16, 1024), id_qz,
-                                       ks > 0);
+                                       ks > 0, lead);
                             }
                         }
-                        mma_commit(&a_full[ab]);
-                        LA_TR(1, 3, n);
+                        if (lead) LA_TR(1, 11, n);
+                        mma_commit(&a_full[ab], lead);
+                        if (lead) LA_TR(1, 3, n);
                     }
                     if (r == 0 && (MODE == kCausal || i == 0)) {
-                        ok = mbar_wait(state_ready, MODE == kCausal ? (i & 1) : 0, err, kErrStateReady);
+                        if (TF32 && MODE == kCausal && i > 0)  // the update of chunk i-1 has completed
+                            ok = warp_wait(state_done, (i - 1) & 1, err, kErrStateDone);
+                        else  // start state in place (tf32), or the hi/lo copy of S(i) (gated)
+                            ok = warp_wait(state_ready, (MODE == kCausal && !TF32) ? (i & 1) : 0, err,
+                                           kErrStateReady);
                         if (!ok) break;
                         tc_fence_after();
-                        LA_TR(1, 4, i);
+                        if (lead) LA_TR(1, 4, i);
                     }
                     if (n >= NY) {
-                        ok = mbar_wait(&y_empty[yb], ((n / NY) & 1) ^ 1, err, kErrYEmpty);
+                        ok = warp_wait(&y_empty[yb], ((n / NY) & 1) ^ 1, err, kErrYEmpty);
                         if (!ok) break;
                         tc_fence_after();
-                        LA_TR(1, 5, n);
+                        if (lead) LA_TR(1, 5, n);
                     }
-                    // inter: Y^T = S_prev^T(hi + lo) . Q^T
+                    // inter: Y^T = S_prev^T . Q^T (tf32 from the fp32 state, or hi + lo)
                     const uint32_t tY = tmem + Cf::kColY + 64 * yb;
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
-                        const uint64_t bq = sdesc_sw128(smem_u32(qop + ko), 16, 1024);
-                        mma_ts(tY, tHi + ks * 8, bq, id_inter, ks > 0);
-                        mma_ts(tY, tLo + ks * 8, bq, id_inter, 1);
-                    }
-                    mma_commit(&empty_q[sq]);
-                    LA_TR(1, 6, n);
-                    if (MODE == kCausal) {
-                        if (r == G - 1) {
-                            // every read-out of this chunk is issued: update the state now
-                            issue_state_update(s);
-                            mma_commit(state_done);
-                            LA_TR(1, 9, i);
+                    if (TF32) {
+                        for (int ks = 0; ks < D / 8; ++ks) {
+                            const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
+                            mma_ts_tf32(tY, tS + ks * 8, sdesc_sw128(smem_u32(Qf(sq) + ko), 16, 1024),
+                                        id_inter_tf32, ks > 0, lead);
                         }
-                        ok = mbar_wait(at_full, n & 1, err, kErrATFull);
+                    } else {
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
+                            const uint64_t bq = sdesc_sw128(smem_u32(qop + ko), 16, 1024);
+                            mma_ts(tY, tHi + ks * 8, bq, id_inter, ks > 0, lead);
+                            mma_ts(tY, tLo + ks * 8, bq, id_inter, 1, lead);
+                        }
+                    }
+                    mma_commit(&empty_q[sq], lead);
+                    if (lead) LA_TR(1, 6, n);
+                    if (MODE == kCausal) {
+                        if (!TF32 && r == G - 1) {
+                            // every read-out of this chunk is issued (from the hi/lo
+                            // copy): update the state now
+                            issue_state_update(s);
+                            mma_commit(state_done, lead);
+                            if (lead) LA_TR(1, 9, i);
+                        }
+                        if (TF32 && r == G - 1) mma_commit(inter_done, lead);
+                        ok = warp_wait(at_full, n & 1, err, kErrATFull);
                         if (!ok) break;
                         tc_fence_after();
-                        LA_TR(1, 7, n);
-                        // intra: Y^T += V^T . A^T (hi + lo).  The masked-score buffer is
+                        if (lead) LA_TR(1, 7, n);
+                        // intra: Y^T += V^T . A^T (hi [+ lo]).  The masked-score buffer is
                         // free again for item n + 1 once its scores complete, because
                         // tensor-core operations complete in issue order.
                         for (int ks = 0; ks < kC / 16; ++ks) {
                             const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                            mma_ss(tY, av, sdesc_sw128(smem_u32(ATh + ks * 32), 16, 1024), id_intra, 1);
-                            mma_ss(tY, av, sdesc_sw128(smem_u32(ATl + ks * 32), 16, 1024), id_intra, 1);
+                            mma_ss(tY, av, sdesc_sw128(smem_u32(ATh + ks * 32), 16, 1024), id_intra, 1, lead);
+                            if (ALO)
+                                mma_ss(tY, av, sdesc_sw128(smem_u32(ATl + ks * 32), 16, 1024), id_intra, 1, lead);
                         }
                     }
-                    mma_commit(&y_full[yb]);
-                    LA_TR(1, 8, n);
+                    mma_commit(&y_full[yb], lead);
+                    if (lead) LA_TR(1, 8, n);
+                    if (TF32 && MODE == kCausal && r == G - 1) {
+                        // the update overwrites the state that this chunk's read-outs
+                        // take as their A operand: only after they have completed
+                        ok = warp_wait(inter_done, i & 1, err, kErrStateDone);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_state_update(s);
+                        mma_commit(state_done, lead);
+                        if (lead) LA_TR(1, 9, i);
+                    }
                 }
                 if (!ok) break;
-                if (Cf::kHasKV) mma_commit(&empty_kv[s]);
+                if (Cf::kHasKV) mma_commit(&empty_kv[s], lead);
             }
+            // last: every operation above has completed (also after an early exit)
+            if (TF32 && MODE == kCausal) mma_commit(final_done, lead);
         }
     } else if (warp < kEpiWarp0) {
         // -------------------------------------------------------- state warps
@@ -485,12 +617,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         if (MODE == kApply) {
-            // fixed global state: hi/lo once
+            // fixed global state (hi/lo once for the gated layout)
             tc_fence_after();
-            convert_state(1.f, false);
+            if (!TF32) convert_state(1.f, false);
             publish_state();
-        } else if (MODE == kState && !GATED) {
-            publish_state();  // the zero state is in place; updates accumulate without hand-offs
+        } else if ((MODE == kState && !GATED) || (MODE == kCausal && TF32)) {
+            // the start (or zero) state is in place; the tensor core reads and
+            // updates it without further hand-offs
+            publish_state();
         } else {
             for (int i = 0; i < nck && ok; ++i) {
                 // S(i): after the update of chunk i-1 and every read-out that used S_prev
@@ -514,13 +648,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (MODE == kState) gsum += gtot;
             }
         }
+        if (TF32 && MODE != kState) {
+            // linear rule: the state needs no per-chunk work here, so these
+            // warps run the output stage, beside the score warps
+            for (int m = 0; m < nck * G && ok; ++m) ok = emit_y(m);
+        }
 
         // ---- final state out: causal (last segment) or every segment in state mode
         const bool write_state =
             ok && nck > 0 && ((MODE == kCausal && seg == nseg - 1 && a.S_dst) || MODE == kState);
-        if (write_state) {
-            // causal: phase nck-1 (one per chunk); non-gated state pass: its single phase
-            ok = warp_wait(state_done, (MODE == kState && !GATED) ? 0 : ((nck - 1) & 1), err, kErrStateDone);
+        if (MODE == kCausal && TF32 && nck > 0) {
+            // the last update is not followed by any read-out: wait for it here,
+            // also when no state is written, before TMEM is released
+            ok = warp_wait(final_done, 0, err, kErrStateDone) && ok;
+            tc_fence_after();
+        }
+        if (write_state && ok) {
+            // gated causal: phase nck-1 (one per chunk); non-gated state pass: its single phase
+            if (!(MODE == kCausal && TF32))
+                ok = warp_wait(state_done, (MODE == kState && !GATED) ? 0 : ((nck - 1) & 1), err, kErrStateDone);
             tc_fence_after();
             if (ok) {
                 float* Sd = MODE == kState ? a.S_dst + ((size_t)bh * nseg + seg) * D * D : a.S_dst + (size_t)bh * D * D;
@@ -547,7 +693,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool arow_ok = lane < 16;
         const int n_total = Cf::kHasQ ? nck * G : 0;
         bool ok = true;
-        uint32_t gphase = 0;
         for (int n = 0; n <= n_total && ok; ++n) {
             if (n < n_total) {
                 // -------- scores of item n: mask, decay, hi/lo split, 1/den
@@ -587,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const uint32_t off = sw128_offset(arow, cch * 16);
                                 if (cch * 8 > arow) {  // entirely above the diagonal
                                     *reinterpret_cast<uint4*>(ATh + off) = make_uint4(0, 0, 0, 0);
-                                    *reinterpret_cast<uint4*>(ATl + off) = make_uint4(0, 0, 0, 0);
+                                    if (ALO) *reinterpret_cast<uint4*>(ATl + off) = make_uint4(0, 0, 0, 0);
                                     continue;
                                 }
                                 float v[8];
@@ -600,10 +745,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (GATED && j <= arow) x *= __expf(gi - gc[j]);
                                     v[e] = x;
                                 }
-                                uint4 hv, lv;
-                                split8(v, hv, lv);
-                                *reinterpret_cast<uint4*>(ATh + off) = hv;
-                                *reinterpret_cast<uint4*>(ATl + off) = lv;
+                                if (ALO) {
+                                    uint4 hv, lv;
+                                    split8(v, hv, lv);
+                                    *reinterpret_cast<uint4*>(ATh + off) = hv;
+                                    *reinterpret_cast<uint4*>(ATl + off) = lv;
+                                } else {
+                                    *reinterpret_cast<uint4*>(ATh + off) = f_to_bf8(v);
+                                }
                             }
                         }
                         fence_proxy_async();
@@ -612,48 +761,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 2, n);
                     }
                 }
-                if (arow_ok) inv_den[(n & 3) * 64 + arow] = NORM ? scale / den : scale;
-            }
-            if (n >= 1) {
-                // -------- output of item m = n - 1, stored straight to global memory
-                const int m = n - 1;
-                const int i_chunk = m / G, r_head = m - i_chunk * G;
-                const int t0 = (c_begin + i_chunk) * kC;
-                const int valid = min(kC, T - t0);
-                const int yb = m % NY;
-                ok = warp_wait(&y_full[yb], (m / NY) & 1, err, kErrYFull);
-                if (!ok) break;
-                tc_fence_after();
-                if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 3, m);
-                uint32_t y0[32], y1[32];
-                tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 0), y0);
-                tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 32), y1);
-                tmem_ld_wait();
-                reg_fence(y0);
-                reg_fence(y1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&y_empty[yb]);
-                // 1/den of item m was written by all four warps one iteration ago
-                ok = group_sync(epi_group, gphase, err, kErrYFull);
-                if (!ok) break;
-                if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 4, m);
-                const float* idn = inv_den + (m & 3) * 64;
-                if (vrow_ok) {
-                    const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
-                    const size_t tstride = (size_t)Hq * D;
-#pragma unroll
-                    for (int x = 0; x < 64; ++x) {
-                        if (x < valid) {
-                            const float v = (x < 32 ? __uint_as_float(y0[x]) : __uint_as_float(y1[x - 32])) * idn[x];
-                            if (OUT_BF16)
-                                reinterpret_cast<__nv_bfloat16*>(yout)[base + x * tstride] = __float2bfloat16_rn(v);
-                            else
-                                reinterpret_cast<float*>(yout)[base + x * tstride] = v;
-                        }
-                    }
+                if (NORM) {
+                    // hand scale/den to the output stage (without the normalizer
+                    // the factor is the constant scale and needs no hand-off)
+                    if (arow_ok) inv_den[(n & 3) * 64 + arow] = scale / den;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&den_full[n & 3]);
                 }
             }
+            if (!TF32 && n >= 1) ok = emit_y(n - 1);  // gated: the output stage runs here
         }
     } else {
         // ------------------------------------------------------ feature warps
@@ -792,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sq = n % NQ1;
             if (!warp_wait(&full_q[sq], (n / NQ1) & 1, err, kErrFullQ)) return false;
             if (ct == 0) LA_TR(2, 3, n);
-            if (fmap != LA_FMAP_NONE || GATED) {
+            if (fmap != LA_FMAP_NONE || GATED || TF32) {
                 const float* gc = Gc(i % NKV1);
                 uint4 in[kPer];
 #pragma unroll
@@ -809,7 +925,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
 #pragma unroll
                         for (int e = 0; e < 8; ++e) f[e] = phi<true>(fmap, f[e], eps);
-                        *reinterpret_cast<uint4*>(Qb(sq) + chunk_off(m)) = f_to_bf8(f);
+                        if (fmap != LA_FMAP_NONE) *reinterpret_cast<uint4*>(Qb(sq) + chunk_off(m)) = f_to_bf8(f);
+                        if (TF32) {
+                            // features 8cc..8cc+7 are two 16-byte chunks of a 32-feature block
+                            const int row = rbase + kRowStep * m;
+                            uint8_t* blk = Qf(sq) + (cc >> 2) * 8192 + row * 128;
+                            const int c16 = 2 * (cc & 3);
+                            *reinterpret_cast<float4*>(blk + ((c16 ^ (row & 7)) << 4)) =
+                                make_float4(f[0], f[1], f[2], f[3]);
+                            *reinterpret_cast<float4*>(blk + (((c16 + 1) ^ (row & 7)) << 4)) =
+                                make_float4(f[4], f[5], f[6], f[7]);
+                        }
                     }
                 }
             }

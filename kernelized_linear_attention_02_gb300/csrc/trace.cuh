@@ -22,14 +22,14 @@ namespace trace {
 static __device__ unsigned int g_count[kTraceCtas];
 static __device__ unsigned long long g_time[kTraceCtas][kTraceEvents];
 static __device__ unsigned int g_tag[kTraceCtas][kTraceEvents];
-// Each role records from one thread into its own quarter of the buffer; the
+// Each role (up to 8) records from one thread into its own eighth of the buffer; the
 // slot counter lives in shared memory so recording costs no global round trip.
 __device__ __forceinline__ void record(unsigned* ctr, int role, int ev, int idx) {
     const int cta = blockIdx.x + blockIdx.y * gridDim.x;
     if (cta >= kTraceCtas) return;
     const unsigned slot = ctr[role]++;
-    if (slot < (unsigned)(kTraceEvents / 4)) {
-        const unsigned at = role * (kTraceEvents / 4) + slot;
+    if (slot < (unsigned)(kTraceEvents / 8)) {
+        const unsigned at = role * (kTraceEvents / 8) + slot;
         g_time[cta][at] = clock64();
         g_tag[cta][at] = (unsigned)(role << 24) | (unsigned)(ev << 16) | (unsigned)(idx & 0xffff);
     }
