@@ -558,19 +558,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         // initial state, decay-weighted for gated.
         const bool fold = MODE == kCausal && a.S_seg && seg > 0;
         const float* S_start = MODE == kState ? nullptr : a.S_init;
+        // Loads are batched 32 columns x 2 segments at a time (independent
+        // addresses, all in flight together); the additions keep the segment
+        // order 0, 1, ..., seg-1.
         for (int c0 = 0; c0 < D; c0 += 32) {
+            float run[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+                run[x] = (S_start && vrow_ok) ? S_start[(size_t)bh * D * D + (size_t)(c0 + x) * D + vrow] : 0.f;
+            if (fold && vrow_ok) {
+                for (int p = 0; p < seg; p += 2) {
+                    const bool two = p + 1 < seg;
+                    const float* s0 = a.S_seg + ((size_t)bh * nseg + p) * D * D + (size_t)c0 * D + vrow;
+                    const float* s1 = s0 + (size_t)D * D;
+                    float d0[32], d1[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        d0[x] = s0[(size_t)x * D];
+                        d1[x] = two ? s1[(size_t)x * D] : 0.f;
+                    }
+                    const float w0 = GATED ? __expf(a.G_seg[(size_t)bh * nseg + p]) : 1.f;
+                    const float w1 = (GATED && two) ? __expf(a.G_seg[(size_t)bh * nseg + p + 1]) : 1.f;
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        run[x] = GATED ? fmaf(w0, run[x], d0[x]) : run[x] + d0[x];
+                        if (two) run[x] = GATED ? fmaf(w1, run[x], d1[x]) : run[x] + d1[x];
+                    }
+                }
+            }
             uint32_t r[32];
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                const size_t e = (size_t)(c0 + x) * D + vrow;
-                float run = (S_start && vrow_ok) ? S_start[(size_t)bh * D * D + e] : 0.f;
-                if (fold && vrow_ok)
-                    for (int p = 0; p < seg; ++p) {
-                        const float dS = a.S_seg[((size_t)bh * nseg + p) * D * D + e];
-                        run = GATED ? fmaf(__expf(a.G_seg[(size_t)bh * nseg + p]), run, dS) : run + dS;
-                    }
-                r[x] = __float_as_uint(run);
-            }
+            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(run[x]);
             tmem_st32(tmem_addr(tmem + Cf::kColS, quad * 32, c0), r);
         }
         tmem_st_wait();
@@ -806,8 +824,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (NORM && ct < D && MODE != kState) {
             const bool fold = MODE == kCausal && a.S_seg && seg > 0;
             zreg = a.Z_init ? a.Z_init[(size_t)bh * D + ct] : 0.f;
-            if (fold && a.Z_seg)
-                for (int p = 0; p < seg; ++p) zreg += a.Z_seg[((size_t)bh * nseg + p) * D + ct];
+            if (fold && a.Z_seg) {
+                // independent loads, four in flight; summed in segment order
+                for (int p = 0; p < seg; p += 4) {
+                    float z4[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        z4[u] = p + u < seg ? a.Z_seg[((size_t)bh * nseg + p + u) * D + ct] : 0.f;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) zreg += z4[u];
+                }
+            }
         }
 
         // ---- keys of chunk i: feature map (+ lo part), decayed keys, Z rows and sums

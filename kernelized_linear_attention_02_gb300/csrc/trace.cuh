@@ -25,7 +25,12 @@ static __device__ unsigned int g_tag[kTraceCtas][kTraceEvents];
 // Each role (up to 8) records from one thread into its own eighth of the buffer; the
 // slot counter lives in shared memory so recording costs no global round trip.
 __device__ __forceinline__ void record(unsigned* ctr, int role, int ev, int idx) {
+#ifdef LA_TRACE_LAST_SEGMENT
+    // the first kTraceCtas (batch, kv head) tiles of the last sequence segment
+    const int cta = blockIdx.y + 1 == gridDim.y ? (int)blockIdx.x : kTraceCtas;
+#else
     const int cta = blockIdx.x + blockIdx.y * gridDim.x;
+#endif
     if (cta >= kTraceCtas) return;
     const unsigned slot = ctr[role]++;
     if (slot < (unsigned)(kTraceEvents / 8)) {
