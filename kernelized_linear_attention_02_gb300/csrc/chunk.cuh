@@ -293,60 +293,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&y_full[yb], (m / NY) & 1, err, kErrYFull)) return false;
         tc_fence_after();
         if (quad == 0 && lane == 0) LA_TR(4, 3, m);
-        uint32_t y0[32], y1[32];
-        tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 0), y0);
-        tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 32), y1);
-        tmem_ld_wait();
-        reg_fence(y0);
-        reg_fence(y1);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&y_empty[yb]);
         // scale/den of item m, written by the four score warps
         if (NORM && !warp_wait(&den_full[m & 3], (m >> 2) & 1, err, kErrYFull)) return false;
         if (quad == 0 && lane == 0) LA_TR(4, 4, m);
-        if (vrow_ok) {
-            // all 64 factors into registers first: a shared load placed
-            // after a global store could not be moved ahead of it
-            float f[64];
-            const float4* idn4 = reinterpret_cast<const float4*>(inv_den + (m & 3) * 64);
+        const float4* idn4 = reinterpret_cast<const float4*>(inv_den + (m & 3) * 64);
+        const size_t tstride = (size_t)Hq * D;
+        const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
+        // A rolled loop over 8-token groups (each read from TMEM as it is
+        // needed) keeps this stage's code small in the instruction cache.
+#pragma unroll 1
+        for (int g = 0; g < 8; ++g) {
+            uint32_t yv[8];
+            tmem_ld8(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, g * 8), yv);
+            tmem_ld_wait();
+            reg_fence(yv);
+            if (vrow_ok) {
+                const float4 fa = NORM ? idn4[2 * g] : make_float4(scale, scale, scale, scale);
+                const float4 fb = NORM ? idn4[2 * g + 1] : fa;
+                const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                const float4 t = NORM ? idn4[x] : make_float4(scale, scale, scale, scale);
-                f[4 * x] = t.x;
-                f[4 * x + 1] = t.y;
-                f[4 * x + 2] = t.z;
-                f[4 * x + 3] = t.w;
-            }
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                f[x] *= __uint_as_float(y0[x]);
-                f[x + 32] *= __uint_as_float(y1[x]);
-            }
-            const size_t tstride = (size_t)Hq * D;
-            const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
-            if (OUT_BF16) {
-                __nv_bfloat16* yp = reinterpret_cast<__nv_bfloat16*>(yout) + base;
-                if (valid == kC) {
-#pragma unroll
-                    for (int x = 0; x < 64; ++x) yp[x * tstride] = __float2bfloat16_rn(f[x]);
-                } else {
-#pragma unroll
-                    for (int x = 0; x < 64; ++x)
-                        if (x < valid) yp[x * tstride] = __float2bfloat16_rn(f[x]);
-                }
-            } else {
-                float* yp = reinterpret_cast<float*>(yout) + base;
-                if (valid == kC) {
-#pragma unroll
-                    for (int x = 0; x < 64; ++x) yp[x * tstride] = f[x];
-                } else {
-#pragma unroll
-                    for (int x = 0; x < 64; ++x)
-                        if (x < valid) yp[x * tstride] = f[x];
+                for (int e = 0; e < 8; ++e) {
+                    const int x = g * 8 + e;
+                    const float o = f[e] * __uint_as_float(yv[e]);
+                    if (x < valid) {
+                        if (OUT_BF16)
+                            reinterpret_cast<__nv_bfloat16*>(yout)[base + x * tstride] = __float2bfloat16_rn(o);
+                        else
+                            reinterpret_cast<float*>(yout)[base + x * tstride] = o;
+                    }
                 }
             }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&y_empty[yb]);
         if (quad == 0 && lane == 0) LA_TR(4, 5, m);
         return true;
     };
@@ -402,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_state_update = [&](int s) {
                 uint8_t* khi = GATED ? Kd(s) : Kb(s);
                 const uint32_t khi_lbo = GATED ? 8192u : (uint32_t)Cf::kKBlk;  // stride of 64-feature blocks
+#pragma unroll 1
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
                     mma_ss(tS, av, sdesc_sw128(smem_u32(khi + ks * 2048), khi_lbo, 1024), id_state, 1, lead);
@@ -447,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lead) LA_TR(1, 10, n);
                         if (MODE == kCausal) {
                             // scores, and in columns 64..71 phi(q).[Z_hi; Z_lo] from the Z rows
+#pragma unroll 1
                             for (int ks = 0; ks < D / 16; ++ks) {
                                 const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
                                 const uint32_t ko = (ks >> 2) * Cf::kKBlk + (ks & 3) * 32;
@@ -454,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        sdesc_sw128(smem_u32(Kb(s) + ko), 16, 1024), id_scores, ks > 0, lead);
                             }
                         } else {
+#pragma unroll 1
                             for (int ks = 0; ks < D / 16; ++ks) {
                                 const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
                                 mma_ss(tA + 64, sdesc_sw128(smem_u32(Qb(sq) + qo), 16, 1024),
@@ -484,12 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // inter: Y^T = S_prev^T . Q^T (tf32 from the fp32 state, or hi + lo)
                     const uint32_t tY = tmem + Cf::kColY + 64 * yb;
                     if (TF32) {
+#pragma unroll 1
                         for (int ks = 0; ks < D / 8; ++ks) {
                             const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
                             mma_ts_tf32(tY, tS + ks * 8, sdesc_sw128(smem_u32(Qf(sq) + ko), 16, 1024),
                                         id_inter_tf32, ks > 0, lead);
                         }
                     } else {
+#pragma unroll 1
                         for (int ks = 0; ks < D / 16; ++ks) {
                             const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
                             const uint64_t bq = sdesc_sw128(smem_u32(qop + ko), 16, 1024);
@@ -515,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // intra: Y^T += V^T . A^T (hi [+ lo]).  The masked-score buffer is
                         // free again for item n + 1 once its scores complete, because
                         // tensor-core operations complete in issue order.
+#pragma unroll 1
                         for (int ks = 0; ks < kC / 16; ++ks) {
                             const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
                             mma_ss(tY, av, sdesc_sw128(smem_u32(ATh + ks * 32), 16, 1024), id_intra, 1, lead);
@@ -723,42 +709,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 1, n);
                     const uint32_t tA = tmem + Cf::kColA + 80 * ab;
-                    uint32_t r[32], r2[32], z[16];
-                    if (MODE == kCausal) {
-                        tmem_ld32(tmem_addr(tA, quad * 32, 0), r);
-                        tmem_ld32(tmem_addr(tA, quad * 32, 32), r2);
+                    if (NORM) {
+                        uint32_t z[16];
+                        tmem_ld16(tmem_addr(tA, quad * 32, 64), z);
+                        tmem_ld_wait();
+                        reg_fence(z);
+                        den = __uint_as_float(z[0]) + __uint_as_float(z[1]) + eps;
                     }
-                    if (NORM) tmem_ld16(tmem_addr(tA, quad * 32, 64), z);
-                    tmem_ld_wait();
                     if (MODE == kCausal) {
-                        reg_fence(r);
-                        reg_fence(r2);
-                    }
-                    if (NORM) reg_fence(z);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_empty[ab]);  // TMEM scores read out
-                    if (NORM) den = __uint_as_float(z[0]) + __uint_as_float(z[1]) + eps;
-                    if (MODE == kCausal) {
-                        // the masked-score buffer is free: the intra product of item n - 1
-                        // was issued before the scores of item n and has completed with them
-                        if (arow_ok) {
-                            const float* gc = reinterpret_cast<const float*>(Gc(s));
-                            const float gi = GATED ? gc[arow] : 0.f;
-#pragma unroll
-                            for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
+                        // The masked-score buffer is free: the intra product of item
+                        // n - 1 was issued before the scores of item n and has
+                        // completed with them.  A rolled loop over 8-column groups,
+                        // each read from TMEM as it is needed.
+                        const float* gc = reinterpret_cast<const float*>(Gc(s));
+                        const float gi = (GATED && arow_ok) ? gc[arow] : 0.f;
+#pragma unroll 1
+                        for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
+                            uint32_t r[8];
+                            tmem_ld8(tmem_addr(tA, quad * 32, cch * 8), r);
+                            tmem_ld_wait();
+                            reg_fence(r);
+                            if (arow_ok) {
                                 const uint32_t off = sw128_offset(arow, cch * 16);
-                                if (cch * 8 > arow) {  // entirely above the diagonal
-                                    *reinterpret_cast<uint4*>(ATh + off) = make_uint4(0, 0, 0, 0);
-                                    if (ALO) *reinterpret_cast<uint4*>(ATl + off) = make_uint4(0, 0, 0, 0);
-                                    continue;
-                                }
                                 float v[8];
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
                                     const int j = cch * 8 + e;
-                                    float x = j < 32 ? __uint_as_float(r[j]) : __uint_as_float(r2[j - 32]);
-                                    x = (j <= arow) ? x : 0.f;
+                                    float x = (j <= arow) ? __uint_as_float(r[e]) : 0.f;
                                     if (NORM) den += x;
                                     if (GATED && j <= arow) x *= __expf(gi - gc[j]);
                                     v[e] = x;
@@ -773,6 +750,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             }
                         }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_empty[ab]);  // TMEM scores read out
+                    if (MODE == kCausal) {
                         fence_proxy_async();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(at_full);
@@ -869,15 +851,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool touch = GATED || SPLITK || NORM || fmap != LA_FMAP_NONE;
             if (ct == 0) LA_TR(2, 7, i);
             if (touch) {
-                uint4 in[kPer];
-#pragma unroll
-                for (int m = 0; m < kPer; ++m) in[m] = *reinterpret_cast<const uint4*>(Kb(s) + chunk_off(m, Cf::kKBlk));
                 float colsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+                // A rolled loop: its body stays in the instruction cache across
+                // iterations (the roles of this kernel share each sub-partition's
+                // instruction cache, so straight-line code would be fetched anew
+                // every chunk).
+                uint4 nxt = *reinterpret_cast<const uint4*>(Kb(s) + chunk_off(0, Cf::kKBlk));
+#pragma unroll 1
                 for (int m = 0; m < kPer; ++m) {
                     const int row = rbase + kRowStep * m;
+                    const uint4 cur = nxt;
+                    if (m + 1 < kPer) nxt = *reinterpret_cast<const uint4*>(Kb(s) + chunk_off(m + 1, Cf::kKBlk));
                     float f[8];
-                    bf8_to_f(in[m], f);
+                    bf8_to_f(cur, f);
                     uint4 hi, lo;
                     if (GATED) {
                         const float w = __expf(gtot - gc[row]);
@@ -937,13 +923,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ct == 0) LA_TR(2, 3, n);
             if (fmap != LA_FMAP_NONE || GATED || TF32) {
                 const float* gc = Gc(i % NKV1);
-                uint4 in[kPer];
-#pragma unroll
-                for (int m = 0; m < kPer; ++m) in[m] = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(m));
-#pragma unroll
+                uint4 nxt = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(0));
+#pragma unroll 1
                 for (int m = 0; m < kPer; ++m) {
+                    const uint4 cur = nxt;
+                    if (m + 1 < kPer) nxt = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(m + 1));
                     float f[8];
-                    bf8_to_f(in[m], f);
+                    bf8_to_f(cur, f);
                     if (GATED) {
                         const float w = __expf(gc[rbase + kRowStep * m]);
 #pragma unroll

@@ -49,6 +49,23 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* b, uint32_t parity) 
         : "memory");
     return ok;
 }
+// Same test, but a thread whose phase is still open is suspended until it
+// completes or `hint_ns` elapses (the suspend-time hint of try_wait), instead
+// of returning at once: waiting warps then take no issue slots from the warps
+// that do the work.
+__device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint64_t* b, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok;
+}
+constexpr uint32_t kSuspendHintNs = 1000000;  // 1 ms; a completed phase wakes the thread at once
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -63,8 +80,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, unsigned
     if (mbar_try_wait(b, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(b, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait_sleep(b, parity, kSuspendHintNs)) return true;
         if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(err, code);
             return false;
@@ -83,8 +101,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, unsigned
     if (lane == 0) t0 = global_timer_ns();
     for (;;) {
         unsigned done = 0;
+#pragma unroll 1
         for (int i = 0; i < 16; ++i) {
-            done = __ballot_sync(full, mbar_try_wait(b, parity));
+            done = __ballot_sync(full, mbar_try_wait_sleep(b, parity, kSuspendHintNs));
             if (done == full) return true;
         }
         int tout = 0;
@@ -251,6 +270,11 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar, uint32_t issue = 1) {
 #define LA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
                  "r"(r[i + 6]), "r"(r[i + 7])
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : LA_R8(0)
+                 : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
