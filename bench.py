@@ -267,6 +267,69 @@ def time_decode(la, w, n_steps, warmup, stream):
     return ev0.elapsed_time(ev1) * 1e3 / n_steps, la.la_launch_count() - n0
 
 
+def time_workload(la, w, steps, warmup, stream, causal=True):
+    """Device time of one call (causal or non-causal) on one of the measured
+    workloads, inputs resident in HBM and rotated so that the data a call
+    reads exceeds L2 (the larger workloads exceed it on their own)."""
+    set_bytes = prefill_alg_bytes(w)
+    nsets = max(1, -(-3 * L2_BYTES // set_bytes))
+    sets = []
+    for s in range(nsets):
+        q, k, v, d = inputs.make_qkv(w, device="cuda", seed=w.seed + s)
+        y = torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype, device="cuda")
+        sets.append((q, k, v, d, y))
+    kw = prefill_kwargs(w)
+    if not causal:
+        kw.pop("update_rule")
+    p = la.make_params(batch=w.B, seq_len=w.T, q_heads=w.q_heads, kv_heads=w.kv_heads, key_dim=w.Dk,
+                       value_dim=w.Dv, io_dtype=w.dtype, feature_map=w.feature_map,
+                       use_normalizer=w.use_normalizer, epsilon=w.eps, scale=w.scale, update_rule=w.rule)
+    ws = torch.empty(max(1, la.la_workspace_bytes(p, causal)), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        q, k, v, d, y = sets[i % nsets]
+        if causal:
+            la.la_forward_causal(q, k, v, decay=d, out=y, workspace=ws, stream=stream, **kw)
+        else:
+            la.la_forward_noncausal(q, k, v, out=y, workspace=ws, stream=stream, **kw)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    torch.cuda.synchronize()
+    n0 = la.la_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            step(warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    launches = la.la_launch_count() - n0
+    del sets, ws
+    torch.cuda.empty_cache()
+    return ev0.elapsed_time(ev1) / steps, launches / steps
+
+
+def workload_sweep(la, steps, warmup, stream, hbm_gbs):
+    """Every prefill workload of the library (causal and non-causal), each
+    with its HBM roofline fraction.  Algorithmic bytes: q, k, v (+ decay)
+    read once and y written once."""
+    out = []
+    cases = [(inputs.PREFILL_2K, True), (inputs.LONG_8K, True), (inputs.LONG_8K_UNNORM, True),
+             (inputs.LONG_8K, False), (inputs.LONG_8K_UNNORM, False), (inputs.ONNX_LINEAR, True),
+             (inputs.ONNX_GATED, True)]
+    for w, causal in cases:
+        ms, lpc = time_workload(la, w, steps, warmup, stream, causal)
+        alg = prefill_alg_bytes(w)
+        gbs = alg / (ms * 1e-3) / 1e9
+        out.append({"workload": w.name, "mode": "causal" if causal else "noncausal", "ms": ms,
+                    "tokens_per_s": w.B * w.T / (ms * 1e-3), "alg_bytes": alg, "achieved_GBps": gbs,
+                    "roofline_frac": gbs / hbm_gbs, "launches_per_call": lpc})
+    return out
+
+
 def cpu_baseline(w, budget_s=8.0):
     """The oracle as it stands on the host cores, on whole (batch, head)
     streams of the workload, repeated until the time budget is used."""
@@ -325,6 +388,10 @@ def run_gpu(args):
                "roofline_frac": dbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"], "steps": args.decode_steps,
                "gpu_launches": dlaunch, "clocks": dclk.summary()}
 
+    sweep = None
+    if not args.skip_sweep:
+        sweep = workload_sweep(la, max(3, min(args.steps, 10)), args.warmup, stream, pk["hbm_gbs"])
+
     if rank != 0:
         return
     traffic = None
@@ -348,6 +415,7 @@ def run_gpu(args):
         "gpu_launches": launches,
         "clocks": clocks,
         "decode": dec,
+        "workloads": sweep,
     }
     if world == 1 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -397,6 +465,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1024)
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-sweep", action="store_true", help="skip the per-workload roofline sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
