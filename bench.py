@@ -456,6 +456,27 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_only(args):
+    """One workload alone (optionally at another batch size): the entry point
+    for profiling a single kernel on a case small enough for a full capture."""
+    import dataclasses
+    import kernelized_linear_attention_02_gb300 as la
+    if torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    la.lib()
+    w = getattr(inputs, args.only)
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch)
+    stream = torch.cuda.Stream()
+    causal = not args.noncausal
+    ms, lpc = time_workload(la, w, args.steps, args.warmup, stream, causal)
+    alg = prefill_alg_bytes(w)
+    gbs = alg / (ms * 1e-3) / 1e9
+    print(json.dumps({"workload": w.name, "B": w.B, "mode": "causal" if causal else "noncausal", "ms": ms,
+                      "tokens_per_s": w.B * w.T / (ms * 1e-3), "alg_bytes": alg, "achieved_GBps": gbs,
+                      "roofline_frac": gbs / peaks()["hbm_gbs"], "launches_per_call": lpc}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -466,11 +487,16 @@ def main():
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-sweep", action="store_true", help="skip the per-workload roofline sweep")
+    ap.add_argument("--only", default=None, help="time one workload of linattn_inputs (e.g. LONG_8K) alone")
+    ap.add_argument("--batch", type=int, default=0, help="with --only: batch size override")
+    ap.add_argument("--noncausal", action="store_true", help="with --only: the non-causal pass")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_gpu(args)
 

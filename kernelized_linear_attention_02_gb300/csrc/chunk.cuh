@@ -83,7 +83,7 @@ struct Cfg {
     static constexpr int kOffKlo = kOffKd + (GATED ? kTile : 0);
     static constexpr int kOffVb = kOffKlo + (kSplitK ? kTile : 0);
     static constexpr int kOffG = kOffVb + kTile;
-    static constexpr int kKvStage = kHasKV ? kOffG + 1024 : 0;
+    static constexpr int kKvStage = kHasKV ? kOffG + (GATED ? 1024 : 0) : 0;  // G: gated rule only
     // linear rule: the read-out with the carried state runs as kind::tf32
     // with the fp32 state straight from TMEM as A, against an fp32 copy of
     // phi(Q) (64 x D, D/32 swizzled blocks of 8 KB); the gated rule, whose
@@ -94,25 +94,38 @@ struct Cfg {
     // masked scores as bf16 hi + lo (one bf16 part suffices without the
     // normalizer, where its rounding stays within ~5e-4 of the output)
     static constexpr bool kALo = NORM || GATED;
-    static constexpr int kAT = MODE == kCausal ? 2 * 8192 : 0;  // hi, lo: 64 x 64 each
+    // one buffer of masked scores: the epilogue writes item n's once the intra
+    // product of item n - 1 (which read the previous ones) has completed
+    static constexpr int kNAT = MODE == kCausal ? 1 : 0;
+    static constexpr int kAT = kNAT * 2 * 8192;  // per buffer: hi, lo (64 x 64 bf16 each)
     static constexpr int kZrApply = (MODE == kApply && NORM) ? kZr : 0;
-    static constexpr int kMisc = 12 * 1024;  // 1/den ring, partial Z sums, barriers
+    static constexpr int kMisc = 10 * 1024;  // 1/den ring (1 KB), partial Z sums (8 KB), barriers
     static constexpr int bytes(int nkv, int nq) {
         return 1024 + nkv * kKvStage + nq * kQStage + kAT + kZrApply + kMisc;
     }
     static constexpr int kLimit = 227 * 1024;
-    static constexpr int kNKV = kHasKV ? (bytes(2, kHasQ ? 1 : 0) <= kLimit ? 2 : 1) : 0;
-    static constexpr int kNQ = kHasQ ? (bytes(kNKV, 2) <= kLimit ? 2 : 1) : 0;
+    // ring depths: the deepest of (4,4), (3,3), (3,2), (2,2) that shared
+    // memory holds (key/value and query stages), else fewer
+    static constexpr bool fits(int nkv, int nq) {
+        return bytes(kHasKV ? nkv : 0, kHasQ ? nq : 0) <= kLimit;
+    }
+    static constexpr int kNKV0 = fits(4, 4) ? 4 : fits(3, 3) ? 3 : fits(3, 2) ? 3 : fits(2, 2) ? 2 : fits(2, 1) ? 2 : 1;
+    static constexpr int kNQ0 = fits(kNKV0, 4) ? 4 : fits(kNKV0, 3) ? 3 : fits(kNKV0, 2) ? 2 : 1;
+    static constexpr int kNKV = kHasKV ? kNKV0 : 0;
+    static constexpr int kNQ = kHasQ ? kNQ0 : 0;
+    static_assert(kNKV <= 4 && kNQ <= 4, "barrier arrays hold four stages");
     static constexpr int kSmem = bytes(kNKV, kNQ);
     static_assert(kSmem <= kLimit, "shared memory budget");
     // TMEM columns
-    static constexpr int kNA = D == 64 ? 2 : 1;    // score buffers (64 + 8 columns for phi(q).Z each)
+    // score buffers (64 + 8 columns for phi(q).Z each); the linear rule needs
+    // no bf16 copy of the state, so its two buffers take those columns
+    static constexpr int kNA = (D == 64 || kTf32) ? 2 : 1;
     static constexpr int kNY = 2;                  // Y^T buffers (64 columns each)
     static constexpr uint32_t kColS = 0;           // S^T fp32: D columns, lanes = value rows
-    static constexpr uint32_t kColHi = D;          // S^T hi bf16 pairs: D/2 columns
-    static constexpr uint32_t kColLo = D + D / 2;  // S^T lo
-    static constexpr uint32_t kColA = 2 * D;       // score buffers, 80 columns apart
-    static constexpr uint32_t kColY = 2 * D + 80 * kNA;
+    static constexpr uint32_t kColHi = D;          // S^T hi bf16 pairs: D/2 columns (gated)
+    static constexpr uint32_t kColLo = D + D / 2;  // S^T lo (gated)
+    static constexpr uint32_t kColA = kTf32 ? D : 2 * D;  // score buffers, 80 columns apart
+    static constexpr uint32_t kColY = kColA + 80 * kNA;
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kColY + 64 * kNY <= kTmemCols, "TMEM budget");
     // vectorised tile passes: 16-byte chunks, 128 threads
@@ -180,29 +193,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* inv_den = misc;           // [4][64] scale / den of the last four items
     float* zpart = misc + 256;       // [2][1024] partial column sums of phi(K)
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc + 256 + 2048);
-    uint64_t* full_kv = bars;        // [2]
-    uint64_t* empty_kv = bars + 2;   // [2]
-    uint64_t* conv_kv = bars + 4;    // [2]
-    uint64_t* full_q = bars + 6;     // [2]
-    uint64_t* empty_q = bars + 8;    // [2]
-    uint64_t* conv_q = bars + 10;    // [2]
-    uint64_t* a_full = bars + 12;    // [2]
-    uint64_t* a_empty = bars + 14;   // [2]
-    uint64_t* at_full = bars + 16;
-    uint64_t* y_full = bars + 17;    // [2]
-    uint64_t* y_empty = bars + 19;   // [2]
-    uint64_t* state_ready = bars + 21;
-    uint64_t* state_done = bars + 22;
-    uint64_t* conv_group = bars + 23;  // barrier among the four feature warps
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 25);
-    uint64_t* inter_done = bars + 28;  // tf32 read-outs of a chunk complete (state may be updated)
-    uint64_t* final_done = bars + 29;  // every tensor-core operation of the CTA complete
+    uint64_t* full_kv = bars;        // [4] ring stages
+    uint64_t* empty_kv = bars + 4;   // [4]
+    uint64_t* conv_kv = bars + 8;    // [4]
+    uint64_t* full_q = bars + 12;    // [4]
+    uint64_t* empty_q = bars + 16;   // [4]
+    uint64_t* conv_q = bars + 20;    // [4]
+    uint64_t* a_full = bars + 24;    // [2]
+    uint64_t* a_empty = bars + 26;   // [2]
+    uint64_t* at_full = bars + 28;   // [2] masked scores written (per buffer)
+    uint64_t* y_full = bars + 32;    // [2]
+    uint64_t* y_empty = bars + 34;   // [2]
+    uint64_t* state_ready = bars + 36;
+    uint64_t* state_done = bars + 37;
+    uint64_t* conv_group = bars + 38;  // barrier among the four feature warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 39);
+    uint64_t* inter_done = bars + 40;  // tf32 read-outs of a chunk complete (state may be updated)
+    uint64_t* final_done = bars + 41;  // every tensor-core operation of the CTA complete
     // [4] scale/den of item n in inv_den[n & 3] (normalizer only).  Four
     // phases in flight at most: the scores of item n + 4 are issued only
     // after the output stage has read item n + 1 out of TMEM.
-    uint64_t* den_full = bars + 30;
+    uint64_t* den_full = bars + 42;  // [4]
 #ifdef LA_TRACE
-    unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 40);
+    unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 46);
     if (threadIdx.x < 8) la_trace_ctr[threadIdx.x] = 0;
 #endif
 
@@ -235,23 +248,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto Qb = [&](int s) { return q_base + s * Cf::kQStage; };
     auto Qd = [&](int s) { return q_base + s * Cf::kQStage + Cf::kTile; };
     auto Qf = [&](int s) { return q_base + s * Cf::kQStage + Cf::kTile; };  // fp32 phi(Q) (linear rule)
-    uint8_t* ATh = at_base;
-    uint8_t* ATl = at_base + 8192;
+    constexpr int NAT = Cf::kNAT ? Cf::kNAT : 1;
+    auto ATh = [&](int buf) { return at_base + buf * 16384; };  // masked scores, hi part
+    auto ATl = [&](int buf) { return at_base + buf * 16384 + 8192; };  // lo part
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&full_kv[i], 1);
             mbar_init(&empty_kv[i], 1);
             mbar_init(&conv_kv[i], 4);
             mbar_init(&full_q[i], 1);
             mbar_init(&empty_q[i], 1);
             mbar_init(&conv_q[i], 4);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], 4);
+            mbar_init(&at_full[i], 4);
             mbar_init(&y_full[i], 1);
             mbar_init(&y_empty[i], 4);
         }
-        mbar_init(at_full, 4);
         mbar_init(state_ready, 4);
         mbar_init(state_done, 1);
         mbar_init(conv_group, 4);
@@ -293,28 +309,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&y_full[yb], (m / NY) & 1, err, kErrYFull)) return false;
         tc_fence_after();
         if (quad == 0 && lane == 0) LA_TR(4, 3, m);
+        // all 64 tokens of this lane in one round trip to TMEM; the buffer is
+        // released before the stores
+        uint32_t y0[32], y1[32];
+        tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 0), y0);
+        tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 32), y1);
+        tmem_ld_wait();
+        reg_fence(y0);
+        reg_fence(y1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&y_empty[yb]);
         // scale/den of item m, written by the four score warps
         if (NORM && !warp_wait(&den_full[m & 3], (m >> 2) & 1, err, kErrYFull)) return false;
         if (quad == 0 && lane == 0) LA_TR(4, 4, m);
         const float4* idn4 = reinterpret_cast<const float4*>(inv_den + (m & 3) * 64);
         const size_t tstride = (size_t)Hq * D;
         const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
-        // A rolled loop over 8-token groups (each read from TMEM as it is
-        // needed) keeps this stage's code small in the instruction cache.
-#pragma unroll 1
-        for (int g = 0; g < 8; ++g) {
-            uint32_t yv[8];
-            tmem_ld8(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, g * 8), yv);
-            tmem_ld_wait();
-            reg_fence(yv);
-            if (vrow_ok) {
+        if (vrow_ok) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
                 const float4 fa = NORM ? idn4[2 * g] : make_float4(scale, scale, scale, scale);
                 const float4 fb = NORM ? idn4[2 * g + 1] : fa;
                 const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int x = g * 8 + e;
-                    const float o = f[e] * __uint_as_float(yv[e]);
+                    const float o = f[e] * __uint_as_float(x < 32 ? y0[x] : y1[x - 32]);
                     if (x < valid) {
                         if (OUT_BF16)
                             reinterpret_cast<__nv_bfloat16*>(yout)[base + x * tstride] = __float2bfloat16_rn(o);
@@ -324,9 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&y_empty[yb]);
         if (quad == 0 && lane == 0) LA_TR(4, 5, m);
         return true;
     };
@@ -493,19 +511,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (lead) LA_TR(1, 9, i);
                         }
                         if (TF32 && r == G - 1) mma_commit(inter_done, lead);
-                        ok = warp_wait(at_full, n & 1, err, kErrATFull);
+                        const int tb = n % NAT;
+                        ok = warp_wait(&at_full[tb], (n / NAT) & 1, err, kErrATFull);
                         if (!ok) break;
                         tc_fence_after();
                         if (lead) LA_TR(1, 7, n);
-                        // intra: Y^T += V^T . A^T (hi [+ lo]).  The masked-score buffer is
-                        // free again for item n + 1 once its scores complete, because
-                        // tensor-core operations complete in issue order.
+                        // intra: Y^T += V^T . A^T (hi [+ lo])
 #pragma unroll 1
                         for (int ks = 0; ks < kC / 16; ++ks) {
                             const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                            mma_ss(tY, av, sdesc_sw128(smem_u32(ATh + ks * 32), 16, 1024), id_intra, 1, lead);
+                            mma_ss(tY, av, sdesc_sw128(smem_u32(ATh(tb) + ks * 32), 16, 1024), id_intra, 1, lead);
                             if (ALO)
-                                mma_ss(tY, av, sdesc_sw128(smem_u32(ATl + ks * 32), 16, 1024), id_intra, 1, lead);
+                                mma_ss(tY, av, sdesc_sw128(smem_u32(ATl(tb) + ks * 32), 16, 1024), id_intra, 1, lead);
                         }
                     }
                     mma_commit(&y_full[yb], lead);
@@ -709,33 +726,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 1, n);
                     const uint32_t tA = tmem + Cf::kColA + 80 * ab;
-                    if (NORM) {
-                        uint32_t z[16];
-                        tmem_ld16(tmem_addr(tA, quad * 32, 64), z);
-                        tmem_ld_wait();
-                        reg_fence(z);
-                        den = __uint_as_float(z[0]) + __uint_as_float(z[1]) + eps;
-                    }
+                    // every score of this row in one round trip to TMEM; the buffer
+                    // is released before the masking
+                    uint32_t r[32], r2[32], z[16];
                     if (MODE == kCausal) {
-                        // The masked-score buffer is free: the intra product of item
-                        // n - 1 was issued before the scores of item n and has
-                        // completed with them.  A rolled loop over 8-column groups,
-                        // each read from TMEM as it is needed.
+                        tmem_ld32(tmem_addr(tA, quad * 32, 0), r);
+                        tmem_ld32(tmem_addr(tA, quad * 32, 32), r2);
+                    }
+                    if (NORM) tmem_ld16(tmem_addr(tA, quad * 32, 64), z);
+                    tmem_ld_wait();
+                    if (MODE == kCausal) {
+                        reg_fence(r);
+                        reg_fence(r2);
+                    }
+                    if (NORM) reg_fence(z);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_empty[ab]);  // TMEM scores read out
+                    if (NORM) den = __uint_as_float(z[0]) + __uint_as_float(z[1]) + eps;
+                    if (MODE == kCausal) {
                         const float* gc = reinterpret_cast<const float*>(Gc(s));
                         const float gi = (GATED && arow_ok) ? gc[arow] : 0.f;
-#pragma unroll 1
-                        for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
-                            uint32_t r[8];
-                            tmem_ld8(tmem_addr(tA, quad * 32, cch * 8), r);
-                            tmem_ld_wait();
-                            reg_fence(r);
-                            if (arow_ok) {
+                        const int tb = n % NAT;
+                        if (n >= NAT) {
+                            // the intra product that read this buffer last (item n - NAT)
+                            // has completed: its completion is the y_full phase of that item
+                            ok = warp_wait(&y_full[(n - NAT) % NY], ((n - NAT) / NY) & 1, err, kErrATEmpty);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        if (arow_ok) {
+#pragma unroll
+                            for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
                                 const uint32_t off = sw128_offset(arow, cch * 16);
                                 float v[8];
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
                                     const int j = cch * 8 + e;
-                                    float x = (j <= arow) ? __uint_as_float(r[e]) : 0.f;
+                                    float x = j < 32 ? __uint_as_float(r[j]) : __uint_as_float(r2[j - 32]);
+                                    x = (j <= arow) ? x : 0.f;
                                     if (NORM) den += x;
                                     if (GATED && j <= arow) x *= __expf(gi - gc[j]);
                                     v[e] = x;
@@ -743,21 +772,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (ALO) {
                                     uint4 hv, lv;
                                     split8(v, hv, lv);
-                                    *reinterpret_cast<uint4*>(ATh + off) = hv;
-                                    *reinterpret_cast<uint4*>(ATl + off) = lv;
+                                    *reinterpret_cast<uint4*>(ATh(tb) + off) = hv;
+                                    *reinterpret_cast<uint4*>(ATl(tb) + off) = lv;
                                 } else {
-                                    *reinterpret_cast<uint4*>(ATh + off) = f_to_bf8(v);
+                                    *reinterpret_cast<uint4*>(ATh(tb) + off) = f_to_bf8(v);
                                 }
                             }
                         }
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_empty[ab]);  // TMEM scores read out
                     if (MODE == kCausal) {
                         fence_proxy_async();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(at_full);
+                        if (lane == 0) mbar_arrive(&at_full[n % NAT]);
                         if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 2, n);
                     }
                 }

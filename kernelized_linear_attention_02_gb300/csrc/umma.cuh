@@ -65,6 +65,10 @@ __device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint64_t* b, uint32_t pa
     return ok;
 }
 constexpr uint32_t kSuspendHintNs = 1000000;  // 1 ms; a completed phase wakes the thread at once
+// Sleep between two failed polls: a polling warp would otherwise issue an
+// instruction every few cycles and take issue slots from the warps that share
+// its sub-partition and do the work.
+constexpr uint32_t kBackoffNs = 64;
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
@@ -81,8 +85,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, unsigned
     const uint64_t t0 = global_timer_ns();
     for (;;) {
 #pragma unroll 1
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 16; ++i) {
             if (mbar_try_wait_sleep(b, parity, kSuspendHintNs)) return true;
+            __nanosleep(kBackoffNs);
+        }
         if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(err, code);
             return false;
@@ -105,6 +111,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, unsigned
         for (int i = 0; i < 16; ++i) {
             done = __ballot_sync(full, mbar_try_wait_sleep(b, parity, kSuspendHintNs));
             if (done == full) return true;
+            __nanosleep(kBackoffNs);
         }
         int tout = 0;
         if (lane == 0) tout = (global_timer_ns() - t0) > limit_ns;
