@@ -353,6 +353,25 @@ def cpu_baseline(w, budget_s=8.0):
                       f"fp64 recurrence, one thread per (batch, kv-head) stream"}
 
 
+def measured_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "chunk_kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    for rel, digest in rec.get("sources_sha256", {}).items():
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
+            return None
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    return rec.get("traffic_bytes_per_launch", {}).get(workload)
+
+
 def run_gpu(args):
     import kernelized_linear_attention_02_gb300 as la
     world, rank, local = dist_init()
@@ -394,11 +413,7 @@ def run_gpu(args):
 
     if rank != 0:
         return
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            traffic = json.load(f).get(w.name)
+    traffic = measured_traffic(w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -409,7 +424,9 @@ def run_gpu(args):
                    "l2": f"inputs rotate over {nsets} sets ({nsets * alg / 1e6:.0f} MB > L2)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                     "peak_source": pk["source"], "alg_bytes_per_launch": alg},
+                     "peak_source": pk["source"], "alg_bytes_per_call": alg,
+                     "scope": "one la_forward_causal call (segment state pass + causal pass); traffic: the "
+                              "causal pass, one launch"},
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
