@@ -29,12 +29,11 @@
 // memory.
 //
 // Roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-5 state (start and final state; gated rule: hi/lo copy of
-// the carried state and its decay; linear rule: the output stage), warps
-// 6-9 epilogue (masking of the scores, 1/den; gated rule: also the output
-// stage), warps 10-13 feature maps (phi of keys and queries, Z rows and
-// sums).  Every wait is bounded and reports a code in
-// *err instead of hanging.
+// owner, warps 2-5 state and output (start and final state, the output stage;
+// gated rule: also the hi/lo copy of the carried state and its decay), warps
+// 6-9 epilogue (masking of the scores, 1/den), warps 10-13 feature maps (phi
+// of keys and queries, Z rows and sums).  Every wait is bounded and reports
+// a code in *err instead of hanging.
 //
 // Pipeline per chunk i (G query heads per kv head): the feature warps run
 // ahead of the tensor core, limited only by the load rings; the MMA issues
@@ -647,7 +646,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // updates it without further hand-offs
             publish_state();
         } else {
+            // Gated causal: these warps also run the output stage, between the
+            // state conversions.  Per chunk i: outputs of heads 0..G-3 of chunk
+            // i-1, the conversion of S(i), then heads G-2 and G-1 of chunk i-1.
+            // The update of chunk i-1 (which S(i) waits for) follows the read-out
+            // of its last head, which needs the Y buffer of head G-3 released
+            // first, so those outputs must come before the conversion.
+            constexpr bool kOut = MODE == kCausal;
             for (int i = 0; i < nck && ok; ++i) {
+                if (kOut && i > 0)
+                    for (int r = 0; r < G - 2 && ok; ++r) ok = emit_y((i - 1) * G + r);
+                if (!ok) break;
                 // S(i): after the update of chunk i-1 and every read-out that used S_prev
                 if (i > 0) {
                     ok = warp_wait(state_done, (i - 1) & 1, err, kErrStateDone);
@@ -667,7 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 publish_state();
                 if (st_t == 0) LA_TR(2, 6, i);
                 if (MODE == kState) gsum += gtot;
+                if (kOut && i > 0)
+                    for (int r = max(0, G - 2); r < G && ok; ++r) ok = emit_y((i - 1) * G + r);
             }
+            if (kOut && nck > 0)
+                for (int r = 0; r < G && ok; ++r) ok = emit_y((nck - 1) * G + r);
         }
         if (TF32 && MODE != kState) {
             // linear rule: the state needs no per-chunk work here, so these
@@ -714,8 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool arow_ok = lane < 16;
         const int n_total = Cf::kHasQ ? nck * G : 0;
         bool ok = true;
-        for (int n = 0; n <= n_total && ok; ++n) {
-            if (n < n_total) {
+        for (int n = 0; n < n_total && ok; ++n) {
+            {
                 // -------- scores of item n: mask, decay, hi/lo split, 1/den
                 const int ab = n % NA;
                 const int s = (n / G) % NKV1;
@@ -795,7 +808,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&den_full[n & 3]);
                 }
             }
-            if (!TF32 && n >= 1) ok = emit_y(n - 1);  // gated: the output stage runs here
         }
     } else {
         // ------------------------------------------------------ feature warps
