@@ -103,6 +103,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, unsigned
                                           uint64_t limit_ns = 2000000000ull) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
+    // fast path: a phase that has already completed costs one poll (the
+    // timer is read only when the wait actually waits)
+    if (__ballot_sync(full, mbar_try_wait(b, parity)) == full) return true;
     uint64_t t0 = 0;
     if (lane == 0) t0 = global_timer_ns();
     for (;;) {
