@@ -28,12 +28,14 @@
 // not exactly representable in bf16.  All accumulation is fp32 in tensor
 // memory.
 //
-// Roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// Roles (480 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-5 state and output (start and final state, the output stage;
 // gated rule: also the hi/lo copy of the carried state and its decay), warps
 // 6-9 epilogue (masking of the scores, 1/den), warps 10-13 feature maps (phi
-// of keys and queries, Z rows and sums).  Every wait is bounded and reports
-// a code in *err instead of hanging.
+// of keys and queries, Z rows and sums), warp 14 (linear causal rule only)
+// second MMA issuer: the read-outs with the carried state and the state
+// updates, while warp 1 issues the scores and intra products.  Every wait is
+// bounded and reports a code in *err instead of hanging.
 //
 // Pipeline per chunk i (G query heads per kv head): the feature warps run
 // ahead of the tensor core, limited only by the load rings; the MMA issues
@@ -59,8 +61,8 @@ namespace chunk {
 using namespace umma;
 
 constexpr int kC = 64;  // tokens per chunk
-constexpr int kThreads = 448;
-constexpr int kStateWarp0 = 2, kEpiWarp0 = 6, kFeatWarp0 = 10;
+constexpr int kThreads = 480;
+constexpr int kStateWarp0 = 2, kEpiWarp0 = 6, kFeatWarp0 = 10, kMmaSWarp = 14;
 
 template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16>
 struct Cfg {
@@ -88,6 +90,12 @@ struct Cfg {
     // phi(Q) (64 x D, D/32 swizzled blocks of 8 KB); the gated rule, whose
     // state is rescaled every chunk anyway, reads a bf16 hi/lo copy of it
     static constexpr bool kTf32 = !GATED;
+    // linear causal with grouped query heads (G > 1, decided at run time):
+    // two MMA issuers -- warp 1 the scores and the intra products, warp 14 the
+    // read-outs of all G heads with the carried state and the state updates --
+    // so that the waits of one overlap the issue of the other.  With one query
+    // head per kv head the single issuer interleaves them better.
+    static constexpr bool kSplitMma = kTf32 && MODE == kCausal;
     static constexpr int kQf = (kHasQ && kTf32) ? 2 * kTile : 0;
     static constexpr int kQStage = kHasQ ? kTile * (GATED ? 2 : 1) + kQf : 0;
     // masked scores as bf16 hi + lo (one bf16 part suffices without the
@@ -213,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // phases in flight at most: the scores of item n + 4 are issued only
     // after the output stage has read item n + 1 out of TMEM.
     uint64_t* den_full = bars + 42;  // [4]
+    uint64_t* inter_cmp = bars + 50;  // [2] read-out of item n complete (split issue; per Y^T buffer)
+    uint64_t* upd_done = bars + 52;   // state update of a chunk complete (split issue)
 #ifdef LA_TRACE
     unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 46);
     if (threadIdx.x < 8) la_trace_ctr[threadIdx.x] = 0;
@@ -225,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // capture by reference, and reading the parameter block through its
     // address inside hot loops would be a long-latency load per use.
     const int T = a.T, Hq = a.Hq, Hkv = a.Hkv, G = a.G, nseg = a.nseg;
+    const bool split = Cf::kSplitMma && G > 1;  // two MMA issuers (see Cfg::kSplitMma)
     constexpr int fmap = FMAP;
     const float eps = a.eps, scale = a.scale;
     const __nv_bfloat16* __restrict__ decay = a.decay;
@@ -254,10 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) {
             mbar_init(&full_kv[i], 1);
-            mbar_init(&empty_kv[i], 1);
+            mbar_init(&empty_kv[i], split ? 2 : 1);
             mbar_init(&conv_kv[i], 4);
             mbar_init(&full_q[i], 1);
-            mbar_init(&empty_q[i], 1);
+            mbar_init(&empty_q[i], split ? 2 : 1);
             mbar_init(&conv_q[i], 4);
         }
         for (int i = 0; i < 2; ++i) {
@@ -272,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(conv_group, 4);
         for (int i = 0; i < 4; ++i) mbar_init(&den_full[i], 4);
         mbar_init(inter_done, 1);
-        mbar_init(final_done, 1);
+        mbar_init(final_done, split ? 2 : 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&inter_cmp[i], 1);
+        mbar_init(upd_done, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -407,6 +420,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
 
+            if (Cf::kSplitMma && split) {
+                // scores and intra products; the read-outs and updates are warp 14's
+                const int N = nck * G;
+                for (int n = 0; n < N && ok; ++n) {
+                    const int i = n / G, r = n - i * G, s = i % NKV1, sq = n % NQ1, ab = n % NA, yb = n % NY;
+                    const int tb = n % NAT;
+                    if (r == 0) {
+                        ok = warp_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
+                        if (!ok) break;
+                        tc_fence_after();
+                        if (lead) LA_TR(1, 1, i);
+                    }
+                    ok = warp_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lead) LA_TR(1, 2, n);
+                    if (n >= NA) {
+                        ok = warp_wait(&a_empty[ab], ((n / NA) & 1) ^ 1, err, kErrAEmpty);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    // scores, and in columns 64..71 phi(q).[Z_hi; Z_lo] from the Z rows
+                    const uint32_t tA = tmem + Cf::kColA + 80 * ab;
+#pragma unroll 1
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
+                        const uint32_t ko = (ks >> 2) * Cf::kKBlk + (ks & 3) * 32;
+                        mma_ss(tA, sdesc_sw128(smem_u32(Qb(sq) + qo), 16, 1024),
+                               sdesc_sw128(smem_u32(Kb(s) + ko), 16, 1024), id_scores, ks > 0, lead);
+                    }
+                    mma_commit(&a_full[ab], lead);
+                    mma_commit(&empty_q[sq], lead);  // this warp is done with the query slot
+                    if (lead) LA_TR(1, 3, n);
+                    ok = warp_wait(&at_full[tb], (n / NAT) & 1, err, kErrATFull);
+                    if (!ok) break;
+                    // the read-out of item n (warp 14) starts this Y^T buffer: complete first
+                    ok = warp_wait(&inter_cmp[yb], (n / NY) & 1, err, kErrStateDone);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lead) LA_TR(1, 7, n);
+                    const uint32_t tY = tmem + Cf::kColY + 64 * yb;
+#pragma unroll 1
+                    for (int ks = 0; ks < kC / 16; ++ks) {
+                        const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
+                        mma_ss(tY, av, sdesc_sw128(smem_u32(ATh(tb) + ks * 32), 16, 1024), id_intra, 1, lead);
+                        if (ALO) mma_ss(tY, av, sdesc_sw128(smem_u32(ATl(tb) + ks * 32), 16, 1024), id_intra, 1, lead);
+                    }
+                    mma_commit(&y_full[yb], lead);
+                    if (lead) LA_TR(1, 8, n);
+                    if (r == G - 1) mma_commit(&empty_kv[s], lead);  // this warp is done with the K/V slot
+                }
+                mma_commit(final_done, lead);  // every operation of this warp complete
+            } else {
             for (int i = 0; i < nck && ok; ++i) {
                 const int s = i % NKV1;
                 if (Cf::kHasKV) {
@@ -542,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // last: every operation above has completed (also after an early exit)
             if (TF32 && MODE == kCausal) mma_commit(final_done, lead);
+            }
         }
     } else if (warp < kEpiWarp0) {
         // -------------------------------------------------------- state warps
@@ -808,6 +875,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&den_full[n & 3]);
                 }
             }
+        }
+    } else if (warp == kMmaSWarp) {
+        // ------------------------------------------------ MMA issuer of the state
+        // (split issue only): per chunk, the read-out of every query head with
+        // the carried fp32 state (kind::tf32, state from TMEM as A), then the
+        // state update once those read-outs have completed.
+        if (Cf::kSplitMma && split) {
+            const uint32_t lead = lane == 0;
+            bool ok = true;
+            constexpr uint32_t id_inter_tf32 = idesc_tf32(D, 64);
+            constexpr uint32_t id_state = idesc_bf16(D, D, true, true);
+            const uint32_t tS = tmem + Cf::kColS;
+            for (int i = 0; i < nck && ok; ++i) {
+                const int s = i % NKV1;
+                // S before chunk i: the start state (state warps) or this warp's last update
+                ok = i == 0 ? warp_wait(state_ready, 0, err, kErrStateReady)
+                            : warp_wait(upd_done, (i - 1) & 1, err, kErrStateDone);
+                if (!ok) break;
+                tc_fence_after();
+                if (lead) LA_TR(5, 4, i);
+                int n = i * G;
+                for (int r = 0; r < G && ok; ++r) {
+                    n = i * G + r;
+                    const int sq = n % NQ1, yb = n % NY;
+                    ok = warp_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ);
+                    if (!ok) break;
+                    if (n >= NY) ok = warp_wait(&y_empty[yb], ((n / NY) & 1) ^ 1, err, kErrYEmpty);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lead) LA_TR(5, 5, n);
+                    const uint32_t tY = tmem + Cf::kColY + 64 * yb;
+#pragma unroll 1
+                    for (int ks = 0; ks < D / 8; ++ks) {
+                        const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
+                        mma_ts_tf32(tY, tS + ks * 8, sdesc_sw128(smem_u32(Qf(sq) + ko), 16, 1024), id_inter_tf32,
+                                    ks > 0, lead);
+                    }
+                    mma_commit(&empty_q[sq], lead);     // this warp is done with the query slot
+                    mma_commit(&inter_cmp[yb], lead);   // the intra product may add to Y^T
+                    if (lead) LA_TR(5, 6, n);
+                }
+                if (!ok) break;
+                // the update overwrites S, which the read-outs take as their A
+                // operand: wait for the last one (and with it every earlier one)
+                ok = warp_wait(&inter_cmp[n % NY], (n / NY) & 1, err, kErrStateDone);
+                if (!ok) break;
+                ok = warp_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
+                if (!ok) break;
+                tc_fence_after();
+                // S^T += V^T . phi(K)
+#pragma unroll 1
+                for (int ks = 0; ks < kC / 16; ++ks) {
+                    const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
+                    mma_ss(tS, av, sdesc_sw128(smem_u32(Kb(s) + ks * 2048), (uint32_t)Cf::kKBlk, 1024), id_state, 1,
+                           lead);
+                }
+                mma_commit(&empty_kv[s], lead);  // this warp is done with the K/V slot
+                mma_commit(upd_done, lead);
+                if (lead) LA_TR(5, 9, i);
+            }
+            mma_commit(final_done, lead);  // every operation of this warp complete
         }
     } else {
         // ------------------------------------------------------ feature warps

@@ -110,6 +110,8 @@ SHAPES = [  # B, T, Hq, Hkv, Dk, Dv
     (2, 130, 3, 1, 32, 64),
     (1, 200, 2, 2, 128, 64),
     (1, 129, 4, 2, 64, 128),
+    (2, 200, 6, 2, 64, 64),    # GQA, 3 query heads per kv head (two MMA issuers; gated output order)
+    (1, 96, 8, 1, 64, 64),     # GQA, 8 query heads per kv head
 ]
 MODES = [("elu_plus_one", True), ("relu", True), ("elu_plus_one", False), ("none", False)]
 
