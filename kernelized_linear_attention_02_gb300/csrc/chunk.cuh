@@ -106,7 +106,18 @@ struct Cfg {
     static constexpr int kNAT = MODE == kCausal ? 1 : 0;
     static constexpr int kAT = kNAT * 2 * 8192;  // per buffer: hi, lo (64 x 64 bf16 each)
     static constexpr int kZrApply = (MODE == kApply && NORM) ? kZr : 0;
-    static constexpr int kMisc = 10 * 1024;  // 1/den ring (1 KB), partial Z sums (8 KB), barriers
+    // feature-map warps: 4 (warps 10-13), or 8 in the state pass (warps 6-13),
+    // which has no scores for the epilogue warps to mask
+    static constexpr int kFeatWarps = MODE == kState ? 8 : 4;
+    static constexpr int kFeatW0 = MODE == kState ? kEpiWarp0 : kFeatWarp0;
+    static constexpr int kFeatThreads = 32 * kFeatWarps;
+    // vectorised tile passes of the feature warps: 16-byte chunks
+    static constexpr int kCPR = D / 8;                    // chunks per 64 x D tile row
+    static constexpr int kRowStep = kFeatThreads / kCPR;  // rows covered by one pass
+    static constexpr int kPer = 64 / kRowStep;            // chunks per thread per tile
+    static_assert(kRowStep * kPer == 64, "feature pass covers the tile");
+    static constexpr int kZpart = kRowStep * D;  // floats of one buffer of partial Z sums
+    static constexpr int kMisc = 1024 + 2 * kZpart * 4 + 512;  // 1/den ring, partial Z sums (x2), barriers
     static constexpr int bytes(int nkv, int nq) {
         return 1024 + nkv * kKvStage + nq * kQStage + kAT + kZrApply + kMisc;
     }
@@ -135,10 +146,6 @@ struct Cfg {
     static constexpr uint32_t kColY = kColA + 80 * kNA;
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kColY + 64 * kNY <= kTmemCols, "TMEM budget");
-    // vectorised tile passes: 16-byte chunks, 128 threads
-    static constexpr int kCPR = D / 8;           // chunks per 64 x D tile row
-    static constexpr int kRowStep = 128 / kCPR;  // rows covered by one pass of 128 threads
-    static constexpr int kPer = 64 / kRowStep;   // chunks per thread per tile
 };
 
 // Rounds a shared-memory pointer up to 1024 bytes by pointer arithmetic (not
@@ -198,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* zr_apply = at_base + Cf::kAT;
     float* misc = reinterpret_cast<float*>(zr_apply + Cf::kZrApply);
     float* inv_den = misc;           // [4][64] scale / den of the last four items
-    float* zpart = misc + 256;       // [2][1024] partial column sums of phi(K)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + 256 + 2048);
+    float* zpart = misc + 256;       // [2][kZpart] partial column sums of phi(K)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + 256 + 2 * Cf::kZpart);
     uint64_t* full_kv = bars;        // [4] ring stages
     uint64_t* empty_kv = bars + 4;   // [4]
     uint64_t* conv_kv = bars + 8;    // [4]
@@ -213,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* y_empty = bars + 34;   // [2]
     uint64_t* state_ready = bars + 36;
     uint64_t* state_done = bars + 37;
-    uint64_t* conv_group = bars + 38;  // barrier among the four feature warps
+    uint64_t* conv_group = bars + 38;  // barrier among the feature warps
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 39);
     uint64_t* inter_done = bars + 40;  // tf32 read-outs of a chunk complete (state may be updated)
     uint64_t* final_done = bars + 41;  // every tensor-core operation of the CTA complete
@@ -266,10 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 4; ++i) {
             mbar_init(&full_kv[i], 1);
             mbar_init(&empty_kv[i], split ? 2 : 1);
-            mbar_init(&conv_kv[i], 4);
+            mbar_init(&conv_kv[i], Cf::kFeatWarps);
             mbar_init(&full_q[i], 1);
             mbar_init(&empty_q[i], split ? 2 : 1);
-            mbar_init(&conv_q[i], 4);
+            mbar_init(&conv_q[i], Cf::kFeatWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&a_full[i], 1);
@@ -280,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(state_ready, 4);
         mbar_init(state_done, 1);
-        mbar_init(conv_group, 4);
+        mbar_init(conv_group, Cf::kFeatWarps);
         for (int i = 0; i < 4; ++i) mbar_init(&den_full[i], 4);
         mbar_init(inter_done, 1);
         mbar_init(final_done, split ? 2 : 1);
@@ -303,6 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (tid == 0) LA_TR(0, 0, 0);
+    // state pass: the causal pass that consumes its increments may launch now
+    // (programmatic dependent launch); it waits for this grid's completion
+    // only where it reads them
+    if (MODE == kState && tid == 0) griddep_launch_dependents();
     const uint32_t tmem = *tmem_slot;
     unsigned* err = a.err;
 
@@ -627,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // initial state, decay-weighted for gated.
         const bool fold = MODE == kCausal && a.S_seg && seg > 0;
         const float* S_start = MODE == kState ? nullptr : a.S_init;
+        if (MODE == kCausal) griddep_wait();  // the segment state pass has completed
         // Loads are batched 32 columns x 2 segments at a time (independent
         // addresses, all in flight together); the additions keep the segment
         // order 0, 1, ..., seg-1.
@@ -784,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (MODE == kState && GATED && st_t == 0) a.G_dst[(size_t)bh * nseg + seg] = gsum;
             }
         }
-    } else if (warp < kFeatWarp0) {
+    } else if (warp < Cf::kFeatW0) {
         // -------------------------------------------------------------- epilogue
         const int quad = warp & 3;
         const bool m64 = D == 64;
@@ -944,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rule, the Z rows of every chunk and the running key sum Z.  Runs
         // ahead of the state chain, limited only by the load rings.
         constexpr int kCPR = Cf::kCPR, kRowStep = Cf::kRowStep, kPer = Cf::kPer;
-        const int ct = tid - kFeatWarp0 * 32;  // 0..127
+        const int ct = tid - Cf::kFeatW0 * 32;  // 0 .. kFeatThreads - 1
         const int cc = ct % kCPR;              // 16-byte chunk column: features 8cc..8cc+7
         const int rbase = ct / kCPR;           // rows rbase + kRowStep * m
         bool ok = true;
@@ -965,11 +977,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (NORM && MODE != kState) {
             const int nzr = MODE == kApply ? 1 : NKV;
             for (int z = 0; z < nzr; ++z)
-                for (int e = ct; e < D * 6; e += 128) zr_elem(z, 2 + e / D, e % D) = __float2bfloat16(0.f);
+                for (int e = ct; e < D * 6; e += Cf::kFeatThreads) zr_elem(z, 2 + e / D, e % D) = __float2bfloat16(0.f);
         }
         // running key sum Z in a register of thread k < D (state pass: the increment)
         float zreg = 0.f;
-        if (NORM && ct < D && MODE != kState) {
+        // start key sum: the initial Z plus, for a later sequence segment, the
+        // increments of the earlier ones (written by the segment state pass:
+        // its completion is awaited first)
+        auto start_z = [&]() {
+            griddep_wait();
             const bool fold = MODE == kCausal && a.S_seg && seg > 0;
             zreg = a.Z_init ? a.Z_init[(size_t)bh * D + ct] : 0.f;
             if (fold && a.Z_seg) {
@@ -983,7 +999,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < 4; ++u) zreg += z4[u];
                 }
             }
-        }
+        };
+        if (NORM && ct < D && MODE == kApply) start_z();
 
         // ---- keys of chunk i: feature map (+ lo part), decayed keys, Z rows and sums
         auto process_kv = [&](int i) -> bool {
@@ -1054,7 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ct == 0) LA_TR(2, 8, i);
                 if (NORM) {
                     // Z rows of this chunk hold Z_prev (hi, lo); then Z += column sums
-                    float* zp = zpart + zbuf * 1024;
+                    float* zp = zpart + zbuf * Cf::kZpart;
                     *reinterpret_cast<float4*>(zp + rbase * D + 8 * cc) =
                         make_float4(colsum[0], colsum[1], colsum[2], colsum[3]);
                     *reinterpret_cast<float4*>(zp + rbase * D + 8 * cc + 4) =
@@ -1062,6 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
                     if (ct == 0) LA_TR(2, 9, i);
                     if (ct < D) {
+                        if (MODE == kCausal && i == 0) start_z();
                         if (MODE != kState) {
                             const __nv_bfloat16 h = __float2bfloat16_rn(zreg);
                             zr_elem(s, 0, ct) = h;

@@ -41,6 +41,7 @@ struct Args {
 struct Launch {
     int mode;
     bool norm, gated, out_bf16;
+    bool pdl;  // launch as a programmatic dependent of the previous kernel on the stream
     dim3 grid;
     Args args;
     CUtensorMap mq, mk, mv;

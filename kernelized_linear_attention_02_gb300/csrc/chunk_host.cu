@@ -226,6 +226,7 @@ cudaError_t chunk_causal(const Problem& P, const void* q, const void* k, const v
         L.args.S_seg = S_seg;
         L.args.Z_seg = P.norm ? Z_seg : nullptr;
         L.args.G_seg = G_seg;
+        L.pdl = true;  // overlaps the state pass's tail; waits for it before the fold
     }
     L.grid = dim3((unsigned)BH, (unsigned)pl.nseg);
     L.args.S_dst = S_out;

@@ -22,7 +22,24 @@ cudaError_t run_one(const Launch& L, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured = dev;
     }
-    kern<<<L.grid, kThreads, Cf::kSmem, st>>>(L.args, L.mq, L.mk, L.mv);
+    if (L.pdl) {
+        // may start while the previous kernel (the segment state pass) drains;
+        // the kernel waits for it (griddepcontrol.wait) before reading its output
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = L.grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = Cf::kSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, L.args, L.mq, L.mk, L.mv);
+        if (e != cudaSuccess) return e;
+    } else {
+        kern<<<L.grid, kThreads, Cf::kSmem, st>>>(L.args, L.mq, L.mk, L.mv);
+    }
     note_launch();
     return cudaGetLastError();
 }
