@@ -202,40 +202,74 @@ def time_prefill(la, w, steps, warmup, stream):
 
 
 def time_prefill_e2e(la, w, steps, warmup, stream):
-    """Same call with host-resident inputs: pinned host -> device copies of q, k,
-    v, the call, and the device -> host copy of y, all inside the timed region."""
+    """Same call with host-resident inputs, as a serving loop would run it: every
+    step copies its q, k, v from pinned host memory to the device, runs the
+    call, and copies y back to pinned host memory, all inside the timed region.
+    Steps are pipelined over three streams (host->device copies, compute,
+    device->host copies) with two device buffer sets, so the copies of one
+    step overlap the compute of its neighbours."""
     q, k, v, d = inputs.make_qkv(w, device="cpu", seed=w.seed)
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     hd = d.pin_memory() if d is not None else None
-    hy = torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype).pin_memory()
-    dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (q, k, v))
-    dd = torch.empty_like(d, device="cuda") if d is not None else None
-    dy = torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype, device="cuda")
+    hys = [torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype).pin_memory() for _ in range(2)]
+    bufs = []
+    p = la.make_params(batch=w.B, seq_len=w.T, q_heads=w.q_heads, kv_heads=w.kv_heads, key_dim=w.Dk,
+                       value_dim=w.Dv, io_dtype=w.dtype, feature_map=w.feature_map,
+                       use_normalizer=w.use_normalizer, epsilon=w.eps, scale=w.scale, update_rule=w.rule)
+    for _ in range(2):
+        bufs.append(dict(q=torch.empty_like(q, device="cuda"), k=torch.empty_like(k, device="cuda"),
+                         v=torch.empty_like(v, device="cuda"),
+                         d=torch.empty_like(d, device="cuda") if d is not None else None,
+                         y=torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype, device="cuda"),
+                         ws=torch.empty(max(1, la.la_workspace_bytes(p, True)), dtype=torch.uint8, device="cuda")))
     kw = prefill_kwargs(w)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-    def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        if dd is not None:
-            dd.copy_(hd, non_blocking=True)
-        la.la_forward_causal(dq, dk, dv, decay=dd, out=dy, stream=stream, **kw)
-        hy.copy_(dy, non_blocking=True)
+    def step(i):
+        b = i % 2
+        u = bufs[b]
+        if used[b]:
+            s_in.wait_event(comp_done[b])      # inputs of step i-2 consumed
+        with torch.cuda.stream(s_in):
+            u["q"].copy_(hq, non_blocking=True)
+            u["k"].copy_(hk, non_blocking=True)
+            u["v"].copy_(hv, non_blocking=True)
+            if hd is not None:
+                u["d"].copy_(hd, non_blocking=True)
+        in_done[b].record(s_in)
+        stream.wait_event(in_done[b])
+        if used[b]:
+            stream.wait_event(out_done[b])     # y of step i-2 copied out
+        with torch.cuda.stream(stream):
+            la.la_forward_causal(u["q"], u["k"], u["v"], decay=u["d"], out=u["y"], workspace=u["ws"],
+                                 stream=stream, **kw)
+        comp_done[b].record(stream)
+        s_out.wait_event(comp_done[b])
+        with torch.cuda.stream(s_out):
+            hys[b].copy_(u["y"], non_blocking=True)
+        out_done[b].record(s_out)
+        used[b] = True
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(steps):
-            step()
+    ev0.record(s_in)
+    stream.wait_event(ev0)
+    s_out.wait_event(ev0)
+    for i in range(steps):
+        step(warmup + i)
+    stream.wait_event(out_done[(warmup + steps - 1) % 2])
+    stream.wait_event(out_done[(warmup + steps - 2) % 2])
     ev1.record(stream)
     torch.cuda.synchronize()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hd,) if hd is not None else ()))
-    return ev0.elapsed_time(ev1) / steps, h2d, hy.numel() * hy.element_size()
+    return ev0.elapsed_time(ev1) / steps, h2d, hys[0].numel() * hys[0].element_size()
 
 
 def time_decode(la, w, n_steps, warmup, stream):
@@ -428,7 +462,9 @@ def run_gpu(args):
                      "scope": "one la_forward_causal call (segment state pass + causal pass); traffic: the "
                               "causal pass, one launch"},
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "how": "pinned host buffers; per step h2d of q, k, v + la_forward_causal + d2h of y, "
+                       "pipelined over three streams with two device buffer sets"},
         "gpu_launches": launches,
         "clocks": clocks,
         "decode": dec,
