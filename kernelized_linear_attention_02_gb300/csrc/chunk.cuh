@@ -186,7 +186,10 @@ __device__ __forceinline__ __nv_bfloat16& bf_at(uint8_t* base, uint32_t off) {
     return *reinterpret_cast<__nv_bfloat16*>(base + off);
 }
 
-template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16>
+// SPLIT: two MMA issuers (linear causal rule with G > 1 query heads per kv
+// head, see Cfg::kSplitMma); a separate instantiation, so that the kernels
+// for G = 1 carry no code of the split issue.
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_kernel(const __grid_constant__ Args a, const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                  const __grid_constant__ CUtensorMap mapV) {
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // capture by reference, and reading the parameter block through its
     // address inside hot loops would be a long-latency load per use.
     const int T = a.T, Hq = a.Hq, Hkv = a.Hkv, G = a.G, nseg = a.nseg;
-    const bool split = Cf::kSplitMma && G > 1;  // two MMA issuers (see Cfg::kSplitMma)
+    constexpr bool split = Cf::kSplitMma && SPLIT;  // two MMA issuers
     constexpr int fmap = FMAP;
     const float eps = a.eps, scale = a.scale;
     const __nv_bfloat16* __restrict__ decay = a.decay;
@@ -431,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
 
-            if (Cf::kSplitMma && split) {
+            if constexpr (split) {
                 // scores and intra products; the read-outs and updates are warp 14's
                 const int N = nck * G;
                 for (int n = 0; n < N && ok; ++n) {
@@ -893,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (split issue only): per chunk, the read-out of every query head with
         // the carried fp32 state (kind::tf32, state from TMEM as A), then the
         // state update once those read-outs have completed.
-        if (Cf::kSplitMma && split) {
+        if constexpr (split) {
             const uint32_t lead = lane == 0;
             bool ok = true;
             constexpr uint32_t id_inter_tf32 = idesc_tf32(D, 64);

@@ -9,10 +9,10 @@
 namespace la {
 namespace chunk {
 
-template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUTBF>
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUTBF, bool SPLIT = false>
 cudaError_t run_one(const Launch& L, cudaStream_t st) {
     using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUTBF>;
-    auto kern = chunk_kernel<D, MODE, NORM, FMAP, GATED, OUTBF>;
+    auto kern = chunk_kernel<D, MODE, NORM, FMAP, GATED, OUTBF, SPLIT>;
     static int configured = -1;  // device on which the shared-memory limit was raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -49,6 +49,9 @@ template <int D, int MODE, int OUT>
 struct Dispatch {
     template <bool NORM, int FMAP, bool GATED>
     static cudaError_t one(const Launch& L, cudaStream_t st) {
+        // linear causal rule with grouped query heads: the two-issuer kernel
+        if (MODE == kCausal && !GATED && L.args.G > 1)
+            return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, MODE == kCausal && !GATED>(L, st);
         return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1>(L, st);
     }
     template <bool NORM>
