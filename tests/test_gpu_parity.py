@@ -112,6 +112,7 @@ SHAPES = [  # B, T, Hq, Hkv, Dk, Dv
     (1, 129, 4, 2, 64, 128),
     (2, 200, 6, 2, 64, 64),    # GQA, 3 query heads per kv head (two MMA issuers; gated output order)
     (1, 96, 8, 1, 64, 64),     # GQA, 8 query heads per kv head
+    (3, 150, 1, 1, 64, 64),    # odd number of (batch, kv head) streams: the last CTA runs one of a pair
 ]
 MODES = [("elu_plus_one", True), ("relu", True), ("elu_plus_one", False), ("none", False)]
 
