@@ -530,6 +530,27 @@ def run_only(args):
                       "roofline_frac": gbs / peaks()["hbm_gbs"], "launches_per_call": lpc}), flush=True)
 
 
+def run_decode_only(args):
+    """The decode step alone on the streaming-decode shape (B=256, H=32, D=128,
+    512 MiB fp32 state), with the state built from a short prompt of
+    --prompt tokens: the entry point for profiling the decode kernel on a case
+    that fits a full capture.  The step's work does not depend on the prompt
+    length."""
+    import dataclasses
+    import kernelized_linear_attention_02_gb300 as la
+    torch.cuda.set_device(0)
+    la.lib()
+    w = dataclasses.replace(inputs.DECODE, T=args.prompt)
+    stream = torch.cuda.Stream()
+    us, launches = time_decode(la, w, args.decode_steps, args.warmup, stream)
+    dbytes, sbytes = decode_alg_bytes(w)
+    pk = peaks()
+    print(json.dumps({"workload": w.name, "prompt": w.T, "us_per_step": us, "us_per_token": us / w.B,
+                      "state_GBps": sbytes / (us * 1e-6) / 1e9, "alg_GBps": dbytes / (us * 1e-6) / 1e9,
+                      "roofline_frac": dbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"], "gpu_launches": launches}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -543,6 +564,8 @@ def main():
     ap.add_argument("--only", default=None, help="time one workload of linattn_inputs (e.g. LONG_8K) alone")
     ap.add_argument("--batch", type=int, default=0, help="with --only: batch size override")
     ap.add_argument("--noncausal", action="store_true", help="with --only: the non-causal pass")
+    ap.add_argument("--decode-only", action="store_true", help="time the decode step alone (see --prompt)")
+    ap.add_argument("--prompt", type=int, default=64, help="with --decode-only: prompt tokens that build the state")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -550,6 +573,8 @@ def main():
         run_reference(args)
     elif args.only:
         run_only(args)
+    elif args.decode_only:
+        run_decode_only(args)
     else:
         run_gpu(args)
 

@@ -278,6 +278,16 @@ cudaError_t chunk_noncausal(const Problem& P, const void* q, const void* k, cons
     return run(La, D, st);
 }
 
+int device_sm_count() {
+    DevInfo di;
+    return dev_info(&di) ? di.sms : 0;
+}
+
+unsigned* device_error_word() {
+    DevInfo di;
+    return dev_info(&di) ? di.err : nullptr;
+}
+
 unsigned chunk_device_error(bool reset) {
     DevInfo di;
     if (!dev_info(&di)) return 0;

@@ -26,6 +26,10 @@ cudaError_t chunk_noncausal(const Problem& P, const void* q, const void* k, cons
                             cudaStream_t st);
 // Reads (and optionally clears) the error word of the bounded waits; 0 = none.
 unsigned chunk_device_error(bool reset);
+// The current device's SM count and the device address of that error word
+// (0 / nullptr if they cannot be queried).
+int device_sm_count();
+unsigned* device_error_word();
 
 // Decode step (decode.cu).
 bool decode_supported(const Problem& P);

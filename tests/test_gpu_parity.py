@@ -225,6 +225,38 @@ def test_decode_steps_small(dtype, rule):
         assert_close(to64(Z), Zr, 1e-5, "decode Z")
 
 
+DECODE_SHAPES = [  # B, Hq, Hkv, Dk, Dv
+    (2, 4, 2, 64, 128),   # Dk != Dv
+    (1, 8, 1, 128, 32),   # 8 query heads per kv head
+    (2, 2, 2, 20, 20),    # rows not a multiple of 16 bytes (bf16): the register-resident kernel
+    (3, 3, 3, 12, 12),    # small odd-width rows
+]
+
+
+@pytest.mark.parametrize("shape", DECODE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_decode_shapes(shape, dtype):
+    """Token-by-token steps from a prefilled state equal one causal pass, for
+    head sizes and groupings away from the benchmarked ones."""
+    B, Hq, Hkv, Dk, Dv = shape
+    T0, steps = 17, 5
+    T = T0 + steps
+    q = rand((B, T, Hq, Dk), 41, dtype, 0.5)
+    k = rand((B, T, Hkv, Dk), 42, dtype, 0.5)
+    v = rand((B, T, Hkv, Dv), 43, dtype)
+    kw = dict(q_heads=Hq, kv_heads=Hkv, feature_map="elu_plus_one", use_normalizer=True, out_dtype=torch.float32)
+    _, (S, Z) = la.la_forward_causal(q[:, :T0].contiguous(), k[:, :T0].contiguous(), v[:, :T0].contiguous(),
+                                     return_state=True, **kw)
+    ys = [la.la_decode_step(q[:, t:t + 1].contiguous(), k[:, t:t + 1].contiguous(), v[:, t:t + 1].contiguous(),
+                            S, Z, **kw) for t in range(T0, T)]
+    torch.cuda.synchronize()
+    yr, Sr, Zr = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="elu_plus_one", use_normalizer=True)
+    tol = tol_for(dtype, torch.float32)
+    assert_close(to64(torch.cat(ys, 1)), yr[:, T0:], tol, "decode y")
+    assert_close(to64(S), Sr, tol, "decode S")
+    assert_close(to64(Z), Zr, 1e-5, "decode Z")
+
+
 def test_invalid_call_raises_and_launches_nothing():
     q = torch.zeros(1, 4, 3, 16, dtype=torch.bfloat16, device=DEV)
     k = torch.zeros(1, 4, 2, 16, dtype=torch.bfloat16, device=DEV)
