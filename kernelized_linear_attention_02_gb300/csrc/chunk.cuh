@@ -61,6 +61,9 @@ namespace chunk {
 using namespace umma;
 
 constexpr int kC = 64;  // tokens per chunk
+// per-stage decay block (gated rule), floats: [0, 64) inclusive cumulative log
+// decay G_j, [64, 128) exp(ref - G_j), then ref and the "factored" flag
+constexpr int kGCol = 64, kGRef = 128, kGFlag = 129;
 constexpr int kThreads = 480;
 constexpr int kStateWarp0 = 2, kEpiWarp0 = 6, kFeatWarp0 = 10, kMmaSWarp = 14;
 
@@ -850,7 +853,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!ok) break;
                             tc_fence_after();
                         }
-                        if (arow_ok) {
+                        // masked row (decay-weighted for the gated rule): weight(j) is
+                        // exp(G_i - G_j) for column j <= this row
+                        auto mask_row = [&](auto weight) {
 #pragma unroll
                             for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
                                 const uint32_t off = sw128_offset(arow, cch * 16);
@@ -861,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     float x = j < 32 ? __uint_as_float(r[j]) : __uint_as_float(r2[j - 32]);
                                     x = (j <= arow) ? x : 0.f;
                                     if (NORM) den += x;
-                                    if (GATED && j <= arow) x *= __expf(gi - gc[j]);
+                                    if (GATED && j <= arow) x *= weight(j);
                                     v[e] = x;
                                 }
                                 if (ALO) {
@@ -872,6 +877,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 } else {
                                     *reinterpret_cast<uint4*>(ATh(tb) + off) = f_to_bf8(v);
                                 }
+                            }
+                        };
+                        if (arow_ok) {
+                            if constexpr (GATED) {
+                                // exp(G_i - G_j) = exp(G_i - ref) * exp(ref - G_j): one exp
+                                // per row and the column factors of the feature warps,
+                                // when the chunk's spread keeps both factors in range
+                                if (gc[kGFlag] != 0.f) {
+                                    const float ei = __expf(gi - gc[kGRef]);
+                                    const float* ef = gc + kGCol;
+                                    mask_row([&](int j) { return ei * ef[j]; });
+                                } else {
+                                    mask_row([&](int j) { return __expf(gi - gc[j]); });
+                                }
+                            } else {
+                                mask_row([&](int) { return 1.f; });
                             }
                         }
                     }
@@ -1028,8 +1049,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float t = __shfl_up_sync(0xffffffffu, incl, o);
                         if (lane >= o) incl += t;
                     }
-                    gc[j0] = incl - sum + g0;
-                    gc[j1] = incl;
+                    const float c0 = incl - sum + g0, c1 = incl;
+                    gc[j0] = c0;
+                    gc[j1] = c1;
+                    // factored weights for the score epilogue: a reference in the
+                    // middle of the chunk's range, usable when both factors stay
+                    // below e^80 (spread < 160)
+                    float mx = fmaxf(c0, c1), mn = fminf(c0, c1);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                    }
+                    const float ref = 0.5f * (mx + mn);
+                    const bool fac = (mx - mn) < 160.f;
+                    gc[kGCol + j0] = fac ? __expf(ref - c0) : 0.f;
+                    gc[kGCol + j1] = fac ? __expf(ref - c1) : 0.f;
+                    if (ct == 0) {
+                        gc[kGRef] = ref;
+                        gc[kGFlag] = fac ? 1.f : 0.f;
+                    }
                 }
                 if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
                 gtot = gc[kC - 1];

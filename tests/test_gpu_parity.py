@@ -39,13 +39,13 @@ def rand(shape, seed, dtype, std=1.0):
 
 
 def run_case(B, T, Hq, Hkv, Dk, Dv, dtype, out_dtype, fmap, norm, rule="linear", S0=False, seed=0,
-             scale=1.0, eps=1e-6, std=1.0):
+             scale=1.0, eps=1e-6, std=1.0, decay_mean=3.0):
     q = rand((B, T, Hq, Dk), seed, dtype, std)
     k = rand((B, T, Hkv, Dk), seed + 1, dtype, std)
     v = rand((B, T, Hkv, Dv), seed + 2, dtype)
     decay = None
     if rule == "gated":
-        x = rand((B, T, Hkv), seed + 3, torch.float32) + 3.0
+        x = rand((B, T, Hkv), seed + 3, torch.float32) + decay_mean
         decay = torch.nn.functional.logsigmoid(x).to(dtype)
     init = None
     if S0:
@@ -140,6 +140,16 @@ def test_gated_small(shape, dtype):
     B, T, Hq, Hkv, Dk, Dv = shape
     run_case(B, T, Hq, Hkv, Dk, Dv, dtype, torch.float32, "none", False, rule="gated", S0=True,
              scale=0.0, seed=7)
+
+
+@pytest.mark.parametrize("shape", [(2, 200, 4, 2, 64, 64), (1, 257, 8, 2, 128, 128)], ids=lambda s: "x".join(map(str, s)))
+def test_gated_strong_decay(shape):
+    """Log decay near -5 per token: a 64-token chunk spans several hundred in
+    cumulative decay, so the score epilogue takes exp(G_i - G_j) per element
+    instead of the factored weights."""
+    B, T, Hq, Hkv, Dk, Dv = shape
+    run_case(B, T, Hq, Hkv, Dk, Dv, torch.bfloat16, torch.float32, "none", False, rule="gated", S0=True,
+             scale=0.0, seed=11, decay_mean=-5.0)
 
 
 @pytest.mark.parametrize("shape", SHAPES[1:], ids=lambda s: "x".join(map(str, s)))
