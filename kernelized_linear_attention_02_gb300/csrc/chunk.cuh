@@ -109,6 +109,10 @@ struct Cfg {
     static constexpr int kNAT = MODE == kCausal ? 1 : 0;
     static constexpr int kAT = kNAT * 2 * 8192;  // per buffer: hi, lo (64 x 64 bf16 each)
     static constexpr int kZrApply = (MODE == kApply && NORM) ? kZr : 0;
+    // linear rule, bf16 output: each item's 64 x D output tile is staged in
+    // shared memory and leaves with 16-byte stores
+    static constexpr bool kYStage = OUT_BF16 && !GATED && MODE != kState;
+    static constexpr int kYS = kYStage ? 64 * D * 2 : 0;
     // feature-map warps: 4 (warps 10-13), or 8 in the state pass (warps 6-13),
     // which has no scores for the epilogue warps to mask
     static constexpr int kFeatWarps = MODE == kState ? 8 : 4;
@@ -122,7 +126,7 @@ struct Cfg {
     static constexpr int kZpart = kRowStep * D;  // floats of one buffer of partial Z sums
     static constexpr int kMisc = 1024 + 2 * kZpart * 4 + 512;  // 1/den ring, partial Z sums (x2), barriers
     static constexpr int bytes(int nkv, int nq) {
-        return 1024 + nkv * kKvStage + nq * kQStage + kAT + kZrApply + kMisc;
+        return 1024 + nkv * kKvStage + nq * kQStage + kAT + kZrApply + kYS + kMisc;
     }
     static constexpr int kLimit = 227 * 1024;
     // ring depths: the deepest of (4,4), (3,3), (3,2), (2,2) that shared
@@ -209,7 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* q_base = kv_base + NKV * Cf::kKvStage;
     uint8_t* at_base = q_base + NQ * Cf::kQStage;
     uint8_t* zr_apply = at_base + Cf::kAT;
-    float* misc = reinterpret_cast<float*>(zr_apply + Cf::kZrApply);
+    uint8_t* ystage = zr_apply + Cf::kZrApply;  // staged output tile (64 x D bf16)
+    float* misc = reinterpret_cast<float*>(ystage + Cf::kYS);
     float* inv_den = misc;           // [4][64] scale / den of the last four items
     float* zpart = misc + 256;       // [2][kZpart] partial column sums of phi(K)
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc + 256 + 2 * Cf::kZpart);
@@ -236,6 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* den_full = bars + 42;  // [4]
     uint64_t* inter_cmp = bars + 50;  // [2] read-out of item n complete (split issue; per Y^T buffer)
     uint64_t* upd_done = bars + 52;   // state update of a chunk complete (split issue)
+    uint64_t* out_group = bars + 55;  // barrier among the four output warps (staged output tile)
+    uint32_t ophase = 0;              // this thread's uses of out_group
 #ifdef LA_TRACE
     unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 46);
     if (threadIdx.x < 8) la_trace_ctr[threadIdx.x] = 0;
@@ -299,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(final_done, split ? 2 : 1);
         for (int i = 0; i < 2; ++i) mbar_init(&inter_cmp[i], 1);
         mbar_init(upd_done, 1);
+        mbar_init(out_group, 4);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -355,7 +363,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4* idn4 = reinterpret_cast<const float4*>(inv_den + (m & 3) * 64);
         const size_t tstride = (size_t)Hq * D;
         const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
-        if (vrow_ok) {
+        if constexpr (Cf::kYStage) {
+            // tile [token][D] in shared memory, then 16-byte stores of its valid
+            // rows by the four output warps (bounded group barrier)
+            __nv_bfloat16* ys = reinterpret_cast<__nv_bfloat16*>(ystage);
+            if (vrow_ok) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const float4 fa = NORM ? idn4[2 * g] : make_float4(scale, scale, scale, scale);
+                    const float4 fb = NORM ? idn4[2 * g + 1] : fa;
+                    const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int x = g * 8 + e;
+                        ys[x * D + vrow] = __float2bfloat16_rn(f[e] * __uint_as_float(x < 32 ? y0[x] : y1[x - 32]));
+                    }
+                }
+            }
+            if (!group_sync(out_group, ophase, err, kErrYFull)) return false;
+            const int ot = tid - kStateWarp0 * 32;  // 0..127
+            constexpr int kCpr = D / 8;            // 16-byte chunks per row
+            const uint4* ys4 = reinterpret_cast<const uint4*>(ystage);
+            __nv_bfloat16* yrow0 = reinterpret_cast<__nv_bfloat16*>(yout) + (base - vrow);
+#pragma unroll
+            for (int c = ot; c < 64 * kCpr; c += 128) {
+                const int x = c / kCpr;
+                if (x < valid)
+                    *reinterpret_cast<uint4*>(yrow0 + x * tstride + (c % kCpr) * 8) = ys4[c];
+            }
+            if (!group_sync(out_group, ophase, err, kErrYFull)) return false;  // tile free again
+        } else if (vrow_ok) {
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
                 const float4 fa = NORM ? idn4[2 * g] : make_float4(scale, scale, scale, scale);
