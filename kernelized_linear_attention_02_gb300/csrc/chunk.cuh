@@ -841,12 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < Cf::kFeatW0) {
         // -------------------------------------------------------------- epilogue
-        const int quad = warp & 3;
-        const bool m64 = D == 64;
-        const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);  // value index of this Y^T lane
-        const bool vrow_ok = m64 ? lane < 16 : true;
-        const int arow = quad * 16 + lane;  // score row (M = 64 layout: lanes 0-15 of each quadrant)
-        const bool arow_ok = lane < 16;
+        const int quad = warp & 3;  // TMEM lane quadrant of this warp
         const int n_total = Cf::kHasQ ? nck * G : 0;
         bool ok = true;
         for (int n = 0; n < n_total && ok; ++n) {
@@ -854,34 +849,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // -------- scores of item n: mask, decay, hi/lo split, 1/den
                 const int ab = n % NA;
                 const int s = (n / G) % NKV1;
-                float den = 1.f;
                 if (MODE == kCausal || NORM) {
                     ok = warp_wait(&a_full[ab], (n / NA) & 1, err, kErrAFull);
                     if (!ok) break;
                     tc_fence_after();
                     if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 1, n);
                     const uint32_t tA = tmem + Cf::kColA + 80 * ab;
-                    // every score of this row in one round trip to TMEM; the buffer
-                    // is released before the masking
-                    uint32_t r[32], r2[32], z[16];
-                    if (MODE == kCausal) {
-                        tmem_ld32(tmem_addr(tA, quad * 32, 0), r);
-                        tmem_ld32(tmem_addr(tA, quad * 32, 32), r2);
-                    }
-                    if (NORM) tmem_ld16(tmem_addr(tA, quad * 32, 64), z);
+                    // The 64 x 64 score tile (M = 64: TMEM lanes 0-15 of each quadrant)
+                    // read in the 16x256b shape, so that all 32 lanes work: this
+                    // thread holds rows r1 = 16 quad + lane/4 and r2 = r1 + 8, columns
+                    // 8g + cq and 8g + cq + 1 of each 8-column group g.  One round
+                    // trip to TMEM; the buffer is released before the masking.
+                    const int r1 = quad * 16 + (lane >> 2), r2 = r1 + 8, cq = 2 * (lane & 3);
+                    const uint32_t tq = tmem_addr(tA, quad * 32, 0);
+                    uint32_t sc[32], zz[4];
+                    if (MODE == kCausal) tmem_ld16x256b_x8(tq, sc);
+                    if (NORM) tmem_ld16x256b_x1(tq + 64, zz);  // columns 64, 65: phi(q).[Z_hi, Z_lo]
                     tmem_ld_wait();
-                    if (MODE == kCausal) {
-                        reg_fence(r);
-                        reg_fence(r2);
-                    }
-                    if (NORM) reg_fence(z);
+                    if (MODE == kCausal) reg_fence(sc);
+                    if (NORM) reg_fence(zz);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&a_empty[ab]);  // TMEM scores read out
-                    if (NORM) den = __uint_as_float(z[0]) + __uint_as_float(z[1]) + eps;
+                    float den1 = 1.f, den2 = 1.f;
+                    if (NORM) {
+                        // phi(q).Z_prev sits in the thread of column pair 0 of each row
+                        const int src = lane & ~3;
+                        den1 = __shfl_sync(0xffffffffu, __uint_as_float(zz[0]) + __uint_as_float(zz[1]), src) + eps;
+                        den2 = __shfl_sync(0xffffffffu, __uint_as_float(zz[2]) + __uint_as_float(zz[3]), src) + eps;
+                    }
                     if (MODE == kCausal) {
                         const float* gc = reinterpret_cast<const float*>(Gc(s));
-                        const float gi = (GATED && arow_ok) ? gc[arow] : 0.f;
                         const int tb = n % NAT;
                         if (n >= NAT) {
                             // the intra product that read this buffer last (item n - NAT)
@@ -890,47 +888,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!ok) break;
                             tc_fence_after();
                         }
-                        // masked row (decay-weighted for the gated rule): weight(j) is
-                        // exp(G_i - G_j) for column j <= this row
-                        auto mask_row = [&](auto weight) {
+                        // masked rows (decay-weighted for the gated rule: w1(j), w2(j)
+                        // are exp(G_i - G_j) for rows r1, r2), bf16 hi [+ lo] pairs into
+                        // the swizzled A^T tile, and the row sums for the normalizer
+                        auto mask_rows = [&](auto w1, auto w2) {
+                            float p1 = 0.f, p2 = 0.f;
 #pragma unroll
-                            for (int cch = 0; cch < 8; ++cch) {  // 8 columns per 16-byte chunk
-                                const uint32_t off = sw128_offset(arow, cch * 16);
-                                float v[8];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const int j = cch * 8 + e;
-                                    float x = j < 32 ? __uint_as_float(r[j]) : __uint_as_float(r2[j - 32]);
-                                    x = (j <= arow) ? x : 0.f;
-                                    if (NORM) den += x;
-                                    if (GATED && j <= arow) x *= weight(j);
-                                    v[e] = x;
+                            for (int g = 0; g < 8; ++g) {
+                                const int j = 8 * g + cq;
+                                float a0 = j <= r1 ? __uint_as_float(sc[4 * g]) : 0.f;
+                                float a1 = j + 1 <= r1 ? __uint_as_float(sc[4 * g + 1]) : 0.f;
+                                float b0 = j <= r2 ? __uint_as_float(sc[4 * g + 2]) : 0.f;
+                                float b1 = j + 1 <= r2 ? __uint_as_float(sc[4 * g + 3]) : 0.f;
+                                if (NORM) {
+                                    p1 += a0 + a1;
+                                    p2 += b0 + b1;
                                 }
+                                if (GATED) {
+                                    if (j <= r1) a0 *= w1(j);
+                                    if (j + 1 <= r1) a1 *= w1(j + 1);
+                                    if (j <= r2) b0 *= w2(j);
+                                    if (j + 1 <= r2) b1 *= w2(j + 1);
+                                }
+                                const uint32_t o1 = (uint32_t)(r1 * 128 + ((g ^ (r1 & 7)) << 4) + 2 * cq);
+                                const uint32_t o2 = (uint32_t)(r2 * 128 + ((g ^ (r2 & 7)) << 4) + 2 * cq);
                                 if (ALO) {
-                                    uint4 hv, lv;
-                                    split8(v, hv, lv);
-                                    *reinterpret_cast<uint4*>(ATh(tb) + off) = hv;
-                                    *reinterpret_cast<uint4*>(ATl(tb) + off) = lv;
+                                    uint32_t h1, l1, h2, l2;
+                                    split2(a0, a1, h1, l1);
+                                    split2(b0, b1, h2, l2);
+                                    *reinterpret_cast<uint32_t*>(ATh(tb) + o1) = h1;
+                                    *reinterpret_cast<uint32_t*>(ATl(tb) + o1) = l1;
+                                    *reinterpret_cast<uint32_t*>(ATh(tb) + o2) = h2;
+                                    *reinterpret_cast<uint32_t*>(ATl(tb) + o2) = l2;
                                 } else {
-                                    *reinterpret_cast<uint4*>(ATh(tb) + off) = f_to_bf8(v);
+                                    *reinterpret_cast<uint32_t*>(ATh(tb) + o1) = bf2_bits(__floats2bfloat162_rn(a0, a1));
+                                    *reinterpret_cast<uint32_t*>(ATh(tb) + o2) = bf2_bits(__floats2bfloat162_rn(b0, b1));
                                 }
+                            }
+                            if (NORM) {  // row sums over the four threads of a row
+                                p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+                                p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+                                p2 += __shfl_xor_sync(0xffffffffu, p2, 1);
+                                p2 += __shfl_xor_sync(0xffffffffu, p2, 2);
+                                den1 += p1;
+                                den2 += p2;
                             }
                         };
-                        if (arow_ok) {
-                            if constexpr (GATED) {
+                        if constexpr (GATED) {
+                            const float g1 = gc[r1], g2 = gc[r2];
+                            if (gc[kGFlag] != 0.f) {
                                 // exp(G_i - G_j) = exp(G_i - ref) * exp(ref - G_j): one exp
-                                // per row and the column factors of the feature warps,
-                                // when the chunk's spread keeps both factors in range
-                                if (gc[kGFlag] != 0.f) {
-                                    const float ei = __expf(gi - gc[kGRef]);
-                                    const float* ef = gc + kGCol;
-                                    mask_row([&](int j) { return ei * ef[j]; });
-                                } else {
-                                    mask_row([&](int j) { return __expf(gi - gc[j]); });
-                                }
+                                // per row and the column factors of the feature warps
+                                const float e1 = __expf(g1 - gc[kGRef]), e2 = __expf(g2 - gc[kGRef]);
+                                const float* ef = gc + kGCol;
+                                mask_rows([&](int j) { return e1 * ef[j]; }, [&](int j) { return e2 * ef[j]; });
                             } else {
-                                mask_row([&](int) { return 1.f; });
+                                mask_rows([&](int j) { return __expf(g1 - gc[j]); },
+                                          [&](int j) { return __expf(g2 - gc[j]); });
                             }
+                        } else {
+                            mask_rows([](int) { return 1.f; }, [](int) { return 1.f; });
                         }
                     }
                     if (MODE == kCausal) {
@@ -939,13 +956,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0) mbar_arrive(&at_full[n % NAT]);
                         if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 2, n);
                     }
-                }
-                if (NORM) {
-                    // hand scale/den to the output stage (without the normalizer
-                    // the factor is the constant scale and needs no hand-off)
-                    if (arow_ok) inv_den[(n & 3) * 64 + arow] = scale / den;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&den_full[n & 3]);
+                    if (NORM) {
+                        // hand scale/den to the output stage (without the normalizer
+                        // the factor is the constant scale and needs no hand-off)
+                        if ((lane & 3) == 0) {
+                            inv_den[(n & 3) * 64 + r1] = scale / den1;
+                            inv_den[(n & 3) * 64 + r2] = scale / den2;
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&den_full[n & 3]);
+                    }
                 }
             }
         }

@@ -336,6 +336,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         LA_W8(0), LA_W8(8), LA_W8(16), LA_W8(24)
         : "memory");
 }
+// 16x256b shape: a warp reads 16 TMEM lanes (from the lane of the address)
+// in groups of 8 columns; thread t holds lanes t/4 and t/4 + 8 at columns
+// 2(t%4) and 2(t%4) + 1 of each group, registers 4g .. 4g+3 of group g in
+// the order (t/4, c), (t/4, c+1), (t/4+8, c), (t/4+8, c+1).
+__device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : LA_R8(0), LA_R8(8), LA_R8(16), LA_R8(24)
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16x256b_x1(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
 #undef LA_R8
 #undef LA_W8
 
