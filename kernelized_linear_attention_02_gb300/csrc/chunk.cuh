@@ -112,7 +112,8 @@ struct Cfg {
     // linear rule, bf16 output: each item's 64 x D output tile is staged in
     // shared memory and leaves with 16-byte stores
     static constexpr bool kYStage = OUT_BF16 && !GATED && MODE != kState;
-    static constexpr int kYS = kYStage ? 64 * D * 2 : 0;
+    static constexpr int kYPitch = D + 8;  // tile row pitch in elements (16 bytes of padding)
+    static constexpr int kYS = kYStage ? 64 * kYPitch * 2 : 0;
     // feature-map warps: 4 (warps 10-13), or 8 in the state pass (warps 6-13),
     // which has no scores for the epilogue warps to mask
     static constexpr int kFeatWarps = MODE == kState ? 8 : 4;
@@ -347,13 +348,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (quad == 0 && lane == 0) LA_TR(4, 3, m);
         // all 64 tokens of this lane in one round trip to TMEM; the buffer is
-        // released before the stores
+        // released before the stores.  Head size 64 with a staged tile: Y^T is
+        // an M = 64 tile (lanes 0-15 of each quadrant), read in the 16x256b
+        // shape so that all 32 lanes work (y0 then holds value rows
+        // 16 quad + lane/4 and + 8, tokens 8g + 2(lane%4) and + 1).
+        constexpr bool kHalfLanes = Cf::kYStage && D == 64;
         uint32_t y0[32], y1[32];
-        tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 0), y0);
-        tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 32), y1);
+        if constexpr (kHalfLanes) {
+            tmem_ld16x256b_x8(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 0), y0);
+        } else {
+            tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 0), y0);
+            tmem_ld32(tmem_addr(tmem + Cf::kColY + 64 * yb, quad * 32, 32), y1);
+        }
         tmem_ld_wait();
         reg_fence(y0);
-        reg_fence(y1);
+        if constexpr (!kHalfLanes) reg_fence(y1);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&y_empty[yb]);
@@ -367,7 +376,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tile [token][D] in shared memory, then 16-byte stores of its valid
             // rows by the four output warps (bounded group barrier)
             __nv_bfloat16* ys = reinterpret_cast<__nv_bfloat16*>(ystage);
-            if (vrow_ok) {
+            constexpr int P = Cf::kYPitch;
+            if constexpr (kHalfLanes) {
+                const int v1 = quad * 16 + (lane >> 2), v2 = v1 + 8, cq = 2 * (lane & 3);
+                const float* idn = inv_den + (m & 3) * 64;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const int x = 8 * g + cq;
+                    const float2 f = NORM ? *reinterpret_cast<const float2*>(idn + x) : make_float2(scale, scale);
+                    ys[x * P + v1] = __float2bfloat16_rn(f.x * __uint_as_float(y0[4 * g]));
+                    ys[(x + 1) * P + v1] = __float2bfloat16_rn(f.y * __uint_as_float(y0[4 * g + 1]));
+                    ys[x * P + v2] = __float2bfloat16_rn(f.x * __uint_as_float(y0[4 * g + 2]));
+                    ys[(x + 1) * P + v2] = __float2bfloat16_rn(f.y * __uint_as_float(y0[4 * g + 3]));
+                }
+            } else if (vrow_ok) {
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                     const float4 fa = NORM ? idn4[2 * g] : make_float4(scale, scale, scale, scale);
@@ -376,20 +398,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int x = g * 8 + e;
-                        ys[x * D + vrow] = __float2bfloat16_rn(f[e] * __uint_as_float(x < 32 ? y0[x] : y1[x - 32]));
+                        ys[x * P + vrow] = __float2bfloat16_rn(f[e] * __uint_as_float(x < 32 ? y0[x] : y1[x - 32]));
                     }
                 }
             }
             if (!group_sync(out_group, ophase, err, kErrYFull)) return false;
             const int ot = tid - kStateWarp0 * 32;  // 0..127
             constexpr int kCpr = D / 8;            // 16-byte chunks per row
-            const uint4* ys4 = reinterpret_cast<const uint4*>(ystage);
             __nv_bfloat16* yrow0 = reinterpret_cast<__nv_bfloat16*>(yout) + (base - vrow);
 #pragma unroll
             for (int c = ot; c < 64 * kCpr; c += 128) {
-                const int x = c / kCpr;
+                const int x = c / kCpr, cc = c - x * kCpr;
                 if (x < valid)
-                    *reinterpret_cast<uint4*>(yrow0 + x * tstride + (c % kCpr) * 8) = ys4[c];
+                    *reinterpret_cast<uint4*>(yrow0 + x * tstride + cc * 8) =
+                        *reinterpret_cast<const uint4*>(ys + x * P + cc * 8);
             }
             if (!group_sync(out_group, ophase, err, kErrYFull)) return false;  // tile free again
         } else if (vrow_ok) {
