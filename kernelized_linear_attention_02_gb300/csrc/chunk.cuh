@@ -1191,33 +1191,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ct == 0) LA_TR(2, 8, i);
                 if (NORM) {
-                    // Z rows of this chunk hold Z_prev (hi, lo); then Z += column sums
+                    // partial column sums of this chunk, reduced after the tile is released
                     float* zp = zpart + zbuf * Cf::kZpart;
                     *reinterpret_cast<float4*>(zp + rbase * D + 8 * cc) =
                         make_float4(colsum[0], colsum[1], colsum[2], colsum[3]);
                     *reinterpret_cast<float4*>(zp + rbase * D + 8 * cc + 4) =
                         make_float4(colsum[4], colsum[5], colsum[6], colsum[7]);
-                    if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
-                    if (ct == 0) LA_TR(2, 9, i);
-                    if (ct < D) {
+                    // Z rows of this chunk hold Z_prev (hi, lo): known before its sums
+                    if (MODE != kState && ct < D) {
                         if (MODE == kCausal && i == 0) start_z();
-                        if (MODE != kState) {
-                            const __nv_bfloat16 h = __float2bfloat16_rn(zreg);
-                            zr_elem(s, 0, ct) = h;
-                            zr_elem(s, 1, ct) = __float2bfloat16_rn(zreg - __bfloat162float(h));
-                        }
-                        float add = 0.f;
-#pragma unroll
-                        for (int g = 0; g < kRowStep; ++g) add += zp[g * D + ct];
-                        zreg += add;
+                        const __nv_bfloat16 h = __float2bfloat16_rn(zreg);
+                        zr_elem(s, 0, ct) = h;
+                        zr_elem(s, 1, ct) = __float2bfloat16_rn(zreg - __bfloat162float(h));
                     }
-                    zbuf ^= 1;
                 }
             }
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&conv_kv[s]);
+            if (lane == 0) mbar_arrive(&conv_kv[s]);  // the tile goes to the tensor core
             if (ct == 0) LA_TR(2, 2, i);
+            if (touch && NORM) {
+                // Z += this chunk's column sums, off the path to the tensor core
+                const float* zp = zpart + zbuf * Cf::kZpart;
+                if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
+                if (ct == 0) LA_TR(2, 9, i);
+                if (ct < D) {
+                    float add = 0.f;
+#pragma unroll
+                    for (int g = 0; g < kRowStep; ++g) add += zp[g * D + ct];
+                    zreg += add;
+                }
+                zbuf ^= 1;
+            }
             return true;
         };
 
