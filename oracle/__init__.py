@@ -73,6 +73,11 @@ def load(path: str = _LIB_PATH):
         lib.orc_causal.restype = ctypes.c_int
         lib.orc_noncausal.argtypes = [ctypes.POINTER(_Params)] + [dp] * 4
         lib.orc_noncausal.restype = ctypes.c_int
+        bp = ctypes.c_void_p
+        lib.orc_causal_masked.argtypes = [ctypes.POINTER(_Params)] + [dp] * 5 + [bp] + [dp] * 5
+        lib.orc_causal_masked.restype = ctypes.c_int
+        lib.orc_noncausal_masked.argtypes = [ctypes.POINTER(_Params)] + [dp] * 3 + [bp, dp]
+        lib.orc_noncausal_masked.restype = ctypes.c_int
         _lib_cache[path] = lib
         return lib
 
@@ -89,6 +94,20 @@ def _ptr(a):
     if a is None:
         return ctypes.POINTER(ctypes.c_double)()
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _mask(mask, B, T):
+    """(B, T) validity mask as a contiguous uint8 array (nonzero = valid), or None."""
+    if mask is None:
+        return None
+    if hasattr(mask, "detach"):
+        mask = mask.detach().cpu().numpy()
+    m = np.ascontiguousarray(np.asarray(mask).reshape(B, T) != 0, dtype=np.uint8)
+    return m
+
+
+def _mptr(m):
+    return None if m is None else ctypes.c_void_p(m.ctypes.data)
 
 
 def resolve_scale(scale: float, dk: int) -> float:
@@ -117,32 +136,39 @@ def _params(q, k, v, q_heads, kv_heads, feature_map, use_normalizer, eps, scale,
 
 def causal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one", use_normalizer=True,
            eps=1e-6, scale=1.0, rule="linear", decay=None, beta=None, S0=None, Z0=None,
-           nthreads=None, lib=None):
+           mask=None, nthreads=None, lib=None):
     """Causal pass.  q (B,T,Hq*Dk) or (B,T,Hq,Dk); k (B,T,Hkv[*]Dk); v (B,T,Hkv[*]Dv).
 
     Returns (y (B,T,Hq,Dv), S (B,Hkv,Dk,Dv), Z (B,Hkv,Dk)) in float64.
-    ``scale`` follows the ONNX attribute: 0.0 means 1/sqrt(d_k)."""
+    ``scale`` follows the ONNX attribute: 0.0 means 1/sqrt(d_k).  ``mask``
+    (B,T) is the Keras sequence-validity mask: an invalid step keeps the
+    state and outputs zero."""
     q, k, v, decay, beta, S0, Z0 = map(_f64, (q, k, v, decay, beta, S0, Z0))
     p, B, T, Dk, Dv = _params(q, k, v, q_heads, kv_heads, feature_map, use_normalizer, eps,
                               scale, rule, decay, beta, nthreads)
     y = np.zeros((B, T, q_heads, Dv))
     S = np.zeros((B, kv_heads, Dk, Dv))
     Z = np.zeros((B, kv_heads, Dk))
-    rc = (lib or load()).orc_causal(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay),
-                                    _ptr(beta), _ptr(S0), _ptr(Z0), _ptr(y), _ptr(S), _ptr(Z))
+    m = _mask(mask, B, T)
+    rc = (lib or load()).orc_causal_masked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay),
+                                           _ptr(beta), _mptr(m), _ptr(S0), _ptr(Z0), _ptr(y), _ptr(S),
+                                           _ptr(Z))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return y, S, Z
 
 
 def noncausal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one", use_normalizer=True,
-              eps=1e-6, scale=1.0, nthreads=None, lib=None):
-    """Non-causal pass with the global state.  Returns y (B,T,Hq,Dv) in float64."""
+              eps=1e-6, scale=1.0, mask=None, nthreads=None, lib=None):
+    """Non-causal pass with the global state.  Returns y (B,T,Hq,Dv) in float64.
+    ``mask`` (B,T): invalid keys/values leave the sums, invalid queries give 0."""
     q, k, v = map(_f64, (q, k, v))
     p, B, T, Dk, Dv = _params(q, k, v, q_heads, kv_heads, feature_map, use_normalizer, eps,
                               scale, "linear", None, None, nthreads)
     y = np.zeros((B, T, q_heads, Dv))
-    rc = (lib or load()).orc_noncausal(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(y))
+    m = _mask(mask, B, T)
+    rc = (lib or load()).orc_noncausal_masked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _mptr(m),
+                                              _ptr(y))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return y

@@ -21,6 +21,10 @@
  *    head sharing, update rules linear / gated / delta / gated_delta, scale,
  *    decay layouts (B,T,H_kv) and (B,T,H_kv*d_k), beta layouts (B,T,H_kv)
  *    and (B,T,1).
+ *  - Same Keras request, section "Masking": a (batch, sequence) validity
+ *    mask.  Causal: an invalid step leaves S and Z as they were and its
+ *    output is zero.  Non-causal: invalid keys/values add nothing to the
+ *    global sums and invalid query positions give zero output.
  *
  * Parity pins: see tests/test_oracle.py (worked examples of the ONNX page,
  * the 0.2188 figure of "Causal Linear Attention", the O(T^2) brute force,
@@ -65,6 +69,7 @@ static double orc_phi(int fmap, double x, double eps)
 typedef struct {
     const orc_params* p;
     const double *q, *k, *v, *decay, *beta, *S0, *Z0;
+    const unsigned char* mask; /* (B,T), nonzero = valid; NULL = all valid */
     double *y, *S_out, *Z_out;
     int causal;
     int64_t next;          /* shared work counter over (b, kv-head) */
@@ -76,7 +81,11 @@ typedef struct {
  * update rules of the ONNX page, token by token: first the state update,
  * then the read-out for every query head that shares this kv head.
  * Non-causal: the global sums S = sum_j phi(K_j)^T V_j, Z = sum_j phi(K_j),
- * then Y_i = phi(Q_i) S / (phi(Q_i) Z + eps). */
+ * then Y_i = phi(Q_i) S / (phi(Q_i) Z + eps).
+ * Masking (Keras request, "Masking"): an invalid causal step is skipped, so
+ * S_t = S_{t-1}, Z_t = Z_{t-1} and Y_t = 0 (the where(mask_t, candidate,
+ * previous) selection, with the candidate never formed); non-causal, an
+ * invalid position is left out of the sums and its output is zero. */
 static void orc_stream(orc_job* J, int64_t b, int32_t hk, double* S, double* Z,
                        double* fk, double* fq, double* u)
 {
@@ -94,6 +103,7 @@ static void orc_stream(orc_job* J, int64_t b, int32_t hk, double* S, double* Z,
     if (!J->causal) {
         /* global state over all positions */
         for (int64_t t = 0; t < T; ++t) {
+            if (J->mask && !J->mask[b * T + t]) continue; /* invalid key/value */
             const double* kt = J->k + ((size_t)(b * T + t) * Hkv + hk) * Dk;
             const double* vt = J->v + ((size_t)(b * T + t) * Hkv + hk) * Dv;
             for (int32_t i = 0; i < Dk; ++i) fk[i] = orc_phi(p->feature_map, kt[i], p->eps);
@@ -106,6 +116,14 @@ static void orc_stream(orc_job* J, int64_t b, int32_t hk, double* S, double* Z,
 
     for (int64_t t = 0; t < T; ++t) {
         const size_t tok = (size_t)(b * T + t);
+        if (J->mask && !J->mask[tok]) {
+            /* invalid step: state kept, zero output for every head of the group */
+            for (int32_t r = 0; r < G; ++r) {
+                double* yt = J->y + (tok * Hq + hk * G + r) * Dv;
+                for (int32_t j = 0; j < Dv; ++j) yt[j] = 0.0;
+            }
+            continue;
+        }
         if (J->causal) {
             const double* kt = J->k + (tok * Hkv + hk) * Dk;
             const double* vt = J->v + (tok * Hkv + hk) * Dv;
@@ -224,25 +242,40 @@ static int orc_run(orc_job* J)
  *   q (B,T,Hq,Dk)  k (B,T,Hkv,Dk)  v (B,T,Hkv,Dv)  y (B,T,Hq,Dv)
  *   S (B,Hkv,Dk,Dv)  Z (B,Hkv,Dk)
  *   decay (B,T,Hkv) or (B,T,Hkv,Dk); beta (B,T,Hkv) or (B,T,1).
+ *   mask (B,T) validity, nonzero = valid; NULL (orc_causal) = all valid.
  * Returns 0 on success, 1 on an argument error. */
-int orc_causal(const orc_params* p, const double* q, const double* k, const double* v,
-               const double* decay, const double* beta, const double* S0, const double* Z0,
-               double* y, double* S_out, double* Z_out)
+int orc_causal_masked(const orc_params* p, const double* q, const double* k, const double* v,
+                      const double* decay, const double* beta, const unsigned char* mask,
+                      const double* S0, const double* Z0, double* y, double* S_out, double* Z_out)
 {
     if (orc_check(p, 1, decay, beta)) return 1;
     orc_job J;
     memset(&J, 0, sizeof(J));
-    J.p = p; J.q = q; J.k = k; J.v = v; J.decay = decay; J.beta = beta;
+    J.p = p; J.q = q; J.k = k; J.v = v; J.decay = decay; J.beta = beta; J.mask = mask;
     J.S0 = S0; J.Z0 = Z0; J.y = y; J.S_out = S_out; J.Z_out = Z_out; J.causal = 1;
     return orc_run(&J);
 }
 
-/* Non-causal pass: global state over all T positions, no state in or out. */
-int orc_noncausal(const orc_params* p, const double* q, const double* k, const double* v, double* y)
+int orc_causal(const orc_params* p, const double* q, const double* k, const double* v,
+               const double* decay, const double* beta, const double* S0, const double* Z0,
+               double* y, double* S_out, double* Z_out)
+{
+    return orc_causal_masked(p, q, k, v, decay, beta, NULL, S0, Z0, y, S_out, Z_out);
+}
+
+/* Non-causal pass: global state over all (valid) positions, no state in or
+ * out.  mask (B,T) as for orc_causal_masked, NULL = all valid. */
+int orc_noncausal_masked(const orc_params* p, const double* q, const double* k, const double* v,
+                         const unsigned char* mask, double* y)
 {
     if (orc_check(p, 0, NULL, NULL)) return 1;
     orc_job J;
     memset(&J, 0, sizeof(J));
-    J.p = p; J.q = q; J.k = k; J.v = v; J.y = y; J.causal = 0;
+    J.p = p; J.q = q; J.k = k; J.v = v; J.mask = mask; J.y = y; J.causal = 0;
     return orc_run(&J);
+}
+
+int orc_noncausal(const orc_params* p, const double* q, const double* k, const double* v, double* y)
+{
+    return orc_noncausal_masked(p, q, k, v, NULL, y);
 }

@@ -257,10 +257,92 @@ def pin_scale(lib=None, seed=8):
     np.testing.assert_allclose(y0, y1 / 3.0, rtol=1e-13, atol=1e-13)
 
 
+def _masks(rng, B, T):
+    """Validity masks of the shapes the Keras request's tests name (Mask and
+    state behavior): right padding, left padding, interior gaps, all false,
+    all true, and random validity."""
+    out = []
+    m = np.ones((B, T), bool); m[0, T - 5:] = False; m[1, T // 2:] = False; out.append(m)
+    m = np.ones((B, T), bool); m[0, :3] = False; m[1, :T - 4] = False; out.append(m)
+    m = np.ones((B, T), bool); m[0, 4:9] = False; m[1, 1::3] = False; out.append(m)
+    out.append(np.zeros((B, T), bool))
+    out.append(np.ones((B, T), bool))
+    out.append(rng.random((B, T)) < 0.6)
+    return out
+
+
+def pin_mask_causal(lib=None, seed=9):
+    """Keras request, Masking (causal): an invalid step leaves (S, Z) as they
+    were and outputs zero.  So the outputs at the valid steps equal the O(T^2)
+    brute force run on the valid tokens alone (with their decays, for the
+    gated rule), invalid outputs are exactly 0, and the returned state is the
+    closed form S0 + sum over valid t of phi(k_t)^T v_t (linear) with Z
+    likewise; for the gated rule the state equals an unmasked pass over the
+    valid tokens alone."""
+    rng = np.random.default_rng(seed)
+    B, T, Hq, Hkv, Dk, Dv = 2, 19, 4, 2, 5, 3
+    cases = [dict(feature_map="elu_plus_one", use_normalizer=True, rule="linear"),
+             dict(feature_map="relu", use_normalizer=False, rule="linear"),
+             dict(feature_map="none", use_normalizer=False, rule="gated")]
+    for c in cases:
+        for mask in _masks(rng, B, T):
+            q = _rand(rng, B, T, Hq, Dk, std=0.7)
+            k = _rand(rng, B, T, Hkv, Dk, std=0.7)
+            v = _rand(rng, B, T, Hkv, Dv)
+            S0 = _rand(rng, B, Hkv, Dk, Dv)
+            Z0 = np.abs(_rand(rng, B, Hkv, Dk)) + 0.5 if c["use_normalizer"] else None
+            decay = np.log(1 / (1 + np.exp(-_rand(rng, B, T, Hkv) - 2.0))) if c["rule"] == "gated" else None
+            kw = dict(feature_map=c["feature_map"], use_normalizer=c["use_normalizer"], eps=1e-3, scale=0.75)
+            y, S, Z = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, rule=c["rule"], decay=decay, S0=S0,
+                                    Z0=Z0, mask=mask, lib=lib, **kw)
+            for b in range(B):
+                idx = np.nonzero(mask[b])[0]
+                assert np.all(y[b, ~mask[b]] == 0.0), str(c)
+                if idx.size:
+                    sl = lambda x: None if x is None else x[b:b + 1, idx]
+                    yb = bf.attention_bthd(sl(q), sl(k), sl(v), q_heads=Hq, kv_heads=Hkv, causal=True,
+                                           decay=sl(decay), S0=S0[b:b + 1],
+                                           Z0=None if Z0 is None else Z0[b:b + 1], **kw)
+                    np.testing.assert_allclose(y[b, idx], yb[0], rtol=1e-10, atol=1e-10, err_msg=str(c))
+                fk = bf.phi(k[b, idx], c["feature_map"], 1e-3)  # (n, Hkv, Dk)
+                if c["rule"] == "linear":
+                    S_ref = S0[b] + np.einsum("thi,thj->hij", fk, v[b, idx])
+                    np.testing.assert_allclose(S[b], S_ref, rtol=1e-11, atol=1e-11, err_msg=str(c))
+                    if c["use_normalizer"]:
+                        np.testing.assert_allclose(Z[b], Z0[b] + fk.sum(axis=0), rtol=1e-11, atol=1e-11)
+                else:
+                    _, Sc, _ = oracle.causal(q[b:b + 1, idx], k[b:b + 1, idx], v[b:b + 1, idx], q_heads=Hq,
+                                             kv_heads=Hkv, rule="gated", decay=decay[b:b + 1, idx],
+                                             S0=S0[b:b + 1], lib=lib, **kw)
+                    np.testing.assert_allclose(S[b], Sc[0], rtol=1e-11, atol=1e-11, err_msg=str(c))
+
+
+def pin_mask_noncausal(lib=None, seed=10):
+    """Keras request, Masking (non-causal): invalid keys and values add nothing
+    to the global sums and invalid query positions output zero, so the valid
+    outputs equal the brute force over the valid positions alone."""
+    rng = np.random.default_rng(seed)
+    B, T, Hq, Hkv, Dk, Dv = 2, 17, 4, 2, 4, 6
+    for fmap, norm in (("elu_plus_one", True), ("relu", False)):
+        for mask in _masks(rng, B, T):
+            q = _rand(rng, B, T, Hq, Dk)
+            k = _rand(rng, B, T, Hkv, Dk)
+            v = _rand(rng, B, T, Hkv, Dv)
+            kw = dict(feature_map=fmap, use_normalizer=norm, eps=1e-3, scale=1.25)
+            y = oracle.noncausal(q, k, v, q_heads=Hq, kv_heads=Hkv, mask=mask, lib=lib, **kw)
+            for b in range(B):
+                idx = np.nonzero(mask[b])[0]
+                assert np.all(y[b, ~mask[b]] == 0.0)
+                if idx.size:
+                    yb = bf.attention_bthd(q[b:b + 1, idx], k[b:b + 1, idx], v[b:b + 1, idx], q_heads=Hq,
+                                           kv_heads=Hkv, causal=False, **kw)
+                    np.testing.assert_allclose(y[b, idx], yb[0], rtol=1e-10, atol=1e-10)
+
+
 ALL_PINS = [pin_paper_mean_abs_diff, pin_recurrence_vs_bruteforce, pin_noncausal_vs_bruteforce,
             pin_last_row_equals_noncausal, pin_chunked_equals_full, pin_state_closed_form,
             pin_first_token, pin_feature_map_values, pin_constant_value, pin_gated_reductions,
-            pin_gqa_equals_repeated_mha, pin_scale]
+            pin_gqa_equals_repeated_mha, pin_scale, pin_mask_causal, pin_mask_noncausal]
 
 
 def run_all(lib=None):

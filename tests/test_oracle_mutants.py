@@ -33,6 +33,11 @@ MUTANTS = [
      "for (int32_t i = 0; i < Dk; ++i) Z[i] += fk[i];\n        }",
      "for (int32_t i = 0; i < Dk; ++i) Z[i] += 0.0 * fk[i];\n        }", 1),
     ("final state not written", "if (J->S_out) memcpy(", "if (0) memcpy(", 1),
+    ("masked causal step still updates the state",
+     "            continue;\n        }\n        if (J->causal) {", "        }\n        if (J->causal) {", 1),
+    ("masked keys kept in the non-causal sums",
+     "if (J->mask && !J->mask[b * T + t]) continue; /* invalid key/value */", "", 1),
+    ("mask read at the wrong batch row", "if (J->mask && !J->mask[tok]) {", "if (J->mask && !J->mask[t]) {", 1),
 ]
 
 
