@@ -151,7 +151,8 @@ def prefill_alg_bytes(w, T=None):
     qy = w.B * T * w.q_heads * (w.Dk + w.Dv) * esz
     kv = w.B * T * w.kv_heads * (w.Dk + w.Dv) * esz
     dec = w.B * T * w.kv_heads * esz if w.rule == "gated" else 0
-    return qy + kv + dec
+    msk = w.B * T if w.mask else 0  # one validity byte per (batch, step)
+    return qy + kv + dec + msk
 
 
 def decode_alg_bytes(w):
@@ -311,7 +312,8 @@ def time_workload(la, w, steps, warmup, stream, causal=True):
     for s in range(nsets):
         q, k, v, d = inputs.make_qkv(w, device="cuda", seed=w.seed + s)
         y = torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype, device="cuda")
-        sets.append((q, k, v, d, y))
+        m = inputs.validity_mask(w.mask, w.B, w.T, w.seed + s, "cuda") if w.mask else None
+        sets.append((q, k, v, d, y, m))
     kw = prefill_kwargs(w)
     if not causal:
         kw.pop("update_rule")
@@ -321,11 +323,11 @@ def time_workload(la, w, steps, warmup, stream, causal=True):
     ws = torch.empty(max(1, la.la_workspace_bytes(p, causal)), dtype=torch.uint8, device="cuda")
 
     def step(i):
-        q, k, v, d, y = sets[i % nsets]
+        q, k, v, d, y, m = sets[i % nsets]
         if causal:
-            la.la_forward_causal(q, k, v, decay=d, out=y, workspace=ws, stream=stream, **kw)
+            la.la_forward_causal(q, k, v, decay=d, out=y, workspace=ws, mask=m, stream=stream, **kw)
         else:
-            la.la_forward_noncausal(q, k, v, out=y, workspace=ws, stream=stream, **kw)
+            la.la_forward_noncausal(q, k, v, out=y, workspace=ws, mask=m, stream=stream, **kw)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -349,11 +351,12 @@ def time_workload(la, w, steps, warmup, stream, causal=True):
 def workload_sweep(la, steps, warmup, stream, hbm_gbs):
     """Every prefill workload of the library (causal and non-causal), each
     with its HBM roofline fraction.  Algorithmic bytes: q, k, v (+ decay)
-    read once and y written once."""
+    read once and y written once (plus one mask byte per step for the
+    masked workload, whose tokens/s counts padded steps too)."""
     out = []
     cases = [(inputs.PREFILL_2K, True), (inputs.LONG_8K, True), (inputs.LONG_8K_UNNORM, True),
              (inputs.LONG_8K, False), (inputs.LONG_8K_UNNORM, False), (inputs.ONNX_LINEAR, True),
-             (inputs.ONNX_GATED, True)]
+             (inputs.ONNX_GATED, True), (inputs.PREFILL_2K_RIGHTPAD, True)]
     for w, causal in cases:
         ms, lpc = time_workload(la, w, steps, warmup, stream, causal)
         alg = prefill_alg_bytes(w)

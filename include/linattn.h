@@ -14,6 +14,9 @@
  *   same page, Streaming State: key_value_state S (B, H, Dk, Dv) and
  *     key_state Z (B, H, Dk), kept in the accumulator dtype (float32); chunked
  *     calls that carry the state equal one full-sequence call.
+ *   same page, Masking: a (batch, sequence) validity mask.  Causal: an
+ *     invalid step leaves S and Z unchanged and outputs zero.  Non-causal:
+ *     invalid keys/values leave the sums and invalid queries output zero.
  *   ONNX-light "LinearAttention" operator: packed [B, T, H*D] activations,
  *     grouped KV heads (query head h reads kv head h / (Hq/Hkv)), update rules
  *       linear  S_t = S_{t-1} + k_t (x) v_t
@@ -49,7 +52,7 @@
 extern "C" {
 #endif
 
-#define LINATTN_ABI_VERSION 1
+#define LINATTN_ABI_VERSION 2
 
 typedef enum la_status {
     LA_OK = 0,
@@ -121,6 +124,20 @@ la_status la_forward_causal(const la_params* p, const void* q, const void* k, co
                             float* S_out, float* Z_out, void* ws, size_t ws_bytes,
                             la_stream_t stream);
 
+/* la_forward_causal with a sequence-validity mask (Keras request, Masking):
+ *   mask  (B, T) uint8 DEVICE array, nonzero = valid step, row-major; NULL
+ *         means every step is valid (the call is then la_forward_causal).
+ * An invalid step t of sequence b leaves that sequence's S and Z exactly as
+ * they were -- no update and, for the gated rule, no decay -- and its
+ * outputs y[b, t, :, :] are zero; later valid steps read the state as the
+ * earlier valid steps left it.  Padding (left, right) and interior gaps are
+ * all allowed.  Arguments, errors and numerics otherwise as
+ * la_forward_causal; masked-out q, k, v values are never used. */
+la_status la_forward_causal_masked(const la_params* p, const void* q, const void* k, const void* v,
+                                   const void* decay, const uint8_t* mask, const float* S0, const float* Z0,
+                                   void* y, float* S_out, float* Z_out, void* ws, size_t ws_bytes,
+                                   la_stream_t stream);
+
 /* Size of the scratch built into the library for la_forward_causal_noalloc:
  * 16 MiB of device memory, reserved once per device when the library's
  * device code is loaded there. */
@@ -161,6 +178,14 @@ la_status la_forward_causal_noalloc(const la_params* p, const void* q, const voi
 la_status la_forward_noncausal(const la_params* p, const void* q, const void* k, const void* v,
                                void* y, void* ws, size_t ws_bytes, la_stream_t stream);
 
+/* la_forward_noncausal with a sequence-validity mask (Keras request,
+ * Masking, non-causal): mask (B, T) uint8 device array as for
+ * la_forward_causal_masked (NULL = all valid).  Invalid positions add
+ * nothing to the global S and Z, and their outputs are zero. */
+la_status la_forward_noncausal_masked(const la_params* p, const void* q, const void* k, const void* v,
+                                      const uint8_t* mask, void* y, void* ws, size_t ws_bytes,
+                                      la_stream_t stream);
+
 /* One streaming token per sequence (seq_len must be 1): the recurrent update
  * and read-out ("Causal Linear Attention": S_i = S_{i-1} + phi(k_i) v_i^T,
  * then the read-out with S_i; ONNX LinearAttention decode, T = 1).
@@ -169,6 +194,14 @@ la_status la_forward_noncausal(const la_params* p, const void* q, const void* k,
  *   Z may be NULL when use_normalizer = 0.  y (B,1,Hq,Dv) out_dtype. */
 la_status la_decode_step(const la_params* p, const void* q, const void* k, const void* v,
                          const void* decay, float* S, float* Z, void* y, la_stream_t stream);
+
+/* la_decode_step with a validity mask (Keras request, Masking): mask (B,)
+ * uint8 device array, one entry per sequence (the (B, T) mask at T = 1);
+ * NULL = all valid.  A sequence whose step is invalid keeps S and Z
+ * bit-for-bit and gets zero outputs. */
+la_status la_decode_step_masked(const la_params* p, const void* q, const void* k, const void* v,
+                                const void* decay, const uint8_t* mask, float* S, float* Z, void* y,
+                                la_stream_t stream);
 
 /* Static string for a status code. */
 const char* la_status_string(la_status s);

@@ -53,6 +53,9 @@ _SIGNATURES = {
     "la_forward_causal_noalloc": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 10),
     "la_forward_noncausal": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 5 + [ctypes.c_size_t, _vp]),
     "la_decode_step": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 8),
+    "la_forward_causal_masked": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 11 + [ctypes.c_size_t, _vp]),
+    "la_forward_noncausal_masked": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 6 + [ctypes.c_size_t, _vp]),
+    "la_decode_step_masked": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 9),
     "la_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "la_last_error": (ctypes.c_char_p, []),
     "la_abi_version": (ctypes.c_int, []),
@@ -127,6 +130,18 @@ def _prep(q, k, v, q_heads, kv_heads, **kw):
     return q, k, v, p
 
 
+def _mask(mask, B, T):
+    """Sequence-validity mask (B, T) as a contiguous one-byte CUDA tensor
+    (bool or uint8, nonzero = valid), or None."""
+    if mask is None:
+        return None
+    if mask.dtype not in (torch.bool, torch.uint8) or not mask.is_cuda:
+        raise ValueError("mask must be a CUDA tensor of dtype bool or uint8")
+    if mask.numel() != B * T:
+        raise ValueError(f"mask must have B*T = {B * T} elements ({B}, {T}), got {tuple(mask.shape)}")
+    return mask.contiguous()
+
+
 def la_workspace_bytes(params: la_params, causal: bool) -> int:
     return int(lib().la_workspace_bytes(ctypes.byref(params), int(bool(causal))))
 
@@ -154,12 +169,13 @@ def la_get_initial_state(batch, kv_heads, key_dim, value_dim, use_normalizer=Tru
 def la_forward_causal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one", use_normalizer=True,
                       epsilon=1e-6, scale=1.0, update_rule="linear", decay=None, initial_state=None,
                       return_state=False, out_dtype=None, out=None, state_out=None, workspace=None,
-                      stream=None):
+                      mask=None, stream=None):
     """Causal pass.  q (B,T,Hq,Dk) / (B,T,Hq*Dk), k and v likewise with Hkv heads.
 
     initial_state: (S0, Z0) or None (zeros).  Returns y, or (y, (S, Z)) with
     return_state.  ``state_out`` may be the initial_state tensors themselves
-    (in-place streaming)."""
+    (in-place streaming).  ``mask`` (B,T) bool/uint8: invalid steps keep the
+    state and output zero (la_forward_causal_masked)."""
     q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=out_dtype, feature_map=feature_map,
                        use_normalizer=use_normalizer, epsilon=epsilon, scale=scale,
                        update_rule=update_rule)
@@ -178,9 +194,15 @@ def la_forward_causal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one",
     if decay is not None and (not decay.is_cuda or not decay.is_contiguous() or decay.dtype != q.dtype):
         raise ValueError("decay must be a contiguous CUDA tensor of the io dtype")
     ws, ws_bytes = _workspace(p, True, q.device, workspace)
-    _check(lib().la_forward_causal(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(S0),
-                                   _ptr(Z0), _ptr(y), _ptr(S), _ptr(Z), _ptr(ws), ws_bytes,
-                                   _stream(stream)))
+    if mask is not None:
+        m = _mask(mask, B, T)
+        _check(lib().la_forward_causal_masked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(m),
+                                              _ptr(S0), _ptr(Z0), _ptr(y), _ptr(S), _ptr(Z), _ptr(ws), ws_bytes,
+                                              _stream(stream)))
+    else:
+        _check(lib().la_forward_causal(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(S0),
+                                       _ptr(Z0), _ptr(y), _ptr(S), _ptr(Z), _ptr(ws), ws_bytes,
+                                       _stream(stream)))
     return (y, (S, Z)) if return_state else y
 
 
@@ -204,31 +226,44 @@ def la_forward_causal_noalloc(q, k, v, *, q_heads, kv_heads, feature_map="elu_pl
 
 
 def la_forward_noncausal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one", use_normalizer=True,
-                         epsilon=1e-6, scale=1.0, out_dtype=None, out=None, workspace=None, stream=None):
-    """Non-causal pass with the global state; returns y (B,T,Hq,Dv)."""
+                         epsilon=1e-6, scale=1.0, out_dtype=None, out=None, workspace=None, mask=None,
+                         stream=None):
+    """Non-causal pass with the global state; returns y (B,T,Hq,Dv).  ``mask``
+    (B,T): invalid keys/values leave the sums, invalid queries output zero."""
     q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=out_dtype, feature_map=feature_map,
                        use_normalizer=use_normalizer, epsilon=epsilon, scale=scale)
     B, T, _, _ = q.shape
     ydt = q.dtype if out_dtype is None else out_dtype
     y = out if out is not None else torch.empty(B, T, q_heads, v.shape[3], dtype=ydt, device=q.device)
     ws, ws_bytes = _workspace(p, False, q.device, workspace)
-    _check(lib().la_forward_noncausal(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(ws),
-                                      ws_bytes, _stream(stream)))
+    if mask is not None:
+        m = _mask(mask, B, T)
+        _check(lib().la_forward_noncausal_masked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(m), _ptr(y),
+                                                 _ptr(ws), ws_bytes, _stream(stream)))
+    else:
+        _check(lib().la_forward_noncausal(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(ws),
+                                          ws_bytes, _stream(stream)))
     return y
 
 
 def la_decode_step(q, k, v, S, Z=None, *, q_heads, kv_heads, feature_map="elu_plus_one",
                    use_normalizer=True, epsilon=1e-6, scale=1.0, update_rule="linear", decay=None,
-                   out_dtype=None, out=None, stream=None):
-    """One token per sequence; S (and Z) are updated in place.  Returns y (B,1,Hq,Dv)."""
+                   out_dtype=None, out=None, mask=None, stream=None):
+    """One token per sequence; S (and Z) are updated in place.  Returns y (B,1,Hq,Dv).
+    ``mask`` (B,) or (B,1): a sequence whose step is invalid keeps S, Z and outputs zero."""
     q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=out_dtype, feature_map=feature_map,
                        use_normalizer=use_normalizer, epsilon=epsilon, scale=scale,
                        update_rule=update_rule)
     ydt = q.dtype if out_dtype is None else out_dtype
     y = out if out is not None else torch.empty(q.shape[0], 1, q_heads, v.shape[3], dtype=ydt,
                                                 device=q.device)
-    _check(lib().la_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(S),
-                                _ptr(Z), _ptr(y), _stream(stream)))
+    if mask is not None:
+        m = _mask(mask, q.shape[0], 1)
+        _check(lib().la_decode_step_masked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(m),
+                                           _ptr(S), _ptr(Z), _ptr(y), _stream(stream)))
+    else:
+        _check(lib().la_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(S),
+                                    _ptr(Z), _ptr(y), _stream(stream)))
     return y
 
 

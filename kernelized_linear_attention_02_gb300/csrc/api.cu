@@ -177,12 +177,14 @@ size_t la_workspace_bytes(const la_params* p, int causal) {
     return workspace_bytes(P, causal != 0);
 }
 
-la_status la_forward_causal(const la_params* p, const void* q, const void* k, const void* v,
-                            const void* decay, const float* S0, const float* Z0, void* y,
-                            float* S_out, float* Z_out, void* ws, size_t ws_bytes, la_stream_t stream) {
+la_status la_forward_causal_masked(const la_params* p, const void* q, const void* k, const void* v,
+                                   const void* decay, const uint8_t* mask, const float* S0, const float* Z0,
+                                   void* y, float* S_out, float* Z_out, void* ws, size_t ws_bytes,
+                                   la_stream_t stream) {
     la::Problem P;
     la_status st = make_problem(p, Call::kCausal, &P);
     if (st != LA_OK) return st;
+    P.mask = mask;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!P.norm) Z0 = nullptr, Z_out = nullptr;  // no key_state without the normalizer
     if (P.T == 0) {  // nothing to attend: the state passes through
@@ -210,6 +212,12 @@ la_status la_forward_causal(const la_params* p, const void* q, const void* k, co
     return LA_OK;
 }
 
+la_status la_forward_causal(const la_params* p, const void* q, const void* k, const void* v,
+                            const void* decay, const float* S0, const float* Z0, void* y,
+                            float* S_out, float* Z_out, void* ws, size_t ws_bytes, la_stream_t stream) {
+    return la_forward_causal_masked(p, q, k, v, decay, nullptr, S0, Z0, y, S_out, Z_out, ws, ws_bytes, stream);
+}
+
 la_status la_forward_causal_noalloc(const la_params* p, const void* q, const void* k, const void* v,
                                     const void* decay, const float* S0, const float* Z0, void* y,
                                     float* S_out, float* Z_out, la_stream_t stream) {
@@ -232,11 +240,13 @@ la_status la_forward_causal_noalloc(const la_params* p, const void* q, const voi
                              stream);
 }
 
-la_status la_forward_noncausal(const la_params* p, const void* q, const void* k, const void* v, void* y,
-                               void* ws, size_t ws_bytes, la_stream_t stream) {
+la_status la_forward_noncausal_masked(const la_params* p, const void* q, const void* k, const void* v,
+                                      const uint8_t* mask, void* y, void* ws, size_t ws_bytes,
+                                      la_stream_t stream) {
     la::Problem P;
     la_status st = make_problem(p, Call::kNonCausal, &P);
     if (st != LA_OK) return st;
+    P.mask = mask;
     if (P.T == 0) {
         g_last_error.clear();
         return LA_OK;
@@ -257,11 +267,18 @@ la_status la_forward_noncausal(const la_params* p, const void* q, const void* k,
     return LA_OK;
 }
 
-la_status la_decode_step(const la_params* p, const void* q, const void* k, const void* v, const void* decay,
-                         float* S, float* Z, void* y, la_stream_t stream) {
+la_status la_forward_noncausal(const la_params* p, const void* q, const void* k, const void* v, void* y,
+                               void* ws, size_t ws_bytes, la_stream_t stream) {
+    return la_forward_noncausal_masked(p, q, k, v, nullptr, y, ws, ws_bytes, stream);
+}
+
+la_status la_decode_step_masked(const la_params* p, const void* q, const void* k, const void* v,
+                                const void* decay, const uint8_t* mask, float* S, float* Z, void* y,
+                                la_stream_t stream) {
     la::Problem P;
     la_status st = make_problem(p, Call::kDecode, &P);
     if (st != LA_OK) return st;
+    P.mask = mask;
     if (!q || !k || !v || !y || !S) return fail(LA_ERR_INVALID_ARG, "q, k, v, y and S are required");
     if (P.norm && !Z) return fail(LA_ERR_INVALID_ARG, "Z is required when use_normalizer = 1");
     if (P.gated && !decay) return fail(LA_ERR_INVALID_ARG, "the gated rule needs decay");
@@ -275,6 +292,11 @@ la_status la_decode_step(const la_params* p, const void* q, const void* k, const
     if (e != cudaSuccess) return cuda_fail(e, "la_decode_step");
     g_last_error.clear();
     return LA_OK;
+}
+
+la_status la_decode_step(const la_params* p, const void* q, const void* k, const void* v, const void* decay,
+                         float* S, float* Z, void* y, la_stream_t stream) {
+    return la_decode_step_masked(p, q, k, v, decay, nullptr, S, Z, y, stream);
 }
 
 }  // extern "C"

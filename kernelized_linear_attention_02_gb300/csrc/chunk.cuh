@@ -260,11 +260,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int fmap = FMAP;
     const float eps = a.eps, scale = a.scale;
     const __nv_bfloat16* __restrict__ decay = a.decay;
+    const uint8_t* __restrict__ mask = a.mask;
     void* const yout = a.y;
     const int b = bh / Hkv, hk = bh - b * Hkv;
     const int nchunks = (T + kC - 1) / kC;
     const int c_begin = seg * a.cps;
     const int nck = min(nchunks, c_begin + a.cps) - c_begin;
+    // Validity of the steps t0 .. t0 + 63 of this sequence as a 64-bit word
+    // (Keras request, Masking; steps past T count as valid, they are cut
+    // elsewhere).  Warp-collective: two loads per lane and two ballots.
+    auto valid_word = [&](int t0) -> uint64_t {
+        if (!mask) return ~0ull;
+        const size_t bt = (size_t)b * T + t0;
+        const bool v0 = t0 + lane >= T || mask[bt + lane] != 0;
+        const bool v1 = t0 + 32 + lane >= T || mask[bt + 32 + lane] != 0;
+        return (uint64_t)__ballot_sync(0xffffffffu, v0) | ((uint64_t)__ballot_sync(0xffffffffu, v1) << 32);
+    };
 
     auto Kb = [&](int s) { return kv_base + s * Cf::kKvStage; };
     auto Kd = [&](int s) { return kv_base + s * Cf::kKvStage + Cf::kOffKd; };
@@ -347,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&y_full[yb], (m / NY) & 1, err, kErrYFull)) return false;
         tc_fence_after();
         if (quad == 0 && lane == 0) LA_TR(4, 3, m);
+        const uint64_t okw = valid_word(t0);  // invalid steps get zero output rows
         // all 64 tokens of this lane in one round trip to TMEM; the buffer is
         // released before the stores.  Head size 64 with a staged tile: Y^T is
         // an M = 64 tile (lanes 0-15 of each quadrant), read in the 16x256b
@@ -411,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int x = c / kCpr, cc = c - x * kCpr;
                 if (x < valid)
                     *reinterpret_cast<uint4*>(yrow0 + x * tstride + cc * 8) =
-                        *reinterpret_cast<const uint4*>(ys + x * P + cc * 8);
+                        (okw >> x) & 1 ? *reinterpret_cast<const uint4*>(ys + x * P + cc * 8) : make_uint4(0, 0, 0, 0);
             }
             if (!group_sync(out_group, ophase, err, kErrYFull)) return false;  // tile free again
         } else if (vrow_ok) {
@@ -423,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int x = g * 8 + e;
-                    const float o = f[e] * __uint_as_float(x < 32 ? y0[x] : y1[x - 32]);
+                    const float o = (okw >> x) & 1 ? f[e] * __uint_as_float(x < 32 ? y0[x] : y1[x - 32]) : 0.f;
                     if (x < valid) {
                         if (OUT_BF16)
                             reinterpret_cast<__nv_bfloat16*>(yout)[base + x * tstride] = __float2bfloat16_rn(o);
@@ -1119,8 +1131,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ct < 32) {
                     float g0 = 0.f, g1 = 0.f;
                     const int j0 = 2 * ct, j1 = 2 * ct + 1;
-                    if (j0 < valid) g0 = __bfloat162float(decay[((size_t)b * T + t0 + j0) * Hkv + hk]);
-                    if (j1 < valid) g1 = __bfloat162float(decay[((size_t)b * T + t0 + j1) * Hkv + hk]);
+                    // an invalid step (mask) keeps the state: no decay either
+                    if (j0 < valid && step_valid(mask, (size_t)b * T + t0 + j0))
+                        g0 = __bfloat162float(decay[((size_t)b * T + t0 + j0) * Hkv + hk]);
+                    if (j1 < valid && step_valid(mask, (size_t)b * T + t0 + j1))
+                        g1 = __bfloat162float(decay[((size_t)b * T + t0 + j1) * Hkv + hk]);
                     const float sum = g0 + g1;
                     float incl = sum;
 #pragma unroll
@@ -1152,7 +1167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
                 gtot = gc[kC - 1];
             }
-            const bool touch = GATED || SPLITK || NORM || fmap != LA_FMAP_NONE;
+            // invalid steps (mask): their phi(k) and v rows become zero, so
+            // they add nothing to the state, the key sum or any score
+            const uint64_t okw = valid_word(t0);
+            const bool touch = GATED || SPLITK || NORM || fmap != LA_FMAP_NONE || mask;
             if (ct == 0) LA_TR(2, 7, i);
             if (touch) {
                 float colsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -1166,19 +1184,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int row = rbase + kRowStep * m;
                     const uint4 cur = nxt;
                     if (m + 1 < kPer) nxt = *reinterpret_cast<const uint4*>(Kb(s) + chunk_off(m + 1, Cf::kKBlk));
+                    const bool drop = !((okw >> row) & 1);
+                    if (drop) {
+                        *reinterpret_cast<uint4*>(Kb(s) + chunk_off(m, Cf::kKBlk)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(Vb(s) + chunk_off(m)) = make_uint4(0, 0, 0, 0);
+                    }
                     float f[8];
                     bf8_to_f(cur, f);
                     uint4 hi, lo;
                     if (GATED) {
                         const float w = __expf(gtot - gc[row]);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] *= w;
+                        for (int e = 0; e < 8; ++e) f[e] = drop ? 0.f : f[e] * w;
                         split8(f, hi, lo);
                         *reinterpret_cast<uint4*>(Kd(s) + chunk_off(m)) = hi;
                         *reinterpret_cast<uint4*>(Klo(s) + chunk_off(m)) = lo;
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = phi<true>(fmap, f[e], eps);
+                        for (int e = 0; e < 8; ++e) f[e] = drop ? 0.f : phi<true>(fmap, f[e], eps);
                         if (fmap != LA_FMAP_NONE || SPLITK) {
                             split8(f, hi, lo);
                             if (fmap != LA_FMAP_NONE) *reinterpret_cast<uint4*>(Kb(s) + chunk_off(m, Cf::kKBlk)) = hi;

@@ -33,6 +33,7 @@ struct Args {
     float* Z_dst;
     float* G_dst;                 // state + gated: (B*Hkv, nseg) log decay of each segment
     const __nv_bfloat16* decay;   // (B, T, Hkv)
+    const uint8_t* mask;          // (B, T) step validity, nonzero = valid; null = every step valid
     void* y;                      // (B, T, Hq, Dv) output, bf16 or fp32
     unsigned* err;
 };

@@ -148,6 +148,7 @@ chunk::Launch base_launch(const Problem& P, int mode, const DevInfo& di) {
     a.fmap = P.fmap;
     a.eps = P.eps;
     a.scale = P.scale;
+    a.mask = P.mask;
     a.err = di.err;
     return L;
 }

@@ -19,7 +19,12 @@ struct Problem {
     int io_bf16, out_bf16;
     int fmap, norm, gated;
     float eps, scale;
+    // (B, T) sequence-validity mask, nonzero = valid; null = every step valid
+    const uint8_t* mask = nullptr;
 };
+
+// Step t of sequence b is valid (Keras request, Masking).
+__device__ __forceinline__ bool step_valid(const uint8_t* mask, int64_t bt) { return !mask || mask[bt] != 0; }
 
 __device__ __forceinline__ float load_in(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float load_in(const __nv_bfloat16* p, int64_t i) {

@@ -14,6 +14,10 @@
 // state, which is touched once per step, from displacing other data in L2.
 // The read-out for every query head of the group is reduced across the
 // eight warps in shared memory.
+//
+// A sequence-validity mask (Keras request, Masking) makes a sequence's step
+// invalid: its state and key sum are left exactly as they were and its
+// outputs are zero.  The decision is per batch row, uniform across a CTA.
 #include <algorithm>
 
 #include "common.cuh"
@@ -78,6 +82,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
         fq[idx] = phi<true>(P.fmap, load_in(q, (b * P.Hq + hk * G + r) * Dk + i), P.eps);
     }
     __syncthreads();
+    const bool valid = step_valid(P.mask, b);
+    if (!valid) {  // state untouched, zero outputs
+        for (int idx = tid; idx < G * Dv; idx += kThreads) store_out(y, (b * P.Hq + hk * G) * Dv + idx, 0.f);
+        return;
+    }
     if (P.norm && tid < Dk) {
         const float z = a.Z[bh * Dk + tid] + fk[tid];
         zs[tid] = z;
@@ -226,7 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jv = tid; jv < Dv; jv += kThreads) vv[jv] = load_in(vs, jv);
         for (int idx = tid; idx < G * Dk; idx += kThreads) fq[idx] = phi<true>(P.fmap, load_in(qs, idx), P.eps);
         __syncthreads();
-        if (P.norm && tid < Dk) {
+        // an invalid step (mask) keeps the stage as loaded: the store below
+        // then writes the state back unchanged
+        const bool valid = step_valid(P.mask, b);
+        if (valid && P.norm && tid < Dk) {
             const float z = reinterpret_cast<const float*>(st + ly.z)[tid] + fk[tid];
             zs[tid] = z;
             a.Z[u * Dk + tid] = z;
@@ -234,15 +246,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float dec = P.gated ? __expf(load_in(static_cast<const TIn*>(a.decay), u)) : 1.f;
         // S <- dec * S + phi(k) (x) v, written back into the stage
         const float4 v4 = colok ? reinterpret_cast<const float4*>(vv)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
 #pragma unroll
-        for (int m = 0; m < kRows; ++m) {
-            const int i = warp + 8 * m;
-            const float f = i < Dk ? fk[i] : 0.f;
-            s[m].x = fmaf(f, v4.x, dec * s[m].x);
-            s[m].y = fmaf(f, v4.y, dec * s[m].y);
-            s[m].z = fmaf(f, v4.z, dec * s[m].z);
-            s[m].w = fmaf(f, v4.w, dec * s[m].w);
-            if (i < Dk && colok) Ss[i * nvec + lane] = s[m];
+            for (int m = 0; m < kRows; ++m) {
+                const int i = warp + 8 * m;
+                const float f = i < Dk ? fk[i] : 0.f;
+                s[m].x = fmaf(f, v4.x, dec * s[m].x);
+                s[m].y = fmaf(f, v4.y, dec * s[m].y);
+                s[m].z = fmaf(f, v4.z, dec * s[m].z);
+                s[m].w = fmaf(f, v4.w, dec * s[m].w);
+                if (i < Dk && colok) Ss[i * nvec + lane] = s[m];
+            }
         }
         fence_proxy_async();  // this thread's state writes, before the bulk store reads them
         __syncthreads();      // every state row written; zs complete
@@ -252,6 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the stage of unit j - 1 is read out by its store: refill it
             bulk_wait_group_read<1>();
             if (j + nst - 1 < nj) issue_load(j + nst - 1);
+        }
+        if (!valid) {  // uniform across the CTA
+            for (int idx = tid; idx < G * Dv; idx += kThreads) store_out(y, (b * P.Hq + hk * G) * Dv + idx, 0.f);
+            continue;
         }
 
         if (P.norm)

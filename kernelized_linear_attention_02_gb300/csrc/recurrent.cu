@@ -11,6 +11,11 @@
 // The same kernel also runs the two halves of the non-causal form: a state
 // pass (update only; S = sum_j phi(K_j)^T V_j, Z = sum_j phi(K_j)) and a
 // read-out pass with that fixed global state.
+//
+// A sequence-validity mask (Keras request, Masking) skips the update of an
+// invalid step (the state passes through unchanged, no decay either) and
+// writes zeros for its outputs.  The mask is per (batch, step), so the
+// decision is uniform across the CTA.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -77,6 +82,12 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(RecArgs a) {
 
     for (int64_t t = 0; t < P.T; ++t) {
         const int64_t tok = b * P.T + t;
+        if (!step_valid(P.mask, tok)) {
+            if (readout)
+                for (int idx = tid; idx < G * Dv; idx += kThreads)
+                    store_out(y, (tok * P.Hq + hk * G) * Dv + idx, 0.f);
+            continue;
+        }
         if (update)
             for (int i = tid; i < Dk; i += kThreads)
                 fk[i] = phi<false>(P.fmap, load_in(k, (tok * P.Hkv + hk) * Dk + i), P.eps);

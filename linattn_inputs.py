@@ -36,6 +36,7 @@ class Workload:
     k_l2_normalize: bool = False
     decay_mu: float = 4.0     # gated: g = log(sigmoid(x)), x ~ N(decay_mu, 1)
     seed: int = 0
+    mask: str = ""            # "" (no mask) or a validity_mask kind, e.g. "right"
 
 
 TINY = Workload("tiny_B1_H2_T64_D16_f32", 1, 64, 2, 2, 16, 16, torch.float32,
@@ -55,7 +56,13 @@ ONNX_LINEAR = Workload("onnx_linear_gqa_B2_T32768_Hq32_Hkv8_D128_bf16", 2, 32768
 ONNX_GATED = dataclasses.replace(ONNX_LINEAR, name="onnx_gated_gqa_B2_T32768_Hq32_Hkv8_D128_bf16",
                                  rule="gated")
 
-ALL = [TINY, PREFILL_2K, LONG_8K, LONG_8K_UNNORM, DECODE, ONNX_LINEAR, ONNX_GATED]
+# the 2k prefill as a right-padded batch: sequence b is valid for its first
+# L_b steps, L_b uniform in [T/2, T] (Keras request, Masking: right padding)
+PREFILL_2K_RIGHTPAD = dataclasses.replace(PREFILL_2K, name=PREFILL_2K.name + "_rightpad_mask", mask="right")
+
+ALL = [TINY, PREFILL_2K, LONG_8K, LONG_8K_UNNORM, DECODE, ONNX_LINEAR, ONNX_GATED, PREFILL_2K_RIGHTPAD]
+
+MASK_KINDS = ("right", "left", "gaps", "random", "none_valid", "all_valid")
 
 
 def generator(seed: int, device="cpu") -> torch.Generator:
@@ -97,6 +104,38 @@ def make_qkv(w: Workload, device="cpu", T=None, B=None, seed=None):
                    device=device)
         decay = torch.nn.functional.logsigmoid(x).to(w.dtype)
     return q, k, v, decay
+
+
+def validity_mask(kind: str, B: int, T: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """A (B, T) bool sequence-validity mask of one of the layouts the Keras
+    request's tests name (Mask and state behavior):
+
+    right       sequence b valid for its first L_b steps, L_b ~ U[T/2, T]
+    left        valid for its last L_b steps
+    gaps        valid except 1-3 interior runs of 1..T/4 steps per sequence
+    random      each step valid with probability 0.7
+    none_valid  all false;  all_valid  all true."""
+    g = generator(seed, "cpu")
+    t = torch.arange(T)
+    if kind in ("right", "left"):
+        L = torch.randint(T // 2, T + 1, (B,), generator=g) if T > 0 else torch.zeros(B, dtype=torch.long)
+        m = t[None, :] < L[:, None] if kind == "right" else t[None, :] >= (T - L)[:, None]
+    elif kind == "gaps":
+        m = torch.ones(B, T, dtype=torch.bool)
+        for b in range(B):
+            for _ in range(int(torch.randint(1, 4, (1,), generator=g))):
+                n = int(torch.randint(1, max(2, T // 4 + 1), (1,), generator=g))
+                s = int(torch.randint(0, max(1, T - n + 1), (1,), generator=g))
+                m[b, s:s + n] = False
+    elif kind == "random":
+        m = torch.rand(B, T, generator=g) < 0.7
+    elif kind == "none_valid":
+        m = torch.zeros(B, T, dtype=torch.bool)
+    elif kind == "all_valid":
+        m = torch.ones(B, T, dtype=torch.bool)
+    else:
+        raise ValueError(kind)
+    return m.to(device)
 
 
 def tiny_paper_inputs(seed=42, n=32, d=16):

@@ -125,4 +125,4 @@ def test_workspace_too_small_rejected(L):
 def test_status_strings(L):
     for s in range(5):
         assert L.la_status_string(s)
-    assert L.la_abi_version() == 1
+    assert L.la_abi_version() == 2
