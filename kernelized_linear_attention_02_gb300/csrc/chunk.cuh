@@ -196,8 +196,11 @@ __device__ __forceinline__ __nv_bfloat16& bf_at(uint8_t* base, uint32_t off) {
 
 // SPLIT: two MMA issuers (linear causal rule with G > 1 query heads per kv
 // head, see Cfg::kSplitMma); a separate instantiation, so that the kernels
-// for G = 1 carry no code of the split issue.
-template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16, bool SPLIT = false>
+// for G = 1 carry no code of the split issue.  MASK: the sequence-validity
+// mask is read (Keras request, Masking); without it the mask pointer is a
+// constant null and every mask branch folds away, so unmasked calls run
+// exactly the code they would run without mask support.
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16, bool SPLIT = false, bool MASK = false>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_kernel(const __grid_constant__ Args a, const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                  const __grid_constant__ CUtensorMap mapV) {
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int fmap = FMAP;
     const float eps = a.eps, scale = a.scale;
     const __nv_bfloat16* __restrict__ decay = a.decay;
-    const uint8_t* __restrict__ mask = a.mask;
+    const uint8_t* __restrict__ mask = MASK ? a.mask : nullptr;
     void* const yout = a.y;
     const int b = bh / Hkv, hk = bh - b * Hkv;
     const int nchunks = (T + kC - 1) / kC;

@@ -56,5 +56,12 @@ cudaError_t chunk_run_causal_d128_bf16(const chunk::Launch& L, cudaStream_t st);
 cudaError_t chunk_run_causal_d128_f32(const chunk::Launch& L, cudaStream_t st);
 cudaError_t chunk_run_other_d64(const chunk::Launch& L, cudaStream_t st);
 cudaError_t chunk_run_other_d128(const chunk::Launch& L, cudaStream_t st);
+// the same launchers for calls with a sequence-validity mask
+cudaError_t chunk_run_causal_d64_bf16_mask(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_causal_d64_f32_mask(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_causal_d128_bf16_mask(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_causal_d128_f32_mask(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_other_d64_mask(const chunk::Launch& L, cudaStream_t st);
+cudaError_t chunk_run_other_d128_mask(const chunk::Launch& L, cudaStream_t st);
 
 }  // namespace la

@@ -125,6 +125,13 @@ bool act_map(CUtensorMap* m, const void* base, int D, int H, int64_t T, int64_t 
 }
 
 cudaError_t run(const chunk::Launch& L, int D, cudaStream_t st) {
+    if (L.args.mask) {  // the masked instantiations
+        if (L.mode == chunk::kCausal) {
+            if (D == 64) return L.out_bf16 ? chunk_run_causal_d64_bf16_mask(L, st) : chunk_run_causal_d64_f32_mask(L, st);
+            return L.out_bf16 ? chunk_run_causal_d128_bf16_mask(L, st) : chunk_run_causal_d128_f32_mask(L, st);
+        }
+        return D == 64 ? chunk_run_other_d64_mask(L, st) : chunk_run_other_d128_mask(L, st);
+    }
     if (L.mode == chunk::kCausal) {
         if (D == 64) return L.out_bf16 ? chunk_run_causal_d64_bf16(L, st) : chunk_run_causal_d64_f32(L, st);
         return L.out_bf16 ? chunk_run_causal_d128_bf16(L, st) : chunk_run_causal_d128_f32(L, st);

@@ -9,10 +9,10 @@
 namespace la {
 namespace chunk {
 
-template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUTBF, bool SPLIT = false>
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUTBF, bool SPLIT = false, bool MASK = false>
 cudaError_t run_one(const Launch& L, cudaStream_t st) {
     using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUTBF>;
-    auto kern = chunk_kernel<D, MODE, NORM, FMAP, GATED, OUTBF, SPLIT>;
+    auto kern = chunk_kernel<D, MODE, NORM, FMAP, GATED, OUTBF, SPLIT, MASK>;
     static int configured = -1;  // device on which the shared-memory limit was raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -44,15 +44,16 @@ cudaError_t run_one(const Launch& L, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-// OUT: 1 = bf16 output, 0 = float32 output (the state pass writes no output)
-template <int D, int MODE, int OUT>
+// OUT: 1 = bf16 output, 0 = float32 output (the state pass writes no output);
+// MASK: the instantiations that read a sequence-validity mask
+template <int D, int MODE, int OUT, bool MASK = false>
 struct Dispatch {
     template <bool NORM, int FMAP, bool GATED>
     static cudaError_t one(const Launch& L, cudaStream_t st) {
         // linear causal rule with grouped query heads: the two-issuer kernel
         if (MODE == kCausal && !GATED && L.args.G > 1)
-            return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, MODE == kCausal && !GATED>(L, st);
-        return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1>(L, st);
+            return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, MODE == kCausal && !GATED, MASK>(L, st);
+        return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, false, MASK>(L, st);
     }
     template <bool NORM>
     static cudaError_t fmap(const Launch& L, cudaStream_t st) {
