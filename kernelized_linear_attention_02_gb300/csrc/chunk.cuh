@@ -346,6 +346,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     unsigned* err = a.err;
 
+    // Query head item n (chunk i): feature map in place (bf16), plus the fp32
+    // copy for the tf32 read-out, or the decayed copy of the gated rule.  Run
+    // by 128 threads (qt = 0..127, whole warps): the feature warps, or, for the
+    // linear causal kernel with one query head per kv head, the epilogue
+    // warps, which convert item n + 1 right after masking the scores of item n
+    // and so take this work off the feature warps that pace the keys.
+    auto q_features = [&](int i, int n, int qt) -> bool {
+        constexpr int kCPR = Cf::kCPR, kRowStep = Cf::kRowStep, kPer = Cf::kPer;
+        const int cc = qt % kCPR, rbase = qt / kCPR;
+        auto chunk_off = [&](int m) -> uint32_t {
+            const int row = rbase + kRowStep * m;
+            return static_cast<uint32_t>((cc >> 3) * 8192 + row * 128 + ((((cc & 7) ^ (row & 7))) << 4));
+        };
+        const int sq = n % NQ1;
+        if (!warp_wait(&full_q[sq], (n / NQ1) & 1, err, kErrFullQ)) return false;
+        if (qt == 0) LA_TR(2, 3, n);
+        if (fmap != LA_FMAP_NONE || GATED || TF32) {
+            const float* gc = Gc(i % NKV1);
+            uint4 nxt = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(0));
+#pragma unroll 1
+            for (int m = 0; m < kPer; ++m) {
+                const uint4 cur = nxt;
+                if (m + 1 < kPer) nxt = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(m + 1));
+                float f[8];
+                bf8_to_f(cur, f);
+                if (GATED) {
+                    const float w = __expf(gc[rbase + kRowStep * m]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] *= w;
+                    *reinterpret_cast<uint4*>(Qd(sq) + chunk_off(m)) = f_to_bf8(f);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = phi<true>(fmap, f[e], eps);
+                    if (fmap != LA_FMAP_NONE) *reinterpret_cast<uint4*>(Qb(sq) + chunk_off(m)) = f_to_bf8(f);
+                    if (TF32) {
+                        // features 8cc..8cc+7 are two 16-byte chunks of a 32-feature block
+                        const int row = rbase + kRowStep * m;
+                        uint8_t* blk = Qf(sq) + (cc >> 2) * 8192 + row * 128;
+                        const int c16 = 2 * (cc & 3);
+                        *reinterpret_cast<float4*>(blk + ((c16 ^ (row & 7)) << 4)) =
+                            make_float4(f[0], f[1], f[2], f[3]);
+                        *reinterpret_cast<float4*>(blk + (((c16 + 1) ^ (row & 7)) << 4)) =
+                            make_float4(f[4], f[5], f[6], f[7]);
+                    }
+                }
+            }
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv_q[sq]);
+        if (qt == 0) LA_TR(2, 4, n);
+        return true;
+    };
+    constexpr bool kQOnEpi = MODE == kCausal && !GATED && !split;
+
     // Output of item m (query head m % G of chunk m / G): Y^T from TMEM times
     // scale/den, stored to global memory.  Run by four warps, one per TMEM lane
     // quadrant: the state warps (linear rule) or the epilogue warps (gated).
@@ -880,7 +935,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------------- epilogue
         const int quad = warp & 3;  // TMEM lane quadrant of this warp
         const int n_total = Cf::kHasQ ? nck * G : 0;
+        const int et = tid - kEpiWarp0 * 32;  // 0..127
         bool ok = true;
+        if (kQOnEpi && n_total > 0) ok = q_features(0, 0, et);
         for (int n = 0; n < n_total && ok; ++n) {
             {
                 // -------- scores of item n: mask, decay, hi/lo split, 1/den
@@ -1005,6 +1062,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // the next query item, while the tensor core runs this item's products
+            if (kQOnEpi && ok && n + 1 < n_total) ok = q_features((n + 1) / G, n + 1, et);
         }
     } else if (warp == kMmaSWarp) {
         // ------------------------------------------------ MMA issuer of the state
@@ -1252,48 +1311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        // ---- query head item n (chunk i): feature map in place, or the decayed copy
-        auto process_q = [&](int i, int n) -> bool {
-            const int sq = n % NQ1;
-            if (!warp_wait(&full_q[sq], (n / NQ1) & 1, err, kErrFullQ)) return false;
-            if (ct == 0) LA_TR(2, 3, n);
-            if (fmap != LA_FMAP_NONE || GATED || TF32) {
-                const float* gc = Gc(i % NKV1);
-                uint4 nxt = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(0));
-#pragma unroll 1
-                for (int m = 0; m < kPer; ++m) {
-                    const uint4 cur = nxt;
-                    if (m + 1 < kPer) nxt = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(m + 1));
-                    float f[8];
-                    bf8_to_f(cur, f);
-                    if (GATED) {
-                        const float w = __expf(gc[rbase + kRowStep * m]);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] *= w;
-                        *reinterpret_cast<uint4*>(Qd(sq) + chunk_off(m)) = f_to_bf8(f);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = phi<true>(fmap, f[e], eps);
-                        if (fmap != LA_FMAP_NONE) *reinterpret_cast<uint4*>(Qb(sq) + chunk_off(m)) = f_to_bf8(f);
-                        if (TF32) {
-                            // features 8cc..8cc+7 are two 16-byte chunks of a 32-feature block
-                            const int row = rbase + kRowStep * m;
-                            uint8_t* blk = Qf(sq) + (cc >> 2) * 8192 + row * 128;
-                            const int c16 = 2 * (cc & 3);
-                            *reinterpret_cast<float4*>(blk + ((c16 ^ (row & 7)) << 4)) =
-                                make_float4(f[0], f[1], f[2], f[3]);
-                            *reinterpret_cast<float4*>(blk + (((c16 + 1) ^ (row & 7)) << 4)) =
-                                make_float4(f[4], f[5], f[6], f[7]);
-                        }
-                    }
-                }
-            }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&conv_q[sq]);
-            if (ct == 0) LA_TR(2, 4, n);
-            return true;
-        };
+        auto process_q = [&](int i, int n) -> bool { return q_features(i, n, ct); };
 
 
         if (MODE == kApply) {
@@ -1309,7 +1327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // keys of chunk i, then its query heads, chunk after chunk
             for (int i = 0; i < nck && ok; ++i) {
                 ok = process_kv(i);
-                if (MODE == kCausal)
+                if (MODE == kCausal && !kQOnEpi)
                     for (int r = 0; r < G && ok; ++r) ok = process_q(i, i * G + r);
             }
             // key sum: final (causal, last segment) or this segment's increment (state pass)
