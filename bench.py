@@ -150,7 +150,7 @@ def prefill_alg_bytes(w, T=None):
     esz = 2 if w.dtype == torch.bfloat16 else 4
     qy = w.B * T * w.q_heads * (w.Dk + w.Dv) * esz
     kv = w.B * T * w.kv_heads * (w.Dk + w.Dv) * esz
-    dec = w.B * T * w.kv_heads * esz if w.rule == "gated" else 0
+    dec = w.B * T * w.kv_heads * (w.Dk if w.decay_per_dim else 1) * esz if w.rule == "gated" else 0
     msk = w.B * T if w.mask else 0  # one validity byte per (batch, step)
     return qy + kv + dec + msk
 
@@ -356,7 +356,7 @@ def workload_sweep(la, steps, warmup, stream, hbm_gbs):
     out = []
     cases = [(inputs.PREFILL_2K, True), (inputs.LONG_8K, True), (inputs.LONG_8K_UNNORM, True),
              (inputs.LONG_8K, False), (inputs.LONG_8K_UNNORM, False), (inputs.ONNX_LINEAR, True),
-             (inputs.ONNX_GATED, True), (inputs.PREFILL_2K_RIGHTPAD, True)]
+             (inputs.ONNX_GATED, True), (inputs.PREFILL_2K_RIGHTPAD, True), (inputs.GATED_PERDIM, True)]
     for w, causal in cases:
         ms, lpc = time_workload(la, w, steps, warmup, stream, causal)
         alg = prefill_alg_bytes(w)

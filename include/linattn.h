@@ -21,6 +21,7 @@
  *     grouped KV heads (query head h reads kv head h / (Hq/Hkv)), update rules
  *       linear  S_t = S_{t-1} + k_t (x) v_t
  *       gated   S_t = exp(g_t) S_{t-1} + k_t (x) v_t   (g_t per kv head, log space)
+ *               or, per key dimension, row i of S_t scaled by exp(g_t[i])
  *     with o_t = scale * q_t^T S_t and scale 0.0 meaning 1/sqrt(d_k).
  *
  * Conventions shared by every entry point
@@ -29,7 +30,8 @@
  *    memory; scratch comes from the caller's workspace.
  *  - Activations: q (B, T, Hq, Dk), k (B, T, Hkv, Dk), v (B, T, Hkv, Dv),
  *    y (B, T, Hq, Dv) -- the same bytes as the ONNX packed (B, T, H*D).
- *    decay (B, T, Hkv) in the io dtype, log space.
+ *    decay (B, T, Hkv) in the io dtype, log space; with decay_per_key_dim
+ *    (B, T, Hkv, Dk), the ONNX (B, T, H_kv*d_k) layout.
  *  - State: S (B, Hkv, Dk, Dv) float32, Z (B, Hkv, Dk) float32.  S[b,h,i,j]
  *    accumulates phi(k)_i * v_j.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
@@ -91,7 +93,9 @@ typedef struct la_params {
     float epsilon;           /* normalization_epsilon >= 0 (also the relu offset) */
     float scale;             /* output scale; 0.0 means 1/sqrt(Dk) (ONNX default) */
     int32_t update_rule;     /* la_update_rule */
-    int32_t reserved;        /* must be 0 */
+    int32_t decay_per_key_dim; /* 0: decay (B,T,Hkv); 1: decay (B,T,Hkv,Dk) (gated rule only).
+                                * The tensor-core prefill takes the per-head form; the
+                                * per-key-dimension form runs on CUDA cores (token by token). */
 } la_params;
 
 /* Zero-filled initial state, Keras get_initial_state / ONNX default

@@ -41,7 +41,7 @@ class la_params(ctypes.Structure):
         ("io_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
         ("feature_map", ctypes.c_int32), ("use_normalizer", ctypes.c_int32),
         ("epsilon", ctypes.c_float), ("scale", ctypes.c_float),
-        ("update_rule", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("update_rule", ctypes.c_int32), ("decay_per_key_dim", ctypes.c_int32),
     ]
 
 
@@ -97,11 +97,11 @@ def _stream(stream=None):
 
 def make_params(*, batch, seq_len, q_heads, kv_heads, key_dim, value_dim, io_dtype=torch.bfloat16,
                 out_dtype=None, feature_map="elu_plus_one", use_normalizer=True, epsilon=1e-6,
-                scale=1.0, update_rule="linear") -> la_params:
+                scale=1.0, update_rule="linear", decay_per_key_dim=False) -> la_params:
     out_dtype = io_dtype if out_dtype is None else out_dtype
     return la_params(batch, seq_len, q_heads, kv_heads, key_dim, value_dim, _DTYPES[io_dtype],
                      _DTYPES[out_dtype], FEATURE_MAPS[feature_map], int(bool(use_normalizer)),
-                     float(epsilon), float(scale), UPDATE_RULES[update_rule], 0)
+                     float(epsilon), float(scale), UPDATE_RULES[update_rule], int(bool(decay_per_key_dim)))
 
 
 def _as_bthd(x, heads, name):
@@ -116,7 +116,7 @@ def _as_bthd(x, heads, name):
     return x
 
 
-def _prep(q, k, v, q_heads, kv_heads, **kw):
+def _prep(q, k, v, q_heads, kv_heads, decay=None, **kw):
     q = _as_bthd(q, q_heads, "q")
     k = _as_bthd(k, kv_heads, "k")
     v = _as_bthd(v, kv_heads, "v")
@@ -125,8 +125,15 @@ def _prep(q, k, v, q_heads, kv_heads, **kw):
     B, T, _, Dk = q.shape
     if k.shape[:2] != (B, T) or v.shape[:2] != (B, T) or k.shape[3] != Dk:
         raise ValueError("q, k, v shapes disagree")
+    per_dim = False
+    if decay is not None:
+        # ONNX decay layouts: (B, T, H_kv) per head, (B, T, H_kv*d_k) per key dimension
+        if decay.numel() == B * T * kv_heads * Dk and Dk > 1:
+            per_dim = True
+        elif decay.numel() != B * T * kv_heads:
+            raise ValueError(f"decay must have B*T*Hkv or B*T*Hkv*Dk elements, got {tuple(decay.shape)}")
     p = make_params(batch=B, seq_len=T, q_heads=q_heads, kv_heads=kv_heads, key_dim=Dk,
-                    value_dim=v.shape[3], io_dtype=q.dtype, **kw)
+                    value_dim=v.shape[3], io_dtype=q.dtype, decay_per_key_dim=per_dim, **kw)
     return q, k, v, p
 
 
@@ -178,7 +185,7 @@ def la_forward_causal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one",
     state and output zero (la_forward_causal_masked)."""
     q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=out_dtype, feature_map=feature_map,
                        use_normalizer=use_normalizer, epsilon=epsilon, scale=scale,
-                       update_rule=update_rule)
+                       update_rule=update_rule, decay=decay)
     B, T, _, Dk = q.shape
     Dv = v.shape[3]
     ydt = q.dtype if out_dtype is None else out_dtype
@@ -215,7 +222,7 @@ def la_forward_causal_noalloc(q, k, v, *, q_heads, kv_heads, feature_map="elu_pl
     that may overlap on one device race on the shared scratch."""
     q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=out.dtype, feature_map=feature_map,
                        use_normalizer=use_normalizer, epsilon=epsilon, scale=scale,
-                       update_rule=update_rule)
+                       update_rule=update_rule, decay=decay)
     if decay is not None and (not decay.is_cuda or not decay.is_contiguous() or decay.dtype != q.dtype):
         raise ValueError("decay must be a contiguous CUDA tensor of the io dtype")
     S0, Z0 = initial_state if initial_state is not None else (None, None)
@@ -253,7 +260,7 @@ def la_decode_step(q, k, v, S, Z=None, *, q_heads, kv_heads, feature_map="elu_pl
     ``mask`` (B,) or (B,1): a sequence whose step is invalid keeps S, Z and outputs zero."""
     q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=out_dtype, feature_map=feature_map,
                        use_normalizer=use_normalizer, epsilon=epsilon, scale=scale,
-                       update_rule=update_rule)
+                       update_rule=update_rule, decay=decay)
     ydt = q.dtype if out_dtype is None else out_dtype
     y = out if out is not None else torch.empty(q.shape[0], 1, q_heads, v.shape[3], dtype=ydt,
                                                 device=q.device)

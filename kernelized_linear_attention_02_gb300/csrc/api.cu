@@ -65,7 +65,10 @@ la_status make_problem(const la_params* p, Call call, la::Problem* P) {
     if (!std::isfinite(p->scale)) return fail(LA_ERR_INVALID_ARG, "scale must be finite");
     if (p->update_rule != LA_RULE_LINEAR && p->update_rule != LA_RULE_GATED)
         return fail(LA_ERR_INVALID_ARG, "unknown update_rule %d", p->update_rule);
-    if (p->reserved != 0) return fail(LA_ERR_INVALID_ARG, "reserved must be 0");
+    if (p->decay_per_key_dim != 0 && p->decay_per_key_dim != 1)
+        return fail(LA_ERR_INVALID_ARG, "decay_per_key_dim must be 0 or 1");
+    if (p->decay_per_key_dim && p->update_rule != LA_RULE_GATED)
+        return fail(LA_ERR_INVALID_ARG, "decay_per_key_dim needs the gated rule");
     if (p->update_rule == LA_RULE_GATED && (p->feature_map != LA_FMAP_NONE || p->use_normalizer))
         return fail(LA_ERR_UNSUPPORTED, "the gated rule is defined without a feature map or normalizer");
     if (call == Call::kNonCausal && p->update_rule != LA_RULE_LINEAR)
@@ -85,6 +88,7 @@ la_status make_problem(const la_params* p, Call call, la::Problem* P) {
     P->fmap = p->feature_map;
     P->norm = p->use_normalizer;
     P->gated = p->update_rule == LA_RULE_GATED;
+    P->decay_dim = p->decay_per_key_dim;
     P->eps = p->epsilon;
     P->scale = p->scale == 0.f ? 1.f / std::sqrt((float)p->key_dim) : p->scale;
     return LA_OK;
@@ -203,7 +207,9 @@ la_status la_forward_causal_masked(const la_params* p, const void* q, const void
     if (P.gated && !decay) return fail(LA_ERR_INVALID_ARG, "the gated rule needs decay");
     if ((st = check_ws(P, true, ws, ws_bytes)) != LA_OK) return st;
     cudaError_t e;
-    if (la::chunk_supported(P) && la::chunk_pointers_ok(q, k, v, y))
+    // per-key-dimension decay: the CUDA-core recurrence (the chunk kernel
+    // factors one decay per kv head)
+    if (!P.decay_dim && la::chunk_supported(P) && la::chunk_pointers_ok(q, k, v, y))
         e = la::chunk_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, ws, s);
     else
         e = la::recurrent_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, s);

@@ -18,6 +18,7 @@ struct Problem {
     int Hq, Hkv, G, Dk, Dv;
     int io_bf16, out_bf16;
     int fmap, norm, gated;
+    int decay_dim;  // gated: decay per key dimension (B, T, Hkv, Dk) instead of per head
     float eps, scale;
     // (B, T) sequence-validity mask, nonzero = valid; null = every step valid
     const uint8_t* mask = nullptr;

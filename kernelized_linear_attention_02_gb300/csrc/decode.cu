@@ -92,18 +92,21 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
         zs[tid] = z;
         a.Z[bh * Dk + tid] = z;
     }
-    const float dec = P.gated ? __expf(load_in(static_cast<const TIn*>(a.decay), bh)) : 1.f;
+    const TIn* dg = static_cast<const TIn*>(a.decay);
+    const float dec = P.gated && !P.decay_dim ? __expf(load_in(dg, bh)) : 1.f;
 
-    // S <- dec * S + phi(k) (x) v, written back in place
+    // S <- dec * S + phi(k) (x) v, written back in place (per-key-dimension
+    // decay: row i scaled by its own exp(g_i))
     const float4 v4 = colok ? reinterpret_cast<const float4*>(vv)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < kRows; ++m) {
         const int i = warp + 8 * m;
         const float f = i < Dk ? fk[i] : 0.f;
-        s[m].x = fmaf(f, v4.x, dec * s[m].x);
-        s[m].y = fmaf(f, v4.y, dec * s[m].y);
-        s[m].z = fmaf(f, v4.z, dec * s[m].z);
-        s[m].w = fmaf(f, v4.w, dec * s[m].w);
+        const float di = P.gated && P.decay_dim && i < Dk ? __expf(load_in(dg, bh * Dk + i)) : dec;
+        s[m].x = fmaf(f, v4.x, di * s[m].x);
+        s[m].y = fmaf(f, v4.y, di * s[m].y);
+        s[m].z = fmaf(f, v4.z, di * s[m].z);
+        s[m].w = fmaf(f, v4.w, di * s[m].w);
         if (i < Dk && colok) __stcs(Srow + (int64_t)i * nvec + lane, s[m]);
     }
     __syncthreads();  // zs complete
@@ -243,18 +246,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             zs[tid] = z;
             a.Z[u * Dk + tid] = z;
         }
-        const float dec = P.gated ? __expf(load_in(static_cast<const TIn*>(a.decay), u)) : 1.f;
-        // S <- dec * S + phi(k) (x) v, written back into the stage
+        const TIn* dg = static_cast<const TIn*>(a.decay);
+        const float dec = P.gated && !P.decay_dim ? __expf(load_in(dg, u)) : 1.f;
+        // S <- dec * S + phi(k) (x) v, written back into the stage (row i
+        // scaled by its own exp(g_i) with the per-key-dimension decay)
         const float4 v4 = colok ? reinterpret_cast<const float4*>(vv)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
         if (valid) {
 #pragma unroll
             for (int m = 0; m < kRows; ++m) {
                 const int i = warp + 8 * m;
                 const float f = i < Dk ? fk[i] : 0.f;
-                s[m].x = fmaf(f, v4.x, dec * s[m].x);
-                s[m].y = fmaf(f, v4.y, dec * s[m].y);
-                s[m].z = fmaf(f, v4.z, dec * s[m].z);
-                s[m].w = fmaf(f, v4.w, dec * s[m].w);
+                const float di = P.gated && P.decay_dim && i < Dk ? __expf(load_in(dg, u * Dk + i)) : dec;
+                s[m].x = fmaf(f, v4.x, di * s[m].x);
+                s[m].y = fmaf(f, v4.y, di * s[m].y);
+                s[m].z = fmaf(f, v4.z, di * s[m].z);
+                s[m].w = fmaf(f, v4.w, di * s[m].w);
                 if (i < Dk && colok) Ss[i * nvec + lane] = s[m];
             }
         }

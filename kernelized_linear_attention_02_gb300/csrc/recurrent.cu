@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(RecArgs a) {
         __syncthreads();
 
         if (update) {
-            const float dec = P.gated ? expf(load_in(decay, tok * P.Hkv + hk)) : 1.f;
+            // decay of this step: one per kv head, or one per key dimension (row of S)
+            const float dec = P.gated && !P.decay_dim ? expf(load_in(decay, tok * P.Hkv + hk)) : 1.f;
             float vj[kColsPerThread];
 #pragma unroll
             for (int n = 0; n < kColsPerThread; ++n) {
@@ -110,8 +111,9 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(RecArgs a) {
             for (int m = 0; m < kRowsPerThread; ++m) {
                 const int i = warp + 8 * m;
                 const float f = i < Dk ? fk[i] : 0.f;
+                const float di = P.gated && P.decay_dim && i < Dk ? expf(load_in(decay, (tok * P.Hkv + hk) * Dk + i)) : dec;
 #pragma unroll
-                for (int n = 0; n < kColsPerThread; ++n) s[m][n] = fmaf(f, vj[n], dec * s[m][n]);
+                for (int n = 0; n < kColsPerThread; ++n) s[m][n] = fmaf(f, vj[n], di * s[m][n]);
             }
             if (P.norm && tid < Dk) Zs[tid] += fk[tid];
         }

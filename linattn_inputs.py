@@ -37,6 +37,7 @@ class Workload:
     decay_mu: float = 4.0     # gated: g = log(sigmoid(x)), x ~ N(decay_mu, 1)
     seed: int = 0
     mask: str = ""            # "" (no mask) or a validity_mask kind, e.g. "right"
+    decay_per_dim: bool = False  # gated: decay (B,T,Hkv,Dk) per key dimension instead of (B,T,Hkv)
 
 
 TINY = Workload("tiny_B1_H2_T64_D16_f32", 1, 64, 2, 2, 16, 16, torch.float32,
@@ -60,7 +61,13 @@ ONNX_GATED = dataclasses.replace(ONNX_LINEAR, name="onnx_gated_gqa_B2_T32768_Hq3
 # L_b steps, L_b uniform in [T/2, T] (Keras request, Masking: right padding)
 PREFILL_2K_RIGHTPAD = dataclasses.replace(PREFILL_2K, name=PREFILL_2K.name + "_rightpad_mask", mask="right")
 
-ALL = [TINY, PREFILL_2K, LONG_8K, LONG_8K_UNNORM, DECODE, ONNX_LINEAR, ONNX_GATED, PREFILL_2K_RIGHTPAD]
+# the gated rule with one log decay per key dimension (ONNX decay layout
+# (B, T, H_kv*d_k)), on a shorter sequence: it runs on the CUDA-core recurrence
+GATED_PERDIM = dataclasses.replace(ONNX_GATED, name="gated_perdim_gqa_B2_T4096_Hq32_Hkv8_D128_bf16", T=4096,
+                                   decay_per_dim=True)
+
+ALL = [TINY, PREFILL_2K, LONG_8K, LONG_8K_UNNORM, DECODE, ONNX_LINEAR, ONNX_GATED, PREFILL_2K_RIGHTPAD,
+       GATED_PERDIM]
 
 MASK_KINDS = ("right", "left", "gaps", "random", "none_valid", "all_valid")
 
@@ -83,7 +90,8 @@ def normal(shape, gen: torch.Generator, std=1.0, mean=0.0, dtype=torch.float32, 
 
 def make_qkv(w: Workload, device="cpu", T=None, B=None, seed=None):
     """q (B,T,Hq,Dk), k (B,T,Hkv,Dk), v (B,T,Hkv,Dv) and, for the gated rule,
-    decay (B,T,Hkv) -- contiguous, the packed [B,T,H*D] memory of the ONNX op.
+    decay (B,T,Hkv) (or (B,T,Hkv,Dk) per key dimension) -- contiguous, the
+    packed [B,T,H*D] memory of the ONNX op.
 
     Draw order q, k, v, decay.  Keys are L2-normalised over Dk in fp32 before
     rounding when the workload asks for it (the ONNX page recommends
@@ -100,8 +108,8 @@ def make_qkv(w: Workload, device="cpu", T=None, B=None, seed=None):
     v = normal((B, T, w.kv_heads, w.Dv), g, w.v_std, dtype=w.dtype, device=device)
     decay = None
     if w.rule == "gated":
-        x = normal((B, T, w.kv_heads), g, 1.0, mean=w.decay_mu, dtype=torch.float32,
-                   device=device)
+        dshape = (B, T, w.kv_heads, w.Dk) if w.decay_per_dim else (B, T, w.kv_heads)
+        x = normal(dshape, g, 1.0, mean=w.decay_mu, dtype=torch.float32, device=device)
         decay = torch.nn.functional.logsigmoid(x).to(w.dtype)
     return q, k, v, decay
 

@@ -82,7 +82,7 @@ def test_bad_enum_values(L):
     p.feature_map = 9
     assert L.la_forward_causal(ctypes.byref(p), *([None] * 10), 0, None) == la.LA_ERR_INVALID_ARG
     p = _p()
-    p.reserved = 1
+    p.decay_per_key_dim = 1  # needs the gated rule
     assert L.la_forward_causal(ctypes.byref(p), *([None] * 10), 0, None) == la.LA_ERR_INVALID_ARG
 
 
