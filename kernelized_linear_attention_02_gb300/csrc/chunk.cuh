@@ -272,13 +272,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Validity of the steps t0 .. t0 + 63 of this sequence as a 64-bit word
     // (Keras request, Masking; steps past T count as valid, they are cut
     // elsewhere).  Warp-collective: two loads per lane and two ballots.
-    auto valid_word = [&](int t0) -> uint64_t {
-        if (!mask) return ~0ull;
+    // The mask bytes of steps t0 + lane and t0 + 32 + lane (1 past the end),
+    // loaded ahead of use; valid_bits turns them into the word.
+    auto mask_bytes = [&](int t0) -> uint32_t {
+        if (!mask) return 0x101u;
         const size_t bt = (size_t)b * T + t0;
-        const bool v0 = t0 + lane >= T || mask[bt + lane] != 0;
-        const bool v1 = t0 + 32 + lane >= T || mask[bt + 32 + lane] != 0;
-        return (uint64_t)__ballot_sync(0xffffffffu, v0) | ((uint64_t)__ballot_sync(0xffffffffu, v1) << 32);
+        const uint32_t m0 = t0 + lane >= T ? 1u : mask[bt + lane];
+        const uint32_t m1 = t0 + 32 + lane >= T ? 1u : mask[bt + 32 + lane];
+        return (m0 != 0) | ((m1 != 0) << 8);
     };
+    auto valid_bits = [&](uint32_t mb) -> uint64_t {
+        if (!mask) return ~0ull;
+        return (uint64_t)__ballot_sync(0xffffffffu, mb & 0xffu) | ((uint64_t)__ballot_sync(0xffffffffu, mb >> 8) << 32);
+    };
+    auto valid_word = [&](int t0) -> uint64_t { return valid_bits(mask_bytes(t0)); };
 
     auto Kb = [&](int s) { return kv_base + s * Cf::kKvStage; };
     auto Kd = [&](int s) { return kv_base + s * Cf::kKvStage + Cf::kOffKd; };
@@ -1180,11 +1187,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (NORM && ct < D && MODE == kApply) start_z();
 
         // ---- keys of chunk i: feature map (+ lo part), decayed keys, Z rows and sums
+        // mask bytes of the next chunk, loaded one chunk ahead (their latency
+        // hides behind the wait for that chunk's tiles)
+        uint32_t mb_next = mask_bytes(c_begin * kC);
         auto process_kv = [&](int i) -> bool {
             const int s = i % NKV1;
             const int t0 = (c_begin + i) * kC;
             const int valid = min(kC, T - t0);
+            const uint32_t mb = mb_next;
+            if (mask && i + 1 < nck) mb_next = mask_bytes(t0 + kC);
             if (!warp_wait(&full_kv[s], (i / NKV1) & 1, err, kErrFullKV)) return false;
+            // invalid steps (mask): their phi(k) and v rows become zero, so
+            // they add nothing to the state, the key sum or any score
+            const uint64_t okw = valid_bits(mb);
             if (ct == 0) LA_TR(2, 1, i);
             float* gc = Gc(s);
             float gtot = 0.f;
@@ -1194,9 +1209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float g0 = 0.f, g1 = 0.f;
                     const int j0 = 2 * ct, j1 = 2 * ct + 1;
                     // an invalid step (mask) keeps the state: no decay either
-                    if (j0 < valid && step_valid(mask, (size_t)b * T + t0 + j0))
+                    if (j0 < valid && ((okw >> j0) & 1))
                         g0 = __bfloat162float(decay[((size_t)b * T + t0 + j0) * Hkv + hk]);
-                    if (j1 < valid && step_valid(mask, (size_t)b * T + t0 + j1))
+                    if (j1 < valid && ((okw >> j1) & 1))
                         g1 = __bfloat162float(decay[((size_t)b * T + t0 + j1) * Hkv + hk]);
                     const float sum = g0 + g1;
                     float incl = sum;
@@ -1229,9 +1244,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
                 gtot = gc[kC - 1];
             }
-            // invalid steps (mask): their phi(k) and v rows become zero, so
-            // they add nothing to the state, the key sum or any score
-            const uint64_t okw = valid_word(t0);
             const bool touch = GATED || SPLITK || NORM || fmap != LA_FMAP_NONE || mask;
             if (ct == 0) LA_TR(2, 7, i);
             if (touch) {

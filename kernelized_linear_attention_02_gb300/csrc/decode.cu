@@ -18,6 +18,8 @@
 // A sequence-validity mask (Keras request, Masking) makes a sequence's step
 // invalid: its state and key sum are left exactly as they were and its
 // outputs are zero.  The decision is per batch row, uniform across a CTA.
+// The mask and the per-key-dimension decay are compiled into separate
+// instantiations (EXT); the plain step carries no code for either.
 #include <algorithm>
 
 #include "common.cuh"
@@ -43,9 +45,11 @@ struct DecArgs {
     Problem P;
 };
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool EXT>
 __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
     const Problem& P = a.P;
+    const uint8_t* mask = EXT ? P.mask : nullptr;     // sequence-validity mask
+    const bool decay_dim = EXT && P.gated && P.decay_dim;  // decay per key dimension
     const int Dk = P.Dk, Dv = P.Dv, G = P.G;
     extern __shared__ float smem[];
     float* fk = smem;                  // [128]
@@ -82,7 +86,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
         fq[idx] = phi<true>(P.fmap, load_in(q, (b * P.Hq + hk * G + r) * Dk + i), P.eps);
     }
     __syncthreads();
-    const bool valid = step_valid(P.mask, b);
+    const bool valid = step_valid(mask, b);
     if (!valid) {  // state untouched, zero outputs
         for (int idx = tid; idx < G * Dv; idx += kThreads) store_out(y, (b * P.Hq + hk * G) * Dv + idx, 0.f);
         return;
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
         a.Z[bh * Dk + tid] = z;
     }
     const TIn* dg = static_cast<const TIn*>(a.decay);
-    const float dec = P.gated && !P.decay_dim ? __expf(load_in(dg, bh)) : 1.f;
+    const float dec = P.gated && !decay_dim ? __expf(load_in(dg, bh)) : 1.f;
 
     // S <- dec * S + phi(k) (x) v, written back in place (per-key-dimension
     // decay: row i scaled by its own exp(g_i))
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecArgs a) {
     for (int m = 0; m < kRows; ++m) {
         const int i = warp + 8 * m;
         const float f = i < Dk ? fk[i] : 0.f;
-        const float di = P.gated && P.decay_dim && i < Dk ? __expf(load_in(dg, bh * Dk + i)) : dec;
+        const float di = decay_dim && i < Dk ? __expf(load_in(dg, bh * Dk + i)) : dec;
         s[m].x = fmaf(f, v4.x, di * s[m].x);
         s[m].y = fmaf(f, v4.y, di * s[m].y);
         s[m].z = fmaf(f, v4.z, di * s[m].z);
@@ -164,10 +168,12 @@ struct StreamLayout {
 
 using namespace umma;
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_stream_kernel(DecArgs a, StreamLayout ly, int nunits, unsigned* err) {
     const Problem& P = a.P;
+    const uint8_t* mask = EXT ? P.mask : nullptr;     // sequence-validity mask
+    const bool decay_dim = EXT && P.gated && P.decay_dim;  // decay per key dimension
     const int Dk = P.Dk, Dv = P.Dv, G = P.G, nst = ly.nst;
     extern __shared__ __align__(128) uint8_t dsm[];
     uint8_t* stages = dsm;
@@ -240,14 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         // an invalid step (mask) keeps the stage as loaded: the store below
         // then writes the state back unchanged
-        const bool valid = step_valid(P.mask, b);
+        const bool valid = step_valid(mask, b);
         if (valid && P.norm && tid < Dk) {
             const float z = reinterpret_cast<const float*>(st + ly.z)[tid] + fk[tid];
             zs[tid] = z;
             a.Z[u * Dk + tid] = z;
         }
         const TIn* dg = static_cast<const TIn*>(a.decay);
-        const float dec = P.gated && !P.decay_dim ? __expf(load_in(dg, u)) : 1.f;
+        const float dec = P.gated && !decay_dim ? __expf(load_in(dg, u)) : 1.f;
         // S <- dec * S + phi(k) (x) v, written back into the stage (row i
         // scaled by its own exp(g_i) with the per-key-dimension decay)
         const float4 v4 = colok ? reinterpret_cast<const float4*>(vv)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -256,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int m = 0; m < kRows; ++m) {
                 const int i = warp + 8 * m;
                 const float f = i < Dk ? fk[i] : 0.f;
-                const float di = P.gated && P.decay_dim && i < Dk ? __expf(load_in(dg, u * Dk + i)) : dec;
+                const float di = decay_dim && i < Dk ? __expf(load_in(dg, u * Dk + i)) : dec;
                 s[m].x = fmaf(f, v4.x, di * s[m].x);
                 s[m].y = fmaf(f, v4.y, di * s[m].y);
                 s[m].z = fmaf(f, v4.z, di * s[m].z);
@@ -318,12 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) bulk_wait_group<0>();
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool EXT>
 cudaError_t launch(const DecArgs& a, cudaStream_t st) {
     const Problem& P = a.P;
     const size_t smem = sizeof(float) * (5 * 128 + (((size_t)P.G * P.Dk + 3) & ~(size_t)3)) +
                         sizeof(float4) * kHeadBlock * 8 * 32;
-    auto kern = decode_kernel<TIn, TOut>;
+    auto kern = decode_kernel<TIn, TOut, EXT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<dim3((unsigned)(P.B * P.Hkv)), kThreads, smem, st>>>(a);
@@ -360,13 +366,13 @@ StreamLayout stream_layout(const Problem& P, const void* q, const void* k, const
     return ly;
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool EXT>
 cudaError_t launch_stream(const DecArgs& a, const StreamLayout& ly, cudaStream_t st) {
     const int nunits = (int)(a.P.B * a.P.Hkv);
     const int sms = device_sm_count();
     unsigned* err = device_error_word();
     if (sms <= 0 || !err) return cudaErrorInvalidDevice;
-    auto kern = decode_stream_kernel<TIn, TOut>;
+    auto kern = decode_stream_kernel<TIn, TOut, EXT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ly.smem);
     if (e != cudaSuccess) return e;
     kern<<<dim3((unsigned)std::min(nunits, sms)), kThreads, ly.smem, st>>>(a, ly, nunits, err);
@@ -378,19 +384,28 @@ cudaError_t launch_stream(const DecArgs& a, const StreamLayout& ly, cudaStream_t
 
 bool decode_supported(const Problem& P) { return P.Dk <= 128 && P.Dv <= 128 && P.Dv % 4 == 0; }
 
+template <bool EXT>
+cudaError_t decode_dispatch(const DecArgs& a, const StreamLayout& ly, cudaStream_t st) {
+    const Problem& P = a.P;
+    if (ly.nst) {  // state streamed through shared memory (bulk async copies)
+        if (P.io_bf16)
+            return P.out_bf16 ? launch_stream<__nv_bfloat16, __nv_bfloat16, EXT>(a, ly, st)
+                              : launch_stream<__nv_bfloat16, float, EXT>(a, ly, st);
+        return P.out_bf16 ? launch_stream<float, __nv_bfloat16, EXT>(a, ly, st)
+                          : launch_stream<float, float, EXT>(a, ly, st);
+    }
+    if (P.io_bf16)
+        return P.out_bf16 ? launch<__nv_bfloat16, __nv_bfloat16, EXT>(a, st) : launch<__nv_bfloat16, float, EXT>(a, st);
+    return P.out_bf16 ? launch<float, __nv_bfloat16, EXT>(a, st) : launch<float, float, EXT>(a, st);
+}
+
 cudaError_t decode_step(const Problem& P, const void* q, const void* k, const void* v,
                         const void* decay, float* S, float* Z, void* y, cudaStream_t st) {
     DecArgs a{q, k, v, decay, S, Z, y, P};
     const StreamLayout ly = stream_layout(P, q, k, v, S, Z);
-    if (ly.nst) {  // state streamed through shared memory (bulk async copies)
-        if (P.io_bf16)
-            return P.out_bf16 ? launch_stream<__nv_bfloat16, __nv_bfloat16>(a, ly, st)
-                              : launch_stream<__nv_bfloat16, float>(a, ly, st);
-        return P.out_bf16 ? launch_stream<float, __nv_bfloat16>(a, ly, st) : launch_stream<float, float>(a, ly, st);
-    }
-    if (P.io_bf16)
-        return P.out_bf16 ? launch<__nv_bfloat16, __nv_bfloat16>(a, st) : launch<__nv_bfloat16, float>(a, st);
-    return P.out_bf16 ? launch<float, __nv_bfloat16>(a, st) : launch<float, float>(a, st);
+    // a mask or a per-key-dimension decay: the instantiations that read them
+    if (P.mask || (P.gated && P.decay_dim)) return decode_dispatch<true>(a, ly, st);
+    return decode_dispatch<false>(a, ly, st);
 }
 
 }  // namespace la
