@@ -354,9 +354,9 @@ def workload_sweep(la, steps, warmup, stream, hbm_gbs):
     read once and y written once (plus one mask byte per step for the
     masked workload, whose tokens/s counts padded steps too)."""
     out = []
-    cases = [(inputs.PREFILL_2K, True), (inputs.LONG_8K, True), (inputs.LONG_8K_UNNORM, True),
-             (inputs.LONG_8K, False), (inputs.LONG_8K_UNNORM, False), (inputs.ONNX_LINEAR, True),
-             (inputs.ONNX_GATED, True), (inputs.PREFILL_2K_RIGHTPAD, True), (inputs.GATED_PERDIM, True)]
+    cases = [(inputs.PREFILL_2K, True), (inputs.PREFILL_2K_RIGHTPAD, True), (inputs.LONG_8K, True),
+             (inputs.LONG_8K_UNNORM, True), (inputs.LONG_8K, False), (inputs.LONG_8K_UNNORM, False),
+             (inputs.ONNX_LINEAR, True), (inputs.ONNX_GATED, True), (inputs.GATED_PERDIM, True)]
     for w, causal in cases:
         ms, lpc = time_workload(la, w, steps, warmup, stream, causal)
         alg = prefill_alg_bytes(w)
