@@ -98,7 +98,7 @@ size_t state_bytes(const la::Problem& P) { return sizeof(float) * (size_t)P.B * 
 size_t key_state_bytes(const la::Problem& P) { return sizeof(float) * (size_t)P.B * P.Hkv * P.Dk; }
 
 size_t workspace_bytes(const la::Problem& P, bool causal) {
-    const size_t rec = causal ? 0 : round_up(state_bytes(P)) + round_up(key_state_bytes(P));
+    const size_t rec = causal ? la::recurrent_workspace_bytes(P) : round_up(state_bytes(P)) + round_up(key_state_bytes(P));
     if (!la::chunk_supported(P)) return rec;
     return std::max(rec, la::chunk_workspace_bytes(P, causal));
 }
@@ -212,7 +212,7 @@ la_status la_forward_causal_masked(const la_params* p, const void* q, const void
     if (!P.decay_dim && la::chunk_supported(P) && la::chunk_pointers_ok(q, k, v, y))
         e = la::chunk_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, ws, s);
     else
-        e = la::recurrent_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, s);
+        e = la::recurrent_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, s, ws, ws_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal");
     g_last_error.clear();
     return LA_OK;

@@ -9,9 +9,13 @@ namespace la {
 
 // CUDA-core recurrence (recurrent.cu): float32 path and uncovered shapes.
 size_t recurrent_smem_bytes(const Problem& P);
+// Scratch the causal recurrence uses to split a long sequence into segments
+// (0: one segment); without it (ws null or too small) it runs unsplit.
+size_t recurrent_workspace_bytes(const Problem& P);
 cudaError_t recurrent_causal(const Problem& P, const void* q, const void* k, const void* v,
                              const void* decay, const float* S0, const float* Z0, void* y,
-                             float* S_out, float* Z_out, cudaStream_t st);
+                             float* S_out, float* Z_out, cudaStream_t st, void* ws = nullptr,
+                             size_t ws_bytes = 0);
 cudaError_t recurrent_noncausal(const Problem& P, const void* q, const void* k, const void* v,
                                 void* y, float* S_ws, float* Z_ws, cudaStream_t st);
 
