@@ -407,6 +407,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
     };
     constexpr bool kQOnEpi = MODE == kCausal && !GATED && !split;
+    // Warp w runs on sub-partition w % 4.  Without the split issue, warp 13
+    // would share the MMA warp's sub-partition (that of warp 1) with two other
+    // busy warps, so the fourth feature warp (they use no TMEM lanes) moves to
+    // the otherwise idle warp 14 and warp 13 idles.
+    constexpr bool kFeatMove = MODE == kCausal && !split;
+    constexpr int kIdleWarp = kFeatMove ? 13 : kMmaSWarp;
 
     // Output of item m (query head m % G of chunk m / G): Y^T from TMEM times
     // scale/den, stored to global memory.  Run by four warps, one per TMEM lane
@@ -1072,7 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the next query item, while the tensor core runs this item's products
             if (kQOnEpi && ok && n + 1 < n_total) ok = q_features((n + 1) / G, n + 1, et);
         }
-    } else if (warp == kMmaSWarp) {
+    } else if (warp == kIdleWarp) {
         // ------------------------------------------------ MMA issuer of the state
         // (split issue only): per chunk, the read-out of every query head with
         // the carried fp32 state (kind::tf32, state from TMEM as A), then the
@@ -1140,7 +1146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rule, the Z rows of every chunk and the running key sum Z.  Runs
         // ahead of the state chain, limited only by the load rings.
         constexpr int kCPR = Cf::kCPR, kRowStep = Cf::kRowStep, kPer = Cf::kPer;
-        const int ct = tid - Cf::kFeatW0 * 32;  // 0 .. kFeatThreads - 1
+        const int fwarp = kFeatMove && warp == kMmaSWarp ? 13 : warp;  // feature warp slot
+        const int ct = (fwarp - Cf::kFeatW0) * 32 + lane;                 // 0 .. kFeatThreads - 1
         const int cc = ct % kCPR;              // 16-byte chunk column: features 8cc..8cc+7
         const int rbase = ct / kCPR;           // rows rbase + kRowStep * m
         bool ok = true;
