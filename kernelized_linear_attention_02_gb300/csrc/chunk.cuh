@@ -64,8 +64,10 @@ constexpr int kC = 64;  // tokens per chunk
 // per-stage decay block (gated rule), floats: [0, 64) inclusive cumulative log
 // decay G_j, [64, 128) exp(ref - G_j), then ref and the "factored" flag
 constexpr int kGCol = 64, kGRef = 128, kGFlag = 129;
-constexpr int kThreads = 480;
-constexpr int kStateWarp0 = 2, kEpiWarp0 = 6, kFeatWarp0 = 10, kMmaSWarp = 14;
+constexpr int kThreads = 480;  // 15 warps; the two-issuer kernel adds warp 15
+template <bool SPLIT>
+constexpr int block_threads() { return SPLIT ? 512 : kThreads; }
+constexpr int kStateWarp0 = 2, kEpiWarp0 = 6, kFeatWarp0 = 10, kMmaSWarp = 14;  // warp 15: see kFeatMovedTo
 
 template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16>
 struct Cfg {
@@ -201,7 +203,7 @@ __device__ __forceinline__ __nv_bfloat16& bf_at(uint8_t* base, uint32_t off) {
 // constant null and every mask branch folds away, so unmasked calls run
 // exactly the code they would run without mask support.
 template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16, bool SPLIT = false, bool MASK = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>::kSplitMma && SPLIT>(), 1)
     chunk_kernel(const __grid_constant__ Args a, const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                  const __grid_constant__ CUtensorMap mapV) {
     using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>;
@@ -407,12 +409,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
     };
     constexpr bool kQOnEpi = MODE == kCausal && !GATED && !split;
-    // Warp w runs on sub-partition w % 4.  Without the split issue, warp 13
-    // would share the MMA warp's sub-partition (that of warp 1) with two other
-    // busy warps, so the fourth feature warp (they use no TMEM lanes) moves to
-    // the otherwise idle warp 14 and warp 13 idles.
-    constexpr bool kFeatMove = MODE == kCausal && !split;
-    constexpr int kIdleWarp = kFeatMove ? 13 : kMmaSWarp;
+    // Warp w runs on sub-partition w % 4.  In the causal pass, feature warp
+    // slot 3 (warp 13) would share the MMA warp's sub-partition (that of warp
+    // 1) with two other busy warps, so it moves: to warp 14 when there is no
+    // second MMA issuer, else to warp 15 (the feature warps use no TMEM lanes
+    // and may run anywhere).  Warp 13, and the warps no role claims, idle.
+    constexpr bool kFeatMove = MODE == kCausal;
+    constexpr int kFeatMovedTo = split ? 15 : 14;
+    constexpr int kIdleWarp = (MODE == kCausal && !split) ? 13 : kMmaSWarp;  // or the second issuer
 
     // Output of item m (query head m % G of chunk m / G): Y^T from TMEM times
     // scale/den, stored to global memory.  Run by four warps, one per TMEM lane
@@ -1139,15 +1143,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(final_done, lead);  // every operation of this warp complete
         }
-    } else {
+    } else if (!split || warp != 13) {
         // ------------------------------------------------------ feature warps
         // Feature maps of keys and queries in shared memory (bf16 hi, lo part
         // of the keys for the state update), decayed copies for the gated
         // rule, the Z rows of every chunk and the running key sum Z.  Runs
         // ahead of the state chain, limited only by the load rings.
         constexpr int kCPR = Cf::kCPR, kRowStep = Cf::kRowStep, kPer = Cf::kPer;
-        const int fwarp = kFeatMove && warp == kMmaSWarp ? 13 : warp;  // feature warp slot
-        const int ct = (fwarp - Cf::kFeatW0) * 32 + lane;                 // 0 .. kFeatThreads - 1
+        const int fslot = kFeatMove && warp == kFeatMovedTo ? 13 - Cf::kFeatW0 : warp - Cf::kFeatW0;
+        const int ct = fslot * 32 + lane;  // 0 .. kFeatThreads - 1
         const int cc = ct % kCPR;              // 16-byte chunk column: features 8cc..8cc+7
         const int rbase = ct / kCPR;           // rows rbase + kRowStep * m
         bool ok = true;

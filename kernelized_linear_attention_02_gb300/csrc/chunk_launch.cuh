@@ -27,7 +27,7 @@ cudaError_t run_one(const Launch& L, cudaStream_t st) {
         // the kernel waits for it (griddepcontrol.wait) before reading its output
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = L.grid;
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(block_threads<Cf::kSplitMma && SPLIT>());
         cfg.dynamicSmemBytes = Cf::kSmem;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -38,7 +38,7 @@ cudaError_t run_one(const Launch& L, cudaStream_t st) {
         e = cudaLaunchKernelEx(&cfg, kern, L.args, L.mq, L.mk, L.mv);
         if (e != cudaSuccess) return e;
     } else {
-        kern<<<L.grid, kThreads, Cf::kSmem, st>>>(L.args, L.mq, L.mk, L.mv);
+        kern<<<L.grid, block_threads<Cf::kSplitMma && SPLIT>(), Cf::kSmem, st>>>(L.args, L.mq, L.mk, L.mv);
     }
     note_launch();
     return cudaGetLastError();
