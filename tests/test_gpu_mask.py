@@ -247,3 +247,20 @@ def test_mask_argument_checks():
         la.la_forward_causal(q, q, q, q_heads=2, kv_heads=2, mask=torch.ones(2, 7, dtype=torch.bool, device=DEV))
     with pytest.raises(ValueError):
         la.la_forward_causal(q, q, q, q_heads=2, kv_heads=2, mask=torch.ones(2, 8, dtype=torch.float32, device=DEV))
+
+
+@pytest.mark.parametrize("shape", [(1, 3001, 2, 2, 64, 64), (2, 2600, 4, 2, 128, 128)], ids=ids)
+@pytest.mark.parametrize("kind", ["gaps", "left"])
+def test_noncausal_masked_segments(shape, kind):
+    """Long non-causal calls with few streams: the global state is reduced over
+    sequence segments, and invalid runs cross their boundaries."""
+    B, T, Hq, Hkv, Dk, Dv = shape
+    q = rand((B, T, Hq, Dk), 71, torch.bfloat16, 0.5)
+    k = rand((B, T, Hkv, Dk), 72, torch.bfloat16, 0.5)
+    v = rand((B, T, Hkv, Dv), 73, torch.bfloat16)
+    mask = inputs.validity_mask(kind, B, T, 74, DEV)
+    y = la.la_forward_noncausal(q, k, v, q_heads=Hq, kv_heads=Hkv, out_dtype=torch.float32, mask=mask)
+    torch.cuda.synchronize()
+    yr = oracle.noncausal(q, k, v, q_heads=Hq, kv_heads=Hkv, mask=mask)
+    assert_zero_where_invalid(y, mask, "y")
+    assert_close(to64(y), yr, tol_for(torch.bfloat16, torch.float32), "non-causal segments")

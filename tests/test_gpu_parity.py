@@ -267,6 +267,26 @@ def test_decode_shapes(shape, dtype):
     assert_close(to64(Z), Zr, 1e-5, "decode Z")
 
 
+EDGE_SHAPES = [  # B, T, Hq, Hkv, Dk, Dv
+    (20, 130, 8, 8, 64, 64),     # 160 (batch, kv head) streams: more CTAs than SMs, no sequence split
+    (12, 70, 16, 16, 128, 128),  # 192 streams at head size 128
+    (1, 192, 32, 2, 64, 64),     # 16 query heads per kv head; T a multiple of the chunk
+    (2, 129, 16, 1, 128, 128),   # 16 query heads on one kv head; one step past a chunk
+]
+
+
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("rule", ["linear", "gated"])
+def test_edge_shapes(shape, rule):
+    B, T, Hq, Hkv, Dk, Dv = shape
+    if rule == "linear":
+        run_case(B, T, Hq, Hkv, Dk, Dv, torch.bfloat16, torch.bfloat16, "elu_plus_one", True, S0=True, std=0.5,
+                 seed=3)
+    else:
+        run_case(B, T, Hq, Hkv, Dk, Dv, torch.bfloat16, torch.float32, "none", False, rule="gated", S0=True,
+                 scale=0.0, seed=4)
+
+
 def test_invalid_call_raises_and_launches_nothing():
     q = torch.zeros(1, 4, 3, 16, dtype=torch.bfloat16, device=DEV)
     k = torch.zeros(1, 4, 2, 16, dtype=torch.bfloat16, device=DEV)
