@@ -22,6 +22,8 @@
  *       linear  S_t = S_{t-1} + k_t (x) v_t
  *       gated   S_t = exp(g_t) S_{t-1} + k_t (x) v_t   (g_t per kv head, log space)
  *               or, per key dimension, row i of S_t scaled by exp(g_t[i])
+ *       delta        S_t = S_{t-1} + beta_t k_t (x) (v_t - S_{t-1}^T k_t)
+ *       gated_delta  S_t = exp(g_t) S_{t-1} + beta_t k_t (x) (v_t - exp(g_t) S_{t-1}^T k_t)
  *     with o_t = scale * q_t^T S_t and scale 0.0 meaning 1/sqrt(d_k).
  *
  * Conventions shared by every entry point
@@ -72,7 +74,12 @@ typedef enum la_feature_map {
     LA_FMAP_RELU_EPS = 2       /* max(x, 0) + epsilon */
 } la_feature_map;
 
-typedef enum la_update_rule { LA_RULE_LINEAR = 0, LA_RULE_GATED = 1 } la_update_rule;
+typedef enum la_update_rule {
+    LA_RULE_LINEAR = 0,
+    LA_RULE_GATED = 1,
+    LA_RULE_DELTA = 2,       /* la_forward_causal_delta / la_decode_step_delta only */
+    LA_RULE_GATED_DELTA = 3  /* idem */
+} la_update_rule;
 
 /* The CUDA stream type without the CUDA headers: identical to cudaStream_t. */
 typedef struct CUstream_st* la_stream_t;
@@ -93,7 +100,7 @@ typedef struct la_params {
     float epsilon;           /* normalization_epsilon >= 0 (also the relu offset) */
     float scale;             /* output scale; 0.0 means 1/sqrt(Dk) (ONNX default) */
     int32_t update_rule;     /* la_update_rule */
-    int32_t decay_per_key_dim; /* 0: decay (B,T,Hkv); 1: decay (B,T,Hkv,Dk) (gated rule only).
+    int32_t decay_per_key_dim; /* 0: decay (B,T,Hkv); 1: decay (B,T,Hkv,Dk) (gated rules only).
                                 * The tensor-core prefill takes the per-head form; the
                                 * per-key-dimension form runs on CUDA cores (token by token). */
 } la_params;
@@ -206,6 +213,32 @@ la_status la_decode_step(const la_params* p, const void* q, const void* k, const
 la_status la_decode_step_masked(const la_params* p, const void* q, const void* k, const void* v,
                                 const void* decay, const uint8_t* mask, float* S, float* Z, void* y,
                                 la_stream_t stream);
+
+/* The delta rules of the ONNX-light "LinearAttention" operator (update_rule
+ * "delta" or "gated_delta", its default), causal prefill or chunk of a
+ * stream:
+ *   delta        S_t = S_{t-1} + beta_t k_t (x) (v_t - S_{t-1}^T k_t)
+ *   gated_delta  S_t = exp(g_t) S_{t-1} + beta_t k_t (x) (v_t - exp(g_t) S_{t-1}^T k_t)
+ *   o_t = scale * q_t^T S_t
+ * p->update_rule is LA_RULE_DELTA or LA_RULE_GATED_DELTA; no feature map and
+ * no normalizer (LA_ERR_UNSUPPORTED otherwise: the page defines neither).
+ *   decay      (B, T, Hkv) or, with decay_per_key_dim, (B, T, Hkv, Dk) in the
+ *              io dtype, log space; required for gated_delta, ignored for delta.
+ *   beta       update rate in the io dtype, required: (B, T, Hkv) when
+ *              beta_per_head = 1, (B, T, 1) when 0.
+ *   mask       (B, T) uint8 validity or NULL (as la_forward_causal_masked).
+ *   S0, S_out  as la_forward_causal (Z is not used by these rules).
+ * The update is not additive in S, so every (batch, kv head) stream runs as
+ * one token-by-token recurrence on CUDA cores.  No workspace is needed. */
+la_status la_forward_causal_delta(const la_params* p, const void* q, const void* k, const void* v,
+                                  const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
+                                  const float* S0, void* y, float* S_out, la_stream_t stream);
+
+/* One token per sequence with a delta rule (seq_len must be 1): S is read
+ * and updated in place; beta (B, 1, Hkv) or (B, 1, 1); mask (B,) or NULL. */
+la_status la_decode_step_delta(const la_params* p, const void* q, const void* k, const void* v,
+                               const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
+                               float* S, void* y, la_stream_t stream);
 
 /* Static string for a status code. */
 const char* la_status_string(la_status s);

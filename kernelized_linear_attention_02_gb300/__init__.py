@@ -22,7 +22,7 @@ LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA = r
 LA_F32, LA_BF16 = 0, 1
 LA_NOALLOC_SCRATCH_BYTES = 16 << 20  # built-in scratch of la_forward_causal_noalloc
 FEATURE_MAPS = {"none": 0, "elu_plus_one": 1, "relu": 2}
-UPDATE_RULES = {"linear": 0, "gated": 1}
+UPDATE_RULES = {"linear": 0, "gated": 1, "delta": 2, "gated_delta": 3}
 _DTYPES = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
 
 
@@ -56,6 +56,9 @@ _SIGNATURES = {
     "la_forward_causal_masked": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 11 + [ctypes.c_size_t, _vp]),
     "la_forward_noncausal_masked": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 6 + [ctypes.c_size_t, _vp]),
     "la_decode_step_masked": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 9),
+    "la_forward_causal_delta": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 5 + [ctypes.c_int]
+                                + [_vp] * 4 + [_vp]),
+    "la_decode_step_delta": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 5 + [ctypes.c_int] + [_vp] * 4),
     "la_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "la_last_error": (ctypes.c_char_p, []),
     "la_abi_version": (ctypes.c_int, []),
@@ -149,6 +152,22 @@ def _mask(mask, B, T):
     return mask.contiguous()
 
 
+DELTA_RULES = ("delta", "gated_delta")
+
+
+def _beta(beta, B, T, kv_heads):
+    """ONNX beta layouts: (B, T, H_kv) -> 1 (per head), (B, T, 1) -> 0."""
+    if beta is None:
+        raise ValueError("the delta rules need beta")
+    if not beta.is_cuda or not beta.is_contiguous():
+        raise ValueError("beta must be a contiguous CUDA tensor")
+    if beta.numel() == B * T * kv_heads:
+        return 1
+    if beta.numel() == B * T:
+        return 0
+    raise ValueError(f"beta must have B*T*Hkv or B*T elements, got {tuple(beta.shape)}")
+
+
 def la_workspace_bytes(params: la_params, causal: bool) -> int:
     return int(lib().la_workspace_bytes(ctypes.byref(params), int(bool(causal))))
 
@@ -176,13 +195,15 @@ def la_get_initial_state(batch, kv_heads, key_dim, value_dim, use_normalizer=Tru
 def la_forward_causal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one", use_normalizer=True,
                       epsilon=1e-6, scale=1.0, update_rule="linear", decay=None, initial_state=None,
                       return_state=False, out_dtype=None, out=None, state_out=None, workspace=None,
-                      mask=None, stream=None):
+                      mask=None, beta=None, stream=None):
     """Causal pass.  q (B,T,Hq,Dk) / (B,T,Hq*Dk), k and v likewise with Hkv heads.
 
     initial_state: (S0, Z0) or None (zeros).  Returns y, or (y, (S, Z)) with
     return_state.  ``state_out`` may be the initial_state tensors themselves
     (in-place streaming).  ``mask`` (B,T) bool/uint8: invalid steps keep the
-    state and output zero (la_forward_causal_masked)."""
+    state and output zero (la_forward_causal_masked).  update_rule "delta" /
+    "gated_delta" take ``beta`` (B,T,Hkv) or (B,T,1) (la_forward_causal_delta);
+    they keep no Z."""
     q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=out_dtype, feature_map=feature_map,
                        use_normalizer=use_normalizer, epsilon=epsilon, scale=scale,
                        update_rule=update_rule, decay=decay)
@@ -200,6 +221,12 @@ def la_forward_causal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one",
             Z = torch.empty(B, kv_heads, Dk, dtype=torch.float32, device=q.device) if use_normalizer else None
     if decay is not None and (not decay.is_cuda or not decay.is_contiguous() or decay.dtype != q.dtype):
         raise ValueError("decay must be a contiguous CUDA tensor of the io dtype")
+    if update_rule in DELTA_RULES:
+        bph = _beta(beta, B, T, kv_heads)
+        m = _mask(mask, B, T) if mask is not None else None
+        _check(lib().la_forward_causal_delta(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta), bph,
+                                             _ptr(m), _ptr(S0), _ptr(y), _ptr(S), _stream(stream)))
+        return (y, (S, None)) if return_state else y
     ws, ws_bytes = _workspace(p, True, q.device, workspace)
     if mask is not None:
         m = _mask(mask, B, T)
@@ -255,7 +282,7 @@ def la_forward_noncausal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_on
 
 def la_decode_step(q, k, v, S, Z=None, *, q_heads, kv_heads, feature_map="elu_plus_one",
                    use_normalizer=True, epsilon=1e-6, scale=1.0, update_rule="linear", decay=None,
-                   out_dtype=None, out=None, mask=None, stream=None):
+                   out_dtype=None, out=None, mask=None, beta=None, stream=None):
     """One token per sequence; S (and Z) are updated in place.  Returns y (B,1,Hq,Dv).
     ``mask`` (B,) or (B,1): a sequence whose step is invalid keeps S, Z and outputs zero."""
     q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=out_dtype, feature_map=feature_map,
@@ -264,6 +291,12 @@ def la_decode_step(q, k, v, S, Z=None, *, q_heads, kv_heads, feature_map="elu_pl
     ydt = q.dtype if out_dtype is None else out_dtype
     y = out if out is not None else torch.empty(q.shape[0], 1, q_heads, v.shape[3], dtype=ydt,
                                                 device=q.device)
+    if update_rule in DELTA_RULES:
+        bph = _beta(beta, q.shape[0], 1, kv_heads)
+        m = _mask(mask, q.shape[0], 1) if mask is not None else None
+        _check(lib().la_decode_step_delta(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta), bph,
+                                          _ptr(m), _ptr(S), _ptr(y), _stream(stream)))
+        return y
     if mask is not None:
         m = _mask(mask, q.shape[0], 1)
         _check(lib().la_decode_step_masked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(m),

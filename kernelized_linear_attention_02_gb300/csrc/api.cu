@@ -36,7 +36,7 @@ la_status cuda_fail(cudaError_t e, const char* where) {
     return fail(LA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
-enum class Call { kCausal, kNonCausal, kDecode, kState };
+enum class Call { kCausal, kNonCausal, kDecode, kState, kDelta };
 
 constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
@@ -63,12 +63,19 @@ la_status make_problem(const la_params* p, Call call, la::Problem* P) {
         return fail(LA_ERR_INVALID_ARG, "use_normalizer must be 0 or 1");
     if (!std::isfinite(p->epsilon) || p->epsilon < 0.f) return fail(LA_ERR_INVALID_ARG, "epsilon must be finite and >= 0");
     if (!std::isfinite(p->scale)) return fail(LA_ERR_INVALID_ARG, "scale must be finite");
-    if (p->update_rule != LA_RULE_LINEAR && p->update_rule != LA_RULE_GATED)
+    if (p->update_rule < LA_RULE_LINEAR || p->update_rule > LA_RULE_GATED_DELTA)
         return fail(LA_ERR_INVALID_ARG, "unknown update_rule %d", p->update_rule);
+    const bool delta = p->update_rule == LA_RULE_DELTA || p->update_rule == LA_RULE_GATED_DELTA;
+    if (delta && call != Call::kDelta && call != Call::kState)
+        return fail(LA_ERR_INVALID_ARG, "the delta rules take beta: call la_forward_causal_delta / la_decode_step_delta");
+    if (!delta && call == Call::kDelta)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_causal_delta needs update_rule delta or gated_delta");
+    if (delta && (p->feature_map != LA_FMAP_NONE || p->use_normalizer))
+        return fail(LA_ERR_UNSUPPORTED, "the delta rules are defined without a feature map or normalizer");
     if (p->decay_per_key_dim != 0 && p->decay_per_key_dim != 1)
         return fail(LA_ERR_INVALID_ARG, "decay_per_key_dim must be 0 or 1");
-    if (p->decay_per_key_dim && p->update_rule != LA_RULE_GATED)
-        return fail(LA_ERR_INVALID_ARG, "decay_per_key_dim needs the gated rule");
+    if (p->decay_per_key_dim && p->update_rule != LA_RULE_GATED && p->update_rule != LA_RULE_GATED_DELTA)
+        return fail(LA_ERR_INVALID_ARG, "decay_per_key_dim needs a gated rule");
     if (p->update_rule == LA_RULE_GATED && (p->feature_map != LA_FMAP_NONE || p->use_normalizer))
         return fail(LA_ERR_UNSUPPORTED, "the gated rule is defined without a feature map or normalizer");
     if (call == Call::kNonCausal && p->update_rule != LA_RULE_LINEAR)
@@ -87,7 +94,8 @@ la_status make_problem(const la_params* p, Call call, la::Problem* P) {
     P->out_bf16 = p->out_dtype == LA_BF16;
     P->fmap = p->feature_map;
     P->norm = p->use_normalizer;
-    P->gated = p->update_rule == LA_RULE_GATED;
+    P->gated = p->update_rule == LA_RULE_GATED || p->update_rule == LA_RULE_GATED_DELTA;
+    P->delta = delta;
     P->decay_dim = p->decay_per_key_dim;
     P->eps = p->epsilon;
     P->scale = p->scale == 0.f ? 1.f / std::sqrt((float)p->key_dim) : p->scale;
@@ -303,6 +311,41 @@ la_status la_decode_step_masked(const la_params* p, const void* q, const void* k
 la_status la_decode_step(const la_params* p, const void* q, const void* k, const void* v, const void* decay,
                          float* S, float* Z, void* y, la_stream_t stream) {
     return la_decode_step_masked(p, q, k, v, decay, nullptr, S, Z, y, stream);
+}
+
+la_status la_forward_causal_delta(const la_params* p, const void* q, const void* k, const void* v,
+                                  const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
+                                  const float* S0, void* y, float* S_out, la_stream_t stream) {
+    la::Problem P;
+    la_status st = make_problem(p, Call::kDelta, &P);
+    if (st != LA_OK) return st;
+    if (beta_per_head != 0 && beta_per_head != 1) return fail(LA_ERR_INVALID_ARG, "beta_per_head must be 0 or 1");
+    P.mask = mask;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (P.T == 0) {  // the state passes through
+        cudaError_t e = cudaSuccess;
+        if (S_out && S_out != S0)
+            e = S0 ? cudaMemcpyAsync(S_out, S0, state_bytes(P), cudaMemcpyDeviceToDevice, s)
+                   : cudaMemsetAsync(S_out, 0, state_bytes(P), s);
+        if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal_delta");
+        g_last_error.clear();
+        return LA_OK;
+    }
+    if (!q || !k || !v || !y || !beta) return fail(LA_ERR_INVALID_ARG, "q, k, v, beta and y are required");
+    if (P.gated && !decay) return fail(LA_ERR_INVALID_ARG, "gated_delta needs decay");
+    cudaError_t e = la::recurrent_delta(P, q, k, v, P.gated ? decay : nullptr, beta, beta_per_head, S0, y, S_out, s);
+    if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal_delta");
+    g_last_error.clear();
+    return LA_OK;
+}
+
+la_status la_decode_step_delta(const la_params* p, const void* q, const void* k, const void* v,
+                               const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
+                               float* S, void* y, la_stream_t stream) {
+    if (p && p->seq_len != 1)
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step_delta needs seq_len == 1 (got %lld)", (long long)p->seq_len);
+    if (!S) return fail(LA_ERR_INVALID_ARG, "S is required");
+    return la_forward_causal_delta(p, q, k, v, decay, beta, beta_per_head, mask, S, y, S, stream);
 }
 
 }  // extern "C"

@@ -19,6 +19,7 @@ struct Problem {
     int io_bf16, out_bf16;
     int fmap, norm, gated;
     int decay_dim;  // gated: decay per key dimension (B, T, Hkv, Dk) instead of per head
+    int delta;      // delta rules: S += beta k (x) (v - S^T k) after the decay (recurrence only)
     float eps, scale;
     // (B, T) sequence-validity mask, nonzero = valid; null = every step valid
     const uint8_t* mask = nullptr;

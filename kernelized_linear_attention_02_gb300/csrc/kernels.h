@@ -18,6 +18,10 @@ cudaError_t recurrent_causal(const Problem& P, const void* q, const void* k, con
                              size_t ws_bytes = 0);
 cudaError_t recurrent_noncausal(const Problem& P, const void* q, const void* k, const void* v,
                                 void* y, float* S_ws, float* Z_ws, cudaStream_t st);
+// The delta rules (P.delta): one CTA per stream, token by token.
+cudaError_t recurrent_delta(const Problem& P, const void* q, const void* k, const void* v, const void* decay,
+                            const void* beta, int beta_per_head, const float* S0, void* y, float* S_out,
+                            cudaStream_t st);
 
 // Tensor-core chunk path (chunk_host.cu): bf16 inputs, Dk == Dv in {64, 128}.
 bool chunk_supported(const Problem& P);

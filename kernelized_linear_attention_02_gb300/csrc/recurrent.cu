@@ -19,6 +19,12 @@
 // segments onto the initial state in order (S <- exp(G_seg) S + dS_seg, Z <-
 // Z + dZ_seg), which is the recurrence regrouped, and walks its own steps.
 //
+// The delta rules of the ONNX-light operator decay the state first, then add
+// beta k (x) (v - S^T k): the residual needs S^T k of the decayed state, a
+// reduction over the key dimensions held by the eight warps (one exchange
+// through shared memory per step).  Their update is not additive in S, so
+// they never take the segment split.
+//
 // A sequence-validity mask (Keras request, Masking) skips the update of an
 // invalid step (the state passes through unchanged, no decay either) and
 // writes zeros for its outputs.  The mask is per (batch, step), so the
@@ -55,6 +61,8 @@ struct RecArgs {
     float* S_seg = nullptr;  // (B*Hkv, nseg, Dk, Dv) state increment of each segment
     float* Z_seg = nullptr;  // (B*Hkv, nseg, Dk) key-sum increment
     float* G_seg = nullptr;  // (B*Hkv, nseg, Dk) summed log decay per key dimension (gated)
+    const void* beta = nullptr;  // delta rules: (B, T, Hkv) or (B, T, 1)
+    int beta_per_head = 1;
 };
 
 enum { kModeCausal = 0, kModeStateOnly = 1, kModeReadoutOnly = 2 };
@@ -78,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(RecArgs a) {
     const TIn* k = static_cast<const TIn*>(a.k);
     const TIn* v = static_cast<const TIn*>(a.v);
     const TIn* decay = static_cast<const TIn*>(a.decay);
+    const TIn* beta = static_cast<const TIn*>(a.beta);
     TOut* y = static_cast<TOut*>(a.y);
     const bool update = a.mode != kModeReadoutOnly;
     const bool readout = a.mode != kModeStateOnly;
@@ -151,15 +160,52 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(RecArgs a) {
                 const int j = lane + 32 * n;
                 vj[n] = j < Dv ? load_in(v, (tok * P.Hkv + hk) * Dv + j) : 0.f;
             }
+            if (P.delta) {
+                // decay, then u = beta (v - S^T k) with the decayed S, then S += k (x) u
+                float pn[kColsPerThread] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int m = 0; m < kRowsPerThread; ++m) {
-                const int i = warp + 8 * m;
-                const float f = i < Dk ? fk[i] : 0.f;
-                const float gi = P.gated && P.decay_dim && i < Dk ? load_in(decay, (tok * P.Hkv + hk) * Dk + i) : gh;
-                const float di = P.gated && P.decay_dim ? expf(gi) : dec;
-                gl[m] += gi;
+                for (int m = 0; m < kRowsPerThread; ++m) {
+                    const int i = warp + 8 * m;
+                    const float f = i < Dk ? fk[i] : 0.f;
+                    const float gi = P.gated && P.decay_dim && i < Dk ? load_in(decay, (tok * P.Hkv + hk) * Dk + i) : gh;
+                    const float di = P.gated && P.decay_dim ? expf(gi) : dec;
 #pragma unroll
-                for (int n = 0; n < kColsPerThread; ++n) s[m][n] = fmaf(f, vj[n], di * s[m][n]);
+                    for (int n = 0; n < kColsPerThread; ++n) {
+                        s[m][n] *= di;
+                        pn[n] = fmaf(s[m][n], f, pn[n]);
+                    }
+                }
+#pragma unroll
+                for (int n = 0; n < kColsPerThread; ++n) red[warp * 128 + lane + 32 * n] = pn[n];
+                __syncthreads();
+                const float bt = load_in(beta, a.beta_per_head ? tok * P.Hkv + hk : tok);
+                float un[kColsPerThread];
+#pragma unroll
+                for (int n = 0; n < kColsPerThread; ++n) {
+                    const int j = lane + 32 * n;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) acc += red[w * 128 + j];
+                    un[n] = bt * (vj[n] - acc);
+                }
+#pragma unroll
+                for (int m = 0; m < kRowsPerThread; ++m) {
+                    const int i = warp + 8 * m;
+                    const float f = i < Dk ? fk[i] : 0.f;
+#pragma unroll
+                    for (int n = 0; n < kColsPerThread; ++n) s[m][n] = fmaf(f, un[n], s[m][n]);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < kRowsPerThread; ++m) {
+                    const int i = warp + 8 * m;
+                    const float f = i < Dk ? fk[i] : 0.f;
+                    const float gi = P.gated && P.decay_dim && i < Dk ? load_in(decay, (tok * P.Hkv + hk) * Dk + i) : gh;
+                    const float di = P.gated && P.decay_dim ? expf(gi) : dec;
+                    gl[m] += gi;
+#pragma unroll
+                    for (int n = 0; n < kColsPerThread; ++n) s[m][n] = fmaf(f, vj[n], di * s[m][n]);
+                }
             }
             if (P.norm && tid < Dk) Zs[tid] += fk[tid];
         }
@@ -253,7 +299,7 @@ constexpr size_t kWsAlign = 256;
 size_t up256(size_t x) { return (x + kWsAlign - 1) & ~(kWsAlign - 1); }
 
 int rec_segments(const Problem& P) {
-    if (P.T < 512) return 1;
+    if (P.T < 512 || P.delta) return 1;
     const int64_t streams = P.B * P.Hkv;
     const int sms = device_sm_count();
     if (sms <= 0 || streams * 2 > sms) return 1;
@@ -327,6 +373,16 @@ cudaError_t recurrent_causal(const Problem& P, const void* q, const void* k, con
     cudaError_t e = dispatch(a1, st, nseg - 1);
     if (e != cudaSuccess) return e;
     return dispatch(a, st, nseg);
+}
+
+cudaError_t recurrent_delta(const Problem& P, const void* q, const void* k, const void* v, const void* decay,
+                            const void* beta, int beta_per_head, const float* S0, void* y, float* S_out,
+                            cudaStream_t st) {
+    RecArgs a{q, k, v, decay, S0, nullptr, y, S_out, nullptr, P, kModeCausal};
+    a.P.norm = 0;
+    a.beta = beta;
+    a.beta_per_head = beta_per_head;
+    return dispatch(a, st);
 }
 
 cudaError_t recurrent_noncausal(const Problem& P, const void* q, const void* k, const void* v,
