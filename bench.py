@@ -150,7 +150,8 @@ def prefill_alg_bytes(w, T=None):
     esz = 2 if w.dtype == torch.bfloat16 else 4
     qy = w.B * T * w.q_heads * (w.Dk + w.Dv) * esz
     kv = w.B * T * w.kv_heads * (w.Dk + w.Dv) * esz
-    dec = w.B * T * w.kv_heads * (w.Dk if w.decay_per_dim else 1) * esz if w.rule == "gated" else 0
+    dec = w.B * T * w.kv_heads * (w.Dk if w.decay_per_dim else 1) * esz if w.rule in ("gated", "gated_delta") else 0
+    dec += w.B * T * w.kv_heads * esz if w.rule in ("delta", "gated_delta") else 0  # beta
     msk = w.B * T if w.mask else 0  # one validity byte per (batch, step)
     return qy + kv + dec + msk
 
@@ -313,7 +314,8 @@ def time_workload(la, w, steps, warmup, stream, causal=True):
         q, k, v, d = inputs.make_qkv(w, device="cuda", seed=w.seed + s)
         y = torch.empty(w.B, w.T, w.q_heads, w.Dv, dtype=w.dtype, device="cuda")
         m = inputs.validity_mask(w.mask, w.B, w.T, w.seed + s, "cuda") if w.mask else None
-        sets.append((q, k, v, d, y, m))
+        bt = inputs.make_beta(w, "cuda", w.seed + s) if w.rule in ("delta", "gated_delta") else None
+        sets.append((q, k, v, d, y, m, bt))
     kw = prefill_kwargs(w)
     if not causal:
         kw.pop("update_rule")
@@ -323,9 +325,9 @@ def time_workload(la, w, steps, warmup, stream, causal=True):
     ws = torch.empty(max(1, la.la_workspace_bytes(p, causal)), dtype=torch.uint8, device="cuda")
 
     def step(i):
-        q, k, v, d, y, m = sets[i % nsets]
+        q, k, v, d, y, m, bt = sets[i % nsets]
         if causal:
-            la.la_forward_causal(q, k, v, decay=d, out=y, workspace=ws, mask=m, stream=stream, **kw)
+            la.la_forward_causal(q, k, v, decay=d, out=y, workspace=ws, mask=m, beta=bt, stream=stream, **kw)
         else:
             la.la_forward_noncausal(q, k, v, out=y, workspace=ws, mask=m, stream=stream, **kw)
 
@@ -356,7 +358,8 @@ def workload_sweep(la, steps, warmup, stream, hbm_gbs):
     out = []
     cases = [(inputs.PREFILL_2K, True), (inputs.PREFILL_2K_RIGHTPAD, True), (inputs.LONG_8K, True),
              (inputs.LONG_8K_UNNORM, True), (inputs.LONG_8K, False), (inputs.LONG_8K_UNNORM, False),
-             (inputs.ONNX_LINEAR, True), (inputs.ONNX_GATED, True), (inputs.GATED_PERDIM, True)]
+             (inputs.ONNX_LINEAR, True), (inputs.ONNX_GATED, True), (inputs.GATED_PERDIM, True),
+             (inputs.GATED_DELTA, True)]
     for w, causal in cases:
         ms, lpc = time_workload(la, w, steps, warmup, stream, causal)
         alg = prefill_alg_bytes(w)

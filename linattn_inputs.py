@@ -30,7 +30,7 @@ class Workload:
     use_normalizer: bool
     eps: float
     scale: float              # 0.0 -> 1/sqrt(Dk) (ONNX convention)
-    rule: str                 # "linear" | "gated"
+    rule: str                 # "linear" | "gated" | "delta" | "gated_delta"
     qk_std: float = 1.0       # q, k ~ N(0, qk_std^2)
     v_std: float = 1.0
     k_l2_normalize: bool = False
@@ -66,8 +66,13 @@ PREFILL_2K_RIGHTPAD = dataclasses.replace(PREFILL_2K, name=PREFILL_2K.name + "_r
 GATED_PERDIM = dataclasses.replace(ONNX_GATED, name="gated_perdim_gqa_B2_T4096_Hq32_Hkv8_D128_bf16", T=4096,
                                    decay_per_dim=True)
 
+# the ONNX operator's default rule, gated_delta (beta per kv head), on the
+# CUDA-core recurrence
+GATED_DELTA = dataclasses.replace(ONNX_GATED, name="gated_delta_gqa_B2_T4096_Hq32_Hkv8_D128_bf16", T=4096,
+                                  rule="gated_delta")
+
 ALL = [TINY, PREFILL_2K, LONG_8K, LONG_8K_UNNORM, DECODE, ONNX_LINEAR, ONNX_GATED, PREFILL_2K_RIGHTPAD,
-       GATED_PERDIM]
+       GATED_PERDIM, GATED_DELTA]
 
 MASK_KINDS = ("right", "left", "gaps", "random", "none_valid", "all_valid")
 
@@ -107,11 +112,19 @@ def make_qkv(w: Workload, device="cpu", T=None, B=None, seed=None):
         k = normal((B, T, w.kv_heads, w.Dk), g, w.qk_std, dtype=w.dtype, device=device)
     v = normal((B, T, w.kv_heads, w.Dv), g, w.v_std, dtype=w.dtype, device=device)
     decay = None
-    if w.rule == "gated":
+    if w.rule in ("gated", "gated_delta"):
         dshape = (B, T, w.kv_heads, w.Dk) if w.decay_per_dim else (B, T, w.kv_heads)
         x = normal(dshape, g, 1.0, mean=w.decay_mu, dtype=torch.float32, device=device)
         decay = torch.nn.functional.logsigmoid(x).to(w.dtype)
     return q, k, v, decay
+
+
+def make_beta(w: Workload, device="cpu", seed=None) -> torch.Tensor:
+    """Update rate of the delta rules, (B, T, Hkv): sigmoid(x), x ~ N(0, 1)
+    (the ONNX page's beta is a sigmoid output), drawn after the other inputs'
+    generator (its own seed offset)."""
+    g = generator((w.seed if seed is None else seed) + 7919, device)
+    return torch.sigmoid(normal((w.B, w.T, w.kv_heads), g, 1.0, dtype=torch.float32, device=device)).to(w.dtype)
 
 
 def validity_mask(kind: str, B: int, T: int, seed: int = 0, device="cpu") -> torch.Tensor:

@@ -144,3 +144,22 @@ def test_delta_argument_checks():
     with pytest.raises(la.LinearAttentionError):  # gated_delta without decay
         la.la_forward_causal(q, q, q, q_heads=2, kv_heads=2, feature_map="none", use_normalizer=False,
                              update_rule="gated_delta", beta=torch.ones(1, 4, 2, device=DEV))
+
+
+def test_gated_delta_workload_sampled_slices():
+    """The measured gated_delta workload at full size (the launch the
+    benchmark times): sampled (batch, kv head) streams against the oracle."""
+    w = inputs.GATED_DELTA
+    q, k, v, d = inputs.make_qkv(w, device=DEV)
+    beta = inputs.make_beta(w, DEV)
+    y = la.la_forward_causal(q, k, v, q_heads=w.q_heads, kv_heads=w.kv_heads, feature_map=w.feature_map,
+                             use_normalizer=w.use_normalizer, epsilon=w.eps, scale=w.scale, update_rule=w.rule,
+                             decay=d, beta=beta)
+    torch.cuda.synchronize()
+    G = w.q_heads // w.kv_heads
+    for b, hk in [(0, 3), (1, 6)]:
+        yr, _, _ = oracle.causal(q[b:b + 1, :, hk * G:(hk + 1) * G], k[b:b + 1, :, hk:hk + 1], v[b:b + 1, :, hk:hk + 1],
+                                 q_heads=G, kv_heads=1, feature_map=w.feature_map, use_normalizer=w.use_normalizer,
+                                 scale=w.scale, rule=w.rule, decay=d[b:b + 1, :, hk:hk + 1],
+                                 beta=beta[b:b + 1, :, hk:hk + 1])
+        assert_close(to64(y[b:b + 1, :, hk * G:(hk + 1) * G]), yr, tol_for(w.dtype, w.dtype), f"slice {b},{hk}")
