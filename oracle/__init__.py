@@ -6,7 +6,7 @@ Python binding) never imports it and shares no code with it.
 
 Two independent formulations live here:
 
-* ``causal`` / ``noncausal`` / ``decode_steps``: the fp64 C recurrence in
+* ``causal`` / ``noncausal``: the fp64 C recurrence in
   ``linattn_oracle.c`` (token by token, exactly as the pages write it), run
   through ctypes.
 * ``oracle.bruteforce``: the O(T^2) pairwise-weight form in numpy, written

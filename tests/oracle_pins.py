@@ -339,10 +339,55 @@ def pin_mask_noncausal(lib=None, seed=10):
                     np.testing.assert_allclose(y[b, idx], yb[0], rtol=1e-10, atol=1e-10)
 
 
+def pin_grad_forward_matches_recurrence(lib=None, seed=11):
+    """The differentiable float64 recurrence used for gradients computes the
+    same outputs as the C oracle (GQA, carried state, every feature map)."""
+    import torch
+    from oracle import grad as og
+    rng = np.random.default_rng(seed)
+    B, T, Hq, Hkv, Dk, Dv = 2, 9, 4, 2, 3, 5
+    for fmap, norm in (("elu_plus_one", True), ("relu", True), ("none", False), ("elu_plus_one", False)):
+        q, k = _rand(rng, B, T, Hq, Dk, std=0.7), _rand(rng, B, T, Hkv, Dk, std=0.7)
+        v = _rand(rng, B, T, Hkv, Dv)
+        S0 = _rand(rng, B, Hkv, Dk, Dv)
+        Z0 = np.abs(_rand(rng, B, Hkv, Dk)) + 0.5 if norm else None
+        kw = dict(q_heads=Hq, kv_heads=Hkv, feature_map=fmap, use_normalizer=norm, eps=1e-3, scale=0.75)
+        y, _, _ = oracle.causal(q, k, v, S0=S0, Z0=Z0, lib=lib, **kw)
+        t = lambda x: None if x is None else torch.tensor(x, dtype=torch.float64)
+        yg = og.causal_forward(t(q), t(k), t(v), S0=t(S0), Z0=t(Z0), **kw).numpy()
+        np.testing.assert_allclose(yg, y, rtol=1e-11, atol=1e-11, err_msg=fmap)
+
+
+def pin_grad_finite_differences(lib=None, seed=12):
+    """Keras request, Test Plan (Stability): float64 numerical-gradient checks.
+    The autograd gradients of the recurrence match central finite
+    differences for q, k, v and the carried state, with and without the
+    normalizer, with grouped heads."""
+    import torch
+    from oracle import grad as og
+    g = torch.Generator().manual_seed(seed)
+    B, T, Hq, Hkv, Dk, Dv = 1, 5, 2, 1, 3, 2
+    for fmap, norm in (("elu_plus_one", True), ("relu", False)):
+        q = (torch.randn(B, T, Hq, Dk, generator=g, dtype=torch.float64) * 0.7).requires_grad_(True)
+        k = (torch.randn(B, T, Hkv, Dk, generator=g, dtype=torch.float64) * 0.7).requires_grad_(True)
+        v = torch.randn(B, T, Hkv, Dv, generator=g, dtype=torch.float64).requires_grad_(True)
+        S0 = torch.randn(B, Hkv, Dk, Dv, generator=g, dtype=torch.float64).requires_grad_(True)
+        Z0 = (torch.rand(B, Hkv, Dk, generator=g, dtype=torch.float64) + 0.5).requires_grad_(True)
+        f = lambda q, k, v, S0, Z0: og.causal_forward(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map=fmap,
+                                                      use_normalizer=norm, eps=1e-3, scale=1.3, S0=S0,
+                                                      Z0=Z0 if norm else None)
+        # keep away from the kinks of elu / relu at 0, where one-sided differences disagree
+        for x in (q, k):
+            with torch.no_grad():
+                x.add_(torch.sign(x) * 0.05)
+        assert torch.autograd.gradcheck(f, (q, k, v, S0, Z0), eps=1e-6, atol=1e-7, rtol=1e-5)
+
+
 ALL_PINS = [pin_paper_mean_abs_diff, pin_recurrence_vs_bruteforce, pin_noncausal_vs_bruteforce,
             pin_last_row_equals_noncausal, pin_chunked_equals_full, pin_state_closed_form,
             pin_first_token, pin_feature_map_values, pin_constant_value, pin_gated_reductions,
-            pin_gqa_equals_repeated_mha, pin_scale, pin_mask_causal, pin_mask_noncausal]
+            pin_gqa_equals_repeated_mha, pin_scale, pin_mask_causal, pin_mask_noncausal,
+            pin_grad_forward_matches_recurrence, pin_grad_finite_differences]
 
 
 def run_all(lib=None):
