@@ -240,6 +240,20 @@ la_status la_decode_step_delta(const la_params* p, const void* q, const void* k,
                                const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
                                float* S, void* y, la_stream_t stream);
 
+/* Gradients of la_forward_causal for the linear rule (the backward pass the
+ * Keras request's Test Plan asks to check numerically; no mask, no decay).
+ *   q, k, v, S0, Z0  the forward call's inputs (S0/Z0 may be NULL = zeros).
+ *   dy               gradient of the output y, (B, T, Hq, Dv) in the io dtype.
+ *   dq, dk, dv       outputs in out_dtype, the shapes of q, k, v.
+ *   dS0, dZ0         gradients of the initial state (float32), or NULL.
+ *   ws               workspace of la_backward_workspace_bytes(p) bytes.
+ * Two CUDA-core passes (tokens forward for dq, backward for dk, dv), one CTA
+ * per (batch, kv head) stream.  LA_ERR_UNSUPPORTED for the other rules. */
+size_t la_backward_workspace_bytes(const la_params* p);
+la_status la_backward_causal(const la_params* p, const void* q, const void* k, const void* v, const float* S0,
+                             const float* Z0, const void* dy, void* dq, void* dk, void* dv, float* dS0, float* dZ0,
+                             void* ws, size_t ws_bytes, la_stream_t stream);
+
 /* Static string for a status code. */
 const char* la_status_string(la_status s);
 

@@ -59,6 +59,8 @@ _SIGNATURES = {
     "la_forward_causal_delta": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 5 + [ctypes.c_int]
                                 + [_vp] * 4 + [_vp]),
     "la_decode_step_delta": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 5 + [ctypes.c_int] + [_vp] * 4),
+    "la_backward_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(la_params)]),
+    "la_backward_causal": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 12 + [ctypes.c_size_t, _vp]),
     "la_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "la_last_error": (ctypes.c_char_p, []),
     "la_abi_version": (ctypes.c_int, []),
@@ -305,6 +307,36 @@ def la_decode_step(q, k, v, S, Z=None, *, q_heads, kv_heads, feature_map="elu_pl
         _check(lib().la_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(S),
                                     _ptr(Z), _ptr(y), _stream(stream)))
     return y
+
+
+def la_backward_causal(q, k, v, dy, *, q_heads, kv_heads, feature_map="elu_plus_one", use_normalizer=True,
+                       epsilon=1e-6, scale=1.0, initial_state=None, grad_dtype=torch.float32,
+                       return_state_grad=False, workspace=None, stream=None):
+    """Gradients of la_forward_causal (linear rule) given dy (the shape of y,
+    io dtype): returns (dq, dk, dv) in ``grad_dtype``, and (dS0, dZ0) as well
+    with ``return_state_grad``."""
+    q, k, v, p = _prep(q, k, v, q_heads, kv_heads, out_dtype=grad_dtype, feature_map=feature_map,
+                       use_normalizer=use_normalizer, epsilon=epsilon, scale=scale)
+    dy = _as_bthd(dy, q_heads, "dy")
+    if dy.dtype != q.dtype or dy.shape[:2] != q.shape[:2] or dy.shape[3] != v.shape[3]:
+        raise ValueError("dy must have the shape of y and the dtype of q")
+    B, T, _, Dk = q.shape
+    Dv = v.shape[3]
+    dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+    dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+    dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
+    S0, Z0 = initial_state if initial_state is not None else (None, None)
+    dS0 = dZ0 = None
+    if return_state_grad:
+        dS0 = torch.empty(B, kv_heads, Dk, Dv, dtype=torch.float32, device=q.device)
+        dZ0 = torch.empty(B, kv_heads, Dk, dtype=torch.float32, device=q.device) if use_normalizer else None
+    need = int(lib().la_backward_workspace_bytes(ctypes.byref(p)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(1, need), dtype=torch.uint8, device=q.device)
+    _check(lib().la_backward_causal(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(S0), _ptr(Z0), _ptr(dy), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(dS0), _ptr(dZ0), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+    return (dq, dk, dv, dS0, dZ0) if return_state_grad else (dq, dk, dv)
 
 
 def la_launch_count() -> int:

@@ -313,6 +313,41 @@ la_status la_decode_step(const la_params* p, const void* q, const void* k, const
     return la_decode_step_masked(p, q, k, v, decay, nullptr, S, Z, y, stream);
 }
 
+size_t la_backward_workspace_bytes(const la_params* p) {
+    la::Problem P;
+    if (make_problem(p, Call::kCausal, &P) != LA_OK) return 0;
+    return la::backward_workspace_bytes(P);
+}
+
+la_status la_backward_causal(const la_params* p, const void* q, const void* k, const void* v, const float* S0,
+                             const float* Z0, const void* dy, void* dq, void* dk, void* dv, float* dS0, float* dZ0,
+                             void* ws, size_t ws_bytes, la_stream_t stream) {
+    la::Problem P;
+    la_status st = make_problem(p, Call::kCausal, &P);
+    if (st != LA_OK) return st;
+    if (P.gated) return fail(LA_ERR_UNSUPPORTED, "la_backward_causal covers the linear rule only");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!P.norm) Z0 = nullptr, dZ0 = nullptr;
+    if (P.T == 0) {  // no tokens: the initial state's gradient is zero
+        cudaError_t e = cudaSuccess;
+        if (dS0) e = cudaMemsetAsync(dS0, 0, state_bytes(P), s);
+        if (e == cudaSuccess && dZ0) e = cudaMemsetAsync(dZ0, 0, key_state_bytes(P), s);
+        if (e != cudaSuccess) return cuda_fail(e, "la_backward_causal");
+        g_last_error.clear();
+        return LA_OK;
+    }
+    if (!q || !k || !v || !dy || !dq || !dk || !dv)
+        return fail(LA_ERR_INVALID_ARG, "q, k, v, dy, dq, dk and dv are required when seq_len > 0");
+    const size_t need = la::backward_workspace_bytes(P);
+    if (!ws || ws_bytes < need)
+        return fail(LA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, ws ? ws_bytes : 0);
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(LA_ERR_WORKSPACE, "workspace must be %zu-byte aligned", kAlign);
+    cudaError_t e = la::backward_causal(P, q, k, v, S0, Z0, dy, dq, dk, dv, dS0, dZ0, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "la_backward_causal");
+    g_last_error.clear();
+    return LA_OK;
+}
+
 la_status la_forward_causal_delta(const la_params* p, const void* q, const void* k, const void* v,
                                   const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
                                   const float* S0, void* y, float* S_out, la_stream_t stream) {

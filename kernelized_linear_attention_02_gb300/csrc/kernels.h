@@ -39,6 +39,12 @@ unsigned chunk_device_error(bool reset);
 int device_sm_count();
 unsigned* device_error_word();
 
+// Gradients of the causal linear rule (backward.cu).
+size_t backward_workspace_bytes(const Problem& P);
+cudaError_t backward_causal(const Problem& P, const void* q, const void* k, const void* v, const float* S0,
+                            const float* Z0, const void* dy, void* dq, void* dk, void* dv, float* dS0, float* dZ0,
+                            void* ws, cudaStream_t st);
+
 // Decode step (decode.cu).
 bool decode_supported(const Problem& P);
 cudaError_t decode_step(const Problem& P, const void* q, const void* k, const void* v,

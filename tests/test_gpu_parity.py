@@ -293,3 +293,35 @@ def test_invalid_call_raises_and_launches_nothing():
     with pytest.raises(la.LinearAttentionError) as e:
         la.la_forward_causal(q, k, k, q_heads=3, kv_heads=2)
     assert e.value.status == la.LA_ERR_INVALID_ARG
+
+
+def test_calls_replay_in_a_cuda_graph():
+    """The library's calls can be captured into a CUDA graph (the causal pass
+    is a programmatic dependent of the segment state pass, an edge the graph
+    keeps) and replay bit-identically to eager calls on new inputs."""
+    B, T, H, D = 2, 1500, 4, 64  # few streams: a segment state pass and a dependent causal pass
+    mk = lambda seed: (rand((B, T, H, D), seed, torch.bfloat16, 0.5), rand((B, T, H, D), seed + 1, torch.bfloat16, 0.5),
+                       rand((B, T, H, D), seed + 2, torch.bfloat16))
+    q, k, v = mk(81)
+    kw = dict(q_heads=H, kv_heads=H)
+    p = la.make_params(batch=B, seq_len=T, q_heads=H, kv_heads=H, key_dim=D, value_dim=D)
+    ws = torch.empty(max(1, la.la_workspace_bytes(p, True)), dtype=torch.uint8, device=DEV)
+    y = torch.empty(B, T, H, D, dtype=torch.bfloat16, device=DEV)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        la.la_forward_causal(q, k, v, out=y, workspace=ws, stream=st, **kw)  # configures the kernels
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    n0 = la.la_launch_count()
+    with torch.cuda.graph(g, stream=st, capture_error_mode="relaxed"):
+        la.la_forward_causal(q, k, v, out=y, workspace=ws, stream=st, **kw)
+    assert la.la_launch_count() - n0 == 2
+    q2, k2, v2 = mk(91)
+    q.copy_(q2), k.copy_(k2), v.copy_(v2)
+    g.replay()
+    torch.cuda.synchronize()
+    y_eager = la.la_forward_causal(q2, k2, v2, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_eager)
+    yr, _, _ = oracle.causal(q2, k2, v2, q_heads=H, kv_heads=H)
+    assert_close(to64(y), yr, tol_for(torch.bfloat16, torch.bfloat16), "graph replay")
