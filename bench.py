@@ -350,6 +350,38 @@ def time_workload(la, w, steps, warmup, stream, causal=True):
     return ev0.elapsed_time(ev1) / steps, launches / steps
 
 
+def time_backward(la, w, steps, warmup, stream):
+    """Device time of la_backward_causal on a workload (linear rule): q, k, v
+    and dy resident in HBM, fp32 gradients.  Algorithmic bytes: q, k, v, dy
+    read once, dq, dk, dv written once."""
+    q, k, v, _ = inputs.make_qkv(w, device="cuda", seed=w.seed)
+    dy = inputs.normal((w.B, w.T, w.q_heads, w.Dv), inputs.generator(w.seed + 1, "cuda"), 1.0, dtype=w.dtype,
+                       device="cuda")
+    kw = prefill_kwargs(w)
+    kw.pop("update_rule")
+    p = la.make_params(batch=w.B, seq_len=w.T, q_heads=w.q_heads, kv_heads=w.kv_heads, key_dim=w.Dk, value_dim=w.Dv,
+                       io_dtype=w.dtype, feature_map=w.feature_map, use_normalizer=w.use_normalizer,
+                       epsilon=w.eps, scale=w.scale)
+    ws = torch.empty(max(1, la.la_backward_workspace_bytes(p)), dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            la.la_backward_causal(q, k, v, dy, workspace=ws, stream=stream, **kw)
+    torch.cuda.synchronize()
+    n0 = la.la_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            la.la_backward_causal(q, k, v, dy, workspace=ws, stream=stream, **kw)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    launches = (la.la_launch_count() - n0) / steps
+    esz = 2 if w.dtype == torch.bfloat16 else 4
+    alg = (w.B * w.T * (w.q_heads * (w.Dk + w.Dv) + w.kv_heads * (w.Dk + w.Dv)) * esz
+           + w.B * w.T * (w.q_heads * w.Dk + w.kv_heads * (w.Dk + w.Dv)) * 4)
+    return ev0.elapsed_time(ev1) / steps, launches, alg
+
+
 def workload_sweep(la, steps, warmup, stream, hbm_gbs):
     """Every prefill workload of the library (causal and non-causal), each
     with its HBM roofline fraction.  Algorithmic bytes: q, k, v (+ decay)
@@ -367,6 +399,12 @@ def workload_sweep(la, steps, warmup, stream, hbm_gbs):
         out.append({"workload": w.name, "mode": "causal" if causal else "noncausal", "ms": ms,
                     "tokens_per_s": w.B * w.T / (ms * 1e-3), "alg_bytes": alg, "achieved_GBps": gbs,
                     "roofline_frac": gbs / hbm_gbs, "launches_per_call": lpc})
+    # the backward pass of the headline workload (CUDA-core scans)
+    w = inputs.PREFILL_2K
+    ms, lpc, alg = time_backward(la, w, max(1, min(steps, 5)), min(warmup, 2), stream)
+    gbs = alg / (ms * 1e-3) / 1e9
+    out.append({"workload": w.name, "mode": "backward", "ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
+                "alg_bytes": alg, "achieved_GBps": gbs, "roofline_frac": gbs / hbm_gbs, "launches_per_call": lpc})
     return out
 
 
@@ -527,6 +565,13 @@ def run_only(args):
     if args.batch:
         w = dataclasses.replace(w, B=args.batch)
     stream = torch.cuda.Stream()
+    if args.backward:
+        ms, lpc, alg = time_backward(la, w, args.steps, args.warmup, stream)
+        gbs = alg / (ms * 1e-3) / 1e9
+        print(json.dumps({"workload": w.name, "B": w.B, "mode": "backward", "ms": ms,
+                          "tokens_per_s": w.B * w.T / (ms * 1e-3), "alg_bytes": alg, "achieved_GBps": gbs,
+                          "roofline_frac": gbs / peaks()["hbm_gbs"], "launches_per_call": lpc}), flush=True)
+        return
     causal = not args.noncausal
     ms, lpc = time_workload(la, w, args.steps, args.warmup, stream, causal)
     alg = prefill_alg_bytes(w)
@@ -570,6 +615,7 @@ def main():
     ap.add_argument("--only", default=None, help="time one workload of linattn_inputs (e.g. LONG_8K) alone")
     ap.add_argument("--batch", type=int, default=0, help="with --only: batch size override")
     ap.add_argument("--noncausal", action="store_true", help="with --only: the non-causal pass")
+    ap.add_argument("--backward", action="store_true", help="with --only: the backward pass (linear rule)")
     ap.add_argument("--decode-only", action="store_true", help="time the decode step alone (see --prompt)")
     ap.add_argument("--prompt", type=int, default=64, help="with --decode-only: prompt tokens that build the state")
     args = ap.parse_args()

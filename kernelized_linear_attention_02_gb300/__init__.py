@@ -309,6 +309,10 @@ def la_decode_step(q, k, v, S, Z=None, *, q_heads, kv_heads, feature_map="elu_pl
     return y
 
 
+def la_backward_workspace_bytes(params: la_params) -> int:
+    return int(lib().la_backward_workspace_bytes(ctypes.byref(params)))
+
+
 def la_backward_causal(q, k, v, dy, *, q_heads, kv_heads, feature_map="elu_plus_one", use_normalizer=True,
                        epsilon=1e-6, scale=1.0, initial_state=None, grad_dtype=torch.float32,
                        return_state_grad=False, workspace=None, stream=None):
@@ -330,7 +334,7 @@ def la_backward_causal(q, k, v, dy, *, q_heads, kv_heads, feature_map="elu_plus_
     if return_state_grad:
         dS0 = torch.empty(B, kv_heads, Dk, Dv, dtype=torch.float32, device=q.device)
         dZ0 = torch.empty(B, kv_heads, Dk, dtype=torch.float32, device=q.device) if use_normalizer else None
-    need = int(lib().la_backward_workspace_bytes(ctypes.byref(p)))
+    need = la_backward_workspace_bytes(p)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(max(1, need), dtype=torch.uint8, device=q.device)
     _check(lib().la_backward_causal(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(S0), _ptr(Z0), _ptr(dy), _ptr(dq),
