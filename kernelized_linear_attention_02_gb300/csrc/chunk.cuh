@@ -161,6 +161,11 @@ struct Cfg {
 // Rounds a shared-memory pointer up to 1024 bytes by pointer arithmetic (not
 // through an integer), so the compiler still knows it addresses shared memory
 // and emits shared loads/stores instead of generic ones.
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
@@ -1263,13 +1268,17 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                 // iterations (the roles of this kernel share each sub-partition's
                 // instruction cache, so straight-line code would be fetched anew
                 // every chunk).
+                // kDrop: the chunk holds invalid steps (mask), dropped row by row;
+                // a chunk whose steps are all valid runs the unmasked loop
+                auto conv_rows = [&](auto drop_tag) {
+                constexpr bool kDrop = decltype(drop_tag)::value;
                 uint4 nxt = *reinterpret_cast<const uint4*>(Kb(s) + chunk_off(0, Cf::kKBlk));
 #pragma unroll 1
                 for (int m = 0; m < kPer; ++m) {
                     const int row = rbase + kRowStep * m;
                     const uint4 cur = nxt;
                     if (m + 1 < kPer) nxt = *reinterpret_cast<const uint4*>(Kb(s) + chunk_off(m + 1, Cf::kKBlk));
-                    const bool drop = !((okw >> row) & 1);
+                    const bool drop = kDrop && !((okw >> row) & 1);
                     if (drop) {
                         *reinterpret_cast<uint4*>(Kb(s) + chunk_off(m, Cf::kKBlk)) = make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4*>(Vb(s) + chunk_off(m)) = make_uint4(0, 0, 0, 0);
@@ -1296,6 +1305,24 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
 #pragma unroll
                             for (int e = 0; e < 8; ++e) colsum[e] += f[e];
                     }
+                }
+                };
+                if (!mask || okw == ~0ull) {
+                    conv_rows(BoolTag<false>{});
+                } else if (okw == 0ull) {
+                    // every step of the chunk invalid: zero key and value rows only
+#pragma unroll 1
+                    for (int m = 0; m < kPer; ++m) {
+                        const uint4 z = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(Kb(s) + chunk_off(m, Cf::kKBlk)) = z;
+                        *reinterpret_cast<uint4*>(Vb(s) + chunk_off(m)) = z;
+                        if (GATED) {
+                            *reinterpret_cast<uint4*>(Kd(s) + chunk_off(m)) = z;
+                            *reinterpret_cast<uint4*>(Klo(s) + chunk_off(m)) = z;
+                        }
+                    }
+                } else {
+                    conv_rows(BoolTag<true>{});
                 }
                 if (ct == 0) LA_TR(2, 8, i);
                 if (NORM) {
