@@ -15,9 +15,16 @@
 //   dS0 = R_0, dZ0 = r_0.
 // Pass 1 walks the tokens forward with (S, Z) and writes dq and (ds, dd) to
 // the workspace; pass 2 walks them backward with (R, r) and writes dk, dv and
-// the gradients of the initial state.  One CTA per (batch, kv head) stream;
+// the gradients of the initial state.  When few streams would leave most SMs
+// idle, the sequence is cut into segments (blockIdx.y): an increment pass
+// gives each segment's (dS, dZ) from zero, pass 1 folds the earlier
+// segments' increments onto the initial state; a reverse increment pass gives
+// each segment's (dR, dr), pass 2 starts from the sum over the later
+// segments.  One CTA per (batch, kv head) stream and segment;
 // warp w holds rows w, w + 8, ... of the Dk x Dv matrix, lane c columns c,
 // c + 32, ... (Dk, Dv <= 128), as in the forward recurrence.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -44,6 +51,14 @@ struct BwdArgs {
     float* ds;  // workspace (B, T, Hq, Dv)
     float* dd;  // workspace (B, T, Hq)
     Problem P;
+    // sequence segments along blockIdx.y: steps [seg * cps, min(T, (seg + 1) * cps))
+    int64_t cps;
+    int nseg;
+    float* S_seg;  // (B*Hkv, nseg, Dk, Dv) state increment of each segment
+    float* Z_seg;  // (B*Hkv, nseg, Dk)
+    float* R_seg;  // (B*Hkv, nseg, Dk, Dv) reverse increment sum_i a_i ds_i^T of each segment
+    float* r_seg;  // (B*Hkv, nseg, Dk)
+    int inc_only;  // increment pass: walk the segment from zero and write its increment only
 };
 
 // derivative of the feature map (Keras request, Feature maps): elu(x) + 1 has
@@ -76,8 +91,10 @@ __global__ void __launch_bounds__(kThreads) bwd_forward_kernel(BwdArgs a) {
     const TIn* dy = static_cast<const TIn*>(a.dy);
     TOut* dq = static_cast<TOut*>(a.dq);
 
+    const int seg = blockIdx.y;
+    const int64_t t_begin = seg * a.cps, t_end = min(P.T, t_begin + a.cps);
     float s[kRows][kCols];
-    const float* S0 = a.S0 ? a.S0 + bh * (int64_t)Dk * Dv : nullptr;
+    const float* S0 = a.S0 && !a.inc_only ? a.S0 + bh * (int64_t)Dk * Dv : nullptr;
 #pragma unroll
     for (int m = 0; m < kRows; ++m)
 #pragma unroll
@@ -85,10 +102,22 @@ __global__ void __launch_bounds__(kThreads) bwd_forward_kernel(BwdArgs a) {
             const int i = warp + 8 * m, j = lane + 32 * n;
             s[m][n] = (S0 && i < Dk && j < Dv) ? S0[(int64_t)i * Dv + j] : 0.f;
         }
-    if (tid < 128) Zs[tid] = (P.norm && a.Z0 && tid < Dk) ? a.Z0[bh * Dk + tid] : 0.f;
+    if (tid < 128) Zs[tid] = (P.norm && a.Z0 && !a.inc_only && tid < Dk) ? a.Z0[bh * Dk + tid] : 0.f;
+    if (!a.inc_only)  // the state at the segment start: the earlier segments' increments
+        for (int p = 0; p < seg; ++p) {
+            const float* Sp = a.S_seg + ((int64_t)bh * a.nseg + p) * Dk * Dv;
+#pragma unroll
+            for (int m = 0; m < kRows; ++m)
+#pragma unroll
+                for (int n = 0; n < kCols; ++n) {
+                    const int i = warp + 8 * m, j = lane + 32 * n;
+                    if (i < Dk && j < Dv) s[m][n] += Sp[(int64_t)i * Dv + j];
+                }
+            if (P.norm && tid < Dk) Zs[tid] += a.Z_seg[((int64_t)bh * a.nseg + p) * Dk + tid];
+        }
     __syncthreads();
 
-    for (int64_t t = 0; t < P.T; ++t) {
+    for (int64_t t = t_begin; t < t_end; ++t) {
         const int64_t tok = b * P.T + t;
         if (tid < Dk) fk[tid] = phi<false>(P.fmap, load_in(k, (tok * P.Hkv + hk) * Dk + tid), P.eps);
         float vj[kCols];
@@ -106,7 +135,7 @@ __global__ void __launch_bounds__(kThreads) bwd_forward_kernel(BwdArgs a) {
             for (int n = 0; n < kCols; ++n) s[m][n] = fmaf(f, vj[n], s[m][n]);
         }
         if (P.norm && tid < Dk) Zs[tid] += fk[tid];
-        for (int r = 0; r < G; ++r) {
+        for (int r = 0; r < G && !a.inc_only; ++r) {
             const int64_t hq = tok * P.Hq + hk * G + r;
             __syncthreads();  // Zs and the previous head's av/dsv consumed
             if (tid < Dk) av[tid] = phi<false>(P.fmap, load_in(q, hq * Dk + tid), P.eps);
@@ -175,6 +204,17 @@ __global__ void __launch_bounds__(kThreads) bwd_forward_kernel(BwdArgs a) {
         }
         __syncthreads();  // fk, av, dsv reused by the next token
     }
+    if (a.inc_only) {  // this segment's state increment
+        float* So = a.S_seg + ((int64_t)bh * a.nseg + seg) * Dk * Dv;
+#pragma unroll
+        for (int m = 0; m < kRows; ++m)
+#pragma unroll
+            for (int n = 0; n < kCols; ++n) {
+                const int i = warp + 8 * m, j = lane + 32 * n;
+                if (i < Dk && j < Dv) So[(int64_t)i * Dv + j] = s[m][n];
+            }
+        if (P.norm && tid < Dk) a.Z_seg[((int64_t)bh * a.nseg + seg) * Dk + tid] = Zs[tid];
+    }
 }
 
 template <typename TIn, typename TOut>
@@ -191,15 +231,31 @@ __global__ void __launch_bounds__(kThreads) bwd_reverse_kernel(BwdArgs a) {
     TOut* dk = static_cast<TOut*>(a.dk);
     TOut* dv = static_cast<TOut*>(a.dv);
 
+    // segment `seg` of the reverse pass; the increment pass runs segments
+    // 1 .. nseg-1 (blockIdx.y + 1), the full pass segments 0 .. nseg-1
+    const int seg = blockIdx.y + (a.inc_only ? 1 : 0);
+    const int64_t t_begin = seg * a.cps, t_end = min(P.T, t_begin + a.cps);
     float R[kRows][kCols];
 #pragma unroll
     for (int m = 0; m < kRows; ++m)
 #pragma unroll
         for (int n = 0; n < kCols; ++n) R[m][n] = 0.f;
     if (tid < 128) rs[tid] = 0.f;
+    if (!a.inc_only)  // R at the segment end: the later segments' increments
+        for (int p = seg + 1; p < a.nseg; ++p) {
+            const float* Rp = a.R_seg + ((int64_t)bh * a.nseg + p) * Dk * Dv;
+#pragma unroll
+            for (int m = 0; m < kRows; ++m)
+#pragma unroll
+                for (int n = 0; n < kCols; ++n) {
+                    const int i = warp + 8 * m, j = lane + 32 * n;
+                    if (i < Dk && j < Dv) R[m][n] += Rp[(int64_t)i * Dv + j];
+                }
+            if (P.norm && tid < Dk) rs[tid] += a.r_seg[((int64_t)bh * a.nseg + p) * Dk + tid];
+        }
     __syncthreads();
 
-    for (int64_t t = P.T - 1; t >= 0; --t) {
+    for (int64_t t = t_end - 1; t >= t_begin; --t) {
         const int64_t tok = b * P.T + t;
         if (tid < Dk) fk[tid] = phi<false>(P.fmap, load_in(k, (tok * P.Hkv + hk) * Dk + tid), P.eps);
         float vj[kCols];
@@ -230,6 +286,7 @@ __global__ void __launch_bounds__(kThreads) bwd_reverse_kernel(BwdArgs a) {
             }
             __syncthreads();  // av / dsv reused by the next block of heads
         }
+        if (a.inc_only) continue;  // uniform: the increment pass needs no outputs
         // d phi(k)_i = sum_j R_ij v_j + r_i (across lanes); dv_j = sum_i R_ij phi(k)_i (across warps)
         float pv[kCols] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -260,7 +317,19 @@ __global__ void __launch_bounds__(kThreads) bwd_reverse_kernel(BwdArgs a) {
         }
         __syncthreads();  // fk, red, rs reused by the previous token
     }
-    if (a.dS0) {
+    if (a.inc_only) {  // this segment's reverse increment
+        float* o = a.R_seg + ((int64_t)bh * a.nseg + seg) * Dk * Dv;
+#pragma unroll
+        for (int m = 0; m < kRows; ++m)
+#pragma unroll
+            for (int n = 0; n < kCols; ++n) {
+                const int i = warp + 8 * m, j = lane + 32 * n;
+                if (i < Dk && j < Dv) o[(int64_t)i * Dv + j] = R[m][n];
+            }
+        if (P.norm && tid < Dk) a.r_seg[((int64_t)bh * a.nseg + seg) * Dk + tid] = rs[tid];
+        return;
+    }
+    if (a.dS0 && seg == 0) {
         float* o = a.dS0 + bh * (int64_t)Dk * Dv;
 #pragma unroll
         for (int m = 0; m < kRows; ++m)
@@ -270,27 +339,73 @@ __global__ void __launch_bounds__(kThreads) bwd_reverse_kernel(BwdArgs a) {
                 if (i < Dk && j < Dv) o[(int64_t)i * Dv + j] = R[m][n];
             }
     }
-    if (a.dZ0 && P.norm && tid < Dk) a.dZ0[bh * Dk + tid] = rs[tid];
+    if (a.dZ0 && P.norm && seg == 0 && tid < Dk) a.dZ0[bh * Dk + tid] = rs[tid];
 }
 
 template <typename TIn, typename TOut>
 cudaError_t launch(const BwdArgs& a, cudaStream_t st) {
-    const dim3 grid((unsigned)(a.P.B * a.P.Hkv));
-    bwd_forward_kernel<TIn, TOut><<<grid, kThreads, 0, st>>>(a);
-    note_launch();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    bwd_reverse_kernel<TIn, TOut><<<grid, kThreads, 0, st>>>(a);
-    note_launch();
-    return cudaGetLastError();
+    const unsigned streams = (unsigned)(a.P.B * a.P.Hkv);
+    auto run = [&](auto kern, const BwdArgs& x, int ny) -> cudaError_t {
+        kern<<<dim3(streams, (unsigned)ny), kThreads, 0, st>>>(x);
+        note_launch();
+        return cudaGetLastError();
+    };
+    cudaError_t e;
+    if (a.nseg > 1) {  // increments of segments 0 .. nseg-2 (forward)
+        BwdArgs x = a;
+        x.inc_only = 1;
+        if ((e = run(bwd_forward_kernel<TIn, TOut>, x, a.nseg - 1)) != cudaSuccess) return e;
+    }
+    if ((e = run(bwd_forward_kernel<TIn, TOut>, a, a.nseg)) != cudaSuccess) return e;
+    if (a.nseg > 1) {  // reverse increments of segments 1 .. nseg-1
+        BwdArgs x = a;
+        x.inc_only = 1;
+        if ((e = run(bwd_reverse_kernel<TIn, TOut>, x, a.nseg - 1)) != cudaSuccess) return e;
+    }
+    return run(bwd_reverse_kernel<TIn, TOut>, a, a.nseg);
+}
+
+// Segments: enough to give most SMs a CTA when the streams alone do not, at
+// least 256 steps each, at most 8 MiB of segment scratch.
+constexpr size_t kSegCap = (size_t)8 << 20;
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int bwd_segments(const Problem& P) {
+    if (P.T < 512) return 1;
+    const int64_t streams = P.B * P.Hkv;
+    const int sms = device_sm_count();
+    if (sms <= 0 || streams * 2 > sms) return 1;
+    int64_t n = std::min<int64_t>(sms / streams, P.T / 256);
+    const size_t per = sizeof(float) * (size_t)streams * (2 * (size_t)P.Dk * P.Dv + 2 * (size_t)P.Dk);
+    n = std::min<int64_t>(n, (int64_t)(kSegCap / per));
+    if (n < 2) return 1;
+    const int64_t cps = (P.T + n - 1) / n;
+    return (int)((P.T + cps - 1) / cps);
+}
+
+struct BwdLayout {
+    size_t ds, dd, S, Z, R, r, total;
+};
+BwdLayout bwd_layout(const Problem& P, int nseg) {
+    const size_t n = (size_t)P.B * P.T * P.Hq, streams = (size_t)(P.B * P.Hkv);
+    BwdLayout L{};
+    L.ds = 0;
+    L.dd = up256(sizeof(float) * n * P.Dv);
+    L.S = L.dd + up256(sizeof(float) * n);
+    if (nseg <= 1) {
+        L.Z = L.R = L.r = L.total = L.S;
+        return L;
+    }
+    L.Z = L.S + up256(sizeof(float) * streams * nseg * P.Dk * P.Dv);
+    L.R = L.Z + up256(sizeof(float) * streams * nseg * P.Dk);
+    L.r = L.R + up256(sizeof(float) * streams * nseg * P.Dk * P.Dv);
+    L.total = L.r + up256(sizeof(float) * streams * nseg * P.Dk);
+    return L;
 }
 
 }  // namespace
 
-size_t backward_workspace_bytes(const Problem& P) {
-    const size_t n = (size_t)P.B * P.T * P.Hq;
-    return ((sizeof(float) * n * P.Dv + 255) & ~(size_t)255) + sizeof(float) * n;
-}
+size_t backward_workspace_bytes(const Problem& P) { return bwd_layout(P, bwd_segments(P)).total; }
 
 cudaError_t backward_causal(const Problem& P, const void* q, const void* k, const void* v, const float* S0,
                             const float* Z0, const void* dy, void* dq, void* dk, void* dv, float* dS0, float* dZ0,
@@ -298,10 +413,19 @@ cudaError_t backward_causal(const Problem& P, const void* q, const void* k, cons
     BwdArgs a{};
     a.q = q, a.k = k, a.v = v, a.S0 = S0, a.Z0 = P.norm ? Z0 : nullptr, a.dy = dy;
     a.dq = dq, a.dk = dk, a.dv = dv, a.dS0 = dS0, a.dZ0 = P.norm ? dZ0 : nullptr;
-    const size_t n = (size_t)P.B * P.T * P.Hq;
-    a.ds = static_cast<float*>(ws);
-    a.dd = reinterpret_cast<float*>(static_cast<char*>(ws) + ((sizeof(float) * n * P.Dv + 255) & ~(size_t)255));
     a.P = P;
+    a.nseg = bwd_segments(P);
+    a.cps = (P.T + a.nseg - 1) / a.nseg;
+    const BwdLayout L = bwd_layout(P, a.nseg);
+    char* w = static_cast<char*>(ws);
+    a.ds = reinterpret_cast<float*>(w + L.ds);
+    a.dd = reinterpret_cast<float*>(w + L.dd);
+    if (a.nseg > 1) {
+        a.S_seg = reinterpret_cast<float*>(w + L.S);
+        a.Z_seg = reinterpret_cast<float*>(w + L.Z);
+        a.R_seg = reinterpret_cast<float*>(w + L.R);
+        a.r_seg = reinterpret_cast<float*>(w + L.r);
+    }
     if (P.io_bf16)
         return P.out_bf16 ? launch<__nv_bfloat16, __nv_bfloat16>(a, st) : launch<__nv_bfloat16, float>(a, st);
     return P.out_bf16 ? launch<float, __nv_bfloat16>(a, st) : launch<float, float>(a, st);

@@ -91,3 +91,32 @@ def test_backward_rejects_other_rules():
     d = ctypes.c_void_p(256)
     assert la.lib().la_backward_causal(ctypes.byref(p), d, d, d, None, None, d, d, d, d, None, None, d, 1 << 20,
                                        None) == la.LA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("shape", [(1, 1500, 2, 2, 64, 64), (2, 1100, 4, 2, 32, 48), (1, 800, 3, 1, 128, 128)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mode", [("elu_plus_one", True), ("relu", False)], ids=["elu-norm", "relu-raw"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_backward_sequence_segments(shape, mode, dtype):
+    """Long sequences with few streams: both scans run over sequence
+    segments, folded from the other segments' increments."""
+    B, T, Hq, Hkv, Dk, Dv = shape
+    fmap, norm = mode
+    std = 0.5 if fmap == "elu_plus_one" else 1.0
+    q = rand((B, T, Hq, Dk), 21, dtype, std)
+    k = rand((B, T, Hkv, Dk), 22, dtype, std)
+    v = rand((B, T, Hkv, Dv), 23, dtype)
+    dy = rand((B, T, Hq, Dv), 24, dtype)
+    S0 = rand((B, Hkv, Dk, Dv), 25, torch.float32)
+    Z0 = rand((B, Hkv, Dk), 26, torch.float32).abs() + 1.0 if norm else None
+    kw = dict(q_heads=Hq, kv_heads=Hkv, feature_map=fmap, use_normalizer=norm)
+    dq, dk, dv, dS0, dZ0 = la.la_backward_causal(q, k, v, dy, initial_state=(S0, Z0), return_state_grad=True, **kw)
+    torch.cuda.synchronize()
+    rq, rk, rv, rS0, rZ0 = og.causal_backward(q, k, v, dy, S0=S0, Z0=Z0, **kw)
+    tol = 2e-5
+    assert_close(to64(dq), rq.numpy(), tol, "dq")
+    assert_close(to64(dk), rk.numpy(), tol, "dk")
+    assert_close(to64(dv), rv.numpy(), tol, "dv")
+    assert_close(to64(dS0), rS0.numpy(), tol, "dS0")
+    if norm:
+        assert_close(to64(dZ0), rZ0.numpy(), tol, "dZ0")
