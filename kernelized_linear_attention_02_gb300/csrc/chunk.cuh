@@ -89,7 +89,12 @@ struct Cfg {
     static constexpr int kOffKlo = kOffKd + (GATED ? kTile : 0);
     static constexpr int kOffVb = kOffKlo + (kSplitK ? kTile : 0);
     static constexpr int kOffG = kOffVb + kTile;
-    static constexpr int kKvStage = kHasKV ? kOffG + (GATED ? 1024 : 0) : 0;  // G: gated rule only
+    static constexpr int kKvStage = kHasKV ? kOffG : 0;
+    // gated rule: the chunk's decay block (cumulative log decay, factored
+    // weights, reference, flag: 130 floats, 544 bytes) of each key/value stage,
+    // kept after the barriers so that the stages stay multiples of 1 KB
+    static constexpr int kGFloats = 136;
+    static constexpr int kGStage = (GATED && kHasKV) ? kGFloats * 4 : 0;
     // linear rule: the read-out with the carried state runs as kind::tf32
     // with the fp32 state straight from TMEM as A, against an fp32 copy of
     // phi(Q) (64 x D, D/32 swizzled blocks of 8 KB); the gated rule, whose
@@ -111,10 +116,13 @@ struct Cfg {
     static constexpr int kNAT = MODE == kCausal ? 1 : 0;
     static constexpr int kAT = kNAT * 2 * 8192;  // per buffer: hi, lo (64 x 64 bf16 each)
     static constexpr int kZrApply = (MODE == kApply && NORM) ? kZr : 0;
-    // linear rule, bf16 output: each item's 64 x D output tile is staged in
-    // shared memory and leaves with 16-byte stores
-    static constexpr bool kYStage = OUT_BF16 && !GATED && MODE != kState;
-    static constexpr int kYPitch = D + 8;  // tile row pitch in elements (16 bytes of padding)
+    // bf16 output: each item's 64 x D output tile is staged in shared memory
+    // and leaves with 16-byte stores.  Row pitch D + 8 elements (16 bytes of
+    // padding against bank conflicts of the head-size-64 transposed writes);
+    // the gated rule at head size 128, whose writes are 64 contiguous bytes
+    // per warp, uses the unpadded pitch to fit its budget
+    static constexpr bool kYStage = OUT_BF16 && MODE != kState;
+    static constexpr int kYPitch = (GATED && D == 128) ? D : D + 8;
     static constexpr int kYS = kYStage ? 64 * kYPitch * 2 : 0;
     // feature-map warps: 4 (warps 10-13), or 8 in the state pass (warps 6-13),
     // which has no scores for the epilogue warps to mask
@@ -127,9 +135,12 @@ struct Cfg {
     static constexpr int kPer = 64 / kRowStep;            // chunks per thread per tile
     static_assert(kRowStep * kPer == 64, "feature pass covers the tile");
     static constexpr int kZpart = kRowStep * D;  // floats of one buffer of partial Z sums
-    static constexpr int kMisc = 1024 + 2 * kZpart * 4 + 512;  // 1/den ring, partial Z sums (x2), barriers
+    // 1/den ring and partial Z sums (x2) -- the normalizer's, so not for the
+    // gated rule, which has none -- then the barriers
+    static constexpr int kMiscNorm = GATED ? 0 : 1024 + 2 * kZpart * 4;
+    static constexpr int kMisc = kMiscNorm + 512;
     static constexpr int bytes(int nkv, int nq) {
-        return 1024 + nkv * kKvStage + nq * kQStage + kAT + kZrApply + kYS + kMisc;
+        return 1024 + nkv * kKvStage + nq * kQStage + kAT + kZrApply + kYS + kMisc + nkv * kGStage;
     }
     static constexpr int kLimit = 227 * 1024;
     // ring depths: the deepest of (4,4), (3,3), (3,2), (2,2) that shared
@@ -226,9 +237,10 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
     uint8_t* zr_apply = at_base + Cf::kAT;
     uint8_t* ystage = zr_apply + Cf::kZrApply;  // staged output tile (64 x D bf16)
     float* misc = reinterpret_cast<float*>(ystage + Cf::kYS);
-    float* inv_den = misc;           // [4][64] scale / den of the last four items
-    float* zpart = misc + 256;       // [2][kZpart] partial column sums of phi(K)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + 256 + 2 * Cf::kZpart);
+    float* inv_den = misc;           // [4][64] scale / den of the last four items (normalizer)
+    float* zpart = misc + 256;       // [2][kZpart] partial column sums of phi(K) (normalizer)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + Cf::kMiscNorm / 4);
+    float* garea = reinterpret_cast<float*>(bars + 64);  // gated: [NKV][kGFloats] decay blocks
     uint64_t* full_kv = bars;        // [4] ring stages
     uint64_t* empty_kv = bars + 4;   // [4]
     uint64_t* conv_kv = bars + 8;    // [4]
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
     auto zr_at = [&](int s, int kb) -> uint8_t* {
         return MODE == kApply ? zr_apply + kb * 1024 : kv_base + s * Cf::kKvStage + kb * Cf::kKBlk + 64 * 128;
     };
-    auto Gc = [&](int s) { return reinterpret_cast<float*>(kv_base + s * Cf::kKvStage + Cf::kOffG); };
+    auto Gc = [&](int s) { return garea + s * Cf::kGFloats; };
     auto Qb = [&](int s) { return q_base + s * Cf::kQStage; };
     auto Qd = [&](int s) { return q_base + s * Cf::kQStage + Cf::kTile; };
     auto Qf = [&](int s) { return q_base + s * Cf::kQStage + Cf::kTile; };  // fp32 phi(Q) (linear rule)

@@ -142,6 +142,15 @@ def test_gated_small(shape, dtype):
              scale=0.0, seed=7)
 
 
+@pytest.mark.parametrize("shape", SHAPES + [(1, 192, 32, 2, 64, 64), (2, 129, 16, 1, 128, 128)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gated_small_bf16_output(shape):
+    """Gated rule with a bf16 output: the staged 16-byte output stores."""
+    B, T, Hq, Hkv, Dk, Dv = shape
+    run_case(B, T, Hq, Hkv, Dk, Dv, torch.bfloat16, torch.bfloat16, "none", False, rule="gated", S0=True,
+             scale=0.0, seed=9)
+
+
 @pytest.mark.parametrize("shape", [(2, 200, 4, 2, 64, 64), (1, 257, 8, 2, 128, 128)], ids=lambda s: "x".join(map(str, s)))
 def test_gated_strong_decay(shape):
     """Log decay near -5 per token: a 64-token chunk spans several hundred in
