@@ -84,7 +84,8 @@ struct Cfg {
     static constexpr int kKRows = (NORM && MODE == kCausal) ? 72 : 64;
     static constexpr int kKBlk = kKRows * 128;  // bytes per 64-feature block of the key tile
     static constexpr int kKTile = (D / 64) * kKBlk;
-    // per KV stage: Kb (+ Z rows) | Kd (gated) | Klo (split) | Vb | G (256 B, padded)
+    // per KV stage: Kb (+ Z rows) | Kd (gated) | Klo (split) | Vb; the gated
+    // rule's decay block of each stage lives after the barriers (kGStage)
     static constexpr int kOffKd = ((kKTile + 1023) / 1024) * 1024;
     static constexpr int kOffKlo = kOffKd + (GATED ? kTile : 0);
     static constexpr int kOffVb = kOffKlo + (kSplitK ? kTile : 0);
