@@ -383,11 +383,61 @@ def pin_grad_finite_differences(lib=None, seed=12):
         assert torch.autograd.gradcheck(f, (q, k, v, S0, Z0), eps=1e-6, atol=1e-7, rtol=1e-5)
 
 
+def pin_delta_overwrite(lib=None, seed=13):
+    """ONNX-light "LinearAttention", update rule delta: with beta = 1 and a
+    unit key, S_t = S_{t-1} + k (v - S_{t-1}^T k)^T stores v at k exactly
+    (S_t^T k = v), overwriting what the key held.  With orthonormal keys
+    (basis vectors, some repeated) and the query equal to the key, every
+    output is scale * v_t, and the final state maps each key to the last
+    value written at it."""
+    rng = np.random.default_rng(seed)
+    Dk, Dv, T = 4, 3, 7
+    order = [0, 1, 2, 1, 3, 0, 2]  # keys e_0, e_1, e_2, e_1 again, ...
+    k = np.zeros((1, T, 1, Dk))
+    for t, i in enumerate(order):
+        k[0, t, 0, i] = 1.0
+    v = rng.standard_normal((1, T, 1, Dv))
+    beta = np.ones((1, T, 1))
+    S0 = rng.standard_normal((1, 1, Dk, Dv))
+    y, S, _ = oracle.causal(k.copy(), k, v, q_heads=1, kv_heads=1, feature_map="none", use_normalizer=False,
+                            scale=0.5, rule="delta", beta=beta, S0=S0, lib=lib)
+    np.testing.assert_allclose(y[0, :, 0], 0.5 * v[0, :, 0], rtol=1e-13, atol=1e-13)
+    last = {}
+    for t, i in enumerate(order):
+        last[i] = v[0, t, 0]
+    for i in range(Dk):
+        np.testing.assert_allclose(S[0, 0, i], last[i], rtol=1e-13, atol=1e-13)
+
+
+def pin_gated_delta_without_decay_is_delta(lib=None, seed=14):
+    """gated_delta with g = 0 (no decay) equals delta; a decay of -inf before
+    step t forgets the earlier state, so step t starts from S = 0."""
+    rng = np.random.default_rng(seed)
+    B, T, Hq, Hkv, D = 1, 9, 2, 1, 4
+    q = rng.standard_normal((B, T, Hq, D))
+    k = rng.standard_normal((B, T, Hkv, D))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, Hkv, D))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((B, T, Hkv))))
+    kw = dict(q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False, beta=beta, lib=lib)
+    yd, Sd, _ = oracle.causal(q, k, v, rule="delta", **kw)
+    yg, Sg, _ = oracle.causal(q, k, v, rule="gated_delta", decay=np.zeros((B, T, Hkv)), **kw)
+    np.testing.assert_allclose(yg, yd, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(Sg, Sd, rtol=1e-13, atol=1e-13)
+    g = np.zeros((B, T, Hkv))
+    g[0, 4] = -800.0
+    yg, _, _ = oracle.causal(q, k, v, rule="gated_delta", decay=g, **kw)
+    kw2 = dict(kw, beta=beta[:, 4:])
+    ys, _, _ = oracle.causal(q[:, 4:], k[:, 4:], v[:, 4:], rule="delta", **kw2)
+    np.testing.assert_allclose(yg[:, 4:], ys, rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [pin_paper_mean_abs_diff, pin_recurrence_vs_bruteforce, pin_noncausal_vs_bruteforce,
             pin_last_row_equals_noncausal, pin_chunked_equals_full, pin_state_closed_form,
             pin_first_token, pin_feature_map_values, pin_constant_value, pin_gated_reductions,
             pin_gqa_equals_repeated_mha, pin_scale, pin_mask_causal, pin_mask_noncausal,
-            pin_grad_forward_matches_recurrence, pin_grad_finite_differences]
+            pin_grad_forward_matches_recurrence, pin_grad_finite_differences, pin_delta_overwrite,
+            pin_gated_delta_without_decay_is_delta]
 
 
 def run_all(lib=None):
