@@ -126,3 +126,75 @@ def test_status_strings(L):
     for s in range(5):
         assert L.la_status_string(s)
     assert L.la_abi_version() == 2
+
+
+# ---- entry points added with the masks, the delta rules and the backward pass:
+# each rejects bad arguments before it enqueues anything (no GPU needed)
+
+def _delta(**kw):
+    base = dict(feature_map="none", use_normalizer=False, update_rule="delta")
+    base.update(kw)
+    return _p(**base)
+
+
+def test_plain_calls_refuse_the_delta_rules(L):
+    p = _delta()
+    d = ctypes.c_void_p(16)
+    assert L.la_forward_causal(ctypes.byref(p), d, d, d, None, None, None, d, None, None, None, 0,
+                               None) == la.LA_ERR_INVALID_ARG
+    assert "la_forward_causal_delta" in L.la_last_error().decode()
+    p1 = _delta(seq_len=1)
+    assert L.la_decode_step(ctypes.byref(p1), d, d, d, None, d, None, d, None) == la.LA_ERR_INVALID_ARG
+
+
+def test_delta_entry_point_checks(L):
+    d = ctypes.c_void_p(16)
+    call = lambda p, beta, bph=1, decay=None: L.la_forward_causal_delta(ctypes.byref(p), d, d, d, decay, beta, bph,
+                                                                        None, None, d, None, None)
+    assert call(_delta(), None) == la.LA_ERR_INVALID_ARG                     # beta missing
+    assert call(_delta(), d, bph=2) == la.LA_ERR_INVALID_ARG                 # beta layout flag
+    assert call(_delta(update_rule="gated_delta"), d) == la.LA_ERR_INVALID_ARG  # gated_delta without decay
+    assert call(_delta(update_rule="linear"), d) == la.LA_ERR_INVALID_ARG    # not a delta rule
+    assert call(_delta(feature_map="elu_plus_one"), d) == la.LA_ERR_UNSUPPORTED
+    assert call(_delta(use_normalizer=True, feature_map="none"), d) == la.LA_ERR_UNSUPPORTED
+    p2 = _delta(seq_len=2)
+    assert L.la_decode_step_delta(ctypes.byref(p2), d, d, d, None, d, 1, None, d, d, None) == la.LA_ERR_INVALID_ARG
+    p1 = _delta(seq_len=1)
+    assert L.la_decode_step_delta(ctypes.byref(p1), d, d, d, None, d, 1, None, None, d, None) == la.LA_ERR_INVALID_ARG
+
+
+def test_masked_entry_points_validate_like_the_plain_ones(L):
+    d = ctypes.c_void_p(16)
+    p = _p(batch=0)
+    assert L.la_forward_causal_masked(ctypes.byref(p), d, d, d, None, d, None, None, d, None, None, None, 0,
+                                      None) == la.LA_ERR_INVALID_ARG
+    assert L.la_forward_noncausal_masked(ctypes.byref(p), d, d, d, d, d, None, 0, None) == la.LA_ERR_INVALID_ARG
+    p = _p(seq_len=3)
+    assert L.la_decode_step_masked(ctypes.byref(p), d, d, d, None, d, d, d, d, None) == la.LA_ERR_INVALID_ARG
+
+
+def test_backward_checks(L):
+    d = ctypes.c_void_p(256)
+    p = _p(update_rule="gated", feature_map="none", use_normalizer=False)
+    assert L.la_backward_causal(ctypes.byref(p), d, d, d, None, None, d, d, d, d, None, None, d, 1 << 20,
+                                None) == la.LA_ERR_UNSUPPORTED
+    p = _p()
+    need = L.la_backward_workspace_bytes(ctypes.byref(p))
+    assert need > 0
+    assert L.la_backward_causal(ctypes.byref(p), d, d, d, None, None, d, d, d, d, None, None, d, need - 1,
+                                None) == la.LA_ERR_WORKSPACE
+    assert L.la_backward_causal(ctypes.byref(p), d, d, d, None, None, None, d, d, d, None, None, d, need,
+                                None) == la.LA_ERR_INVALID_ARG  # dy missing
+
+
+def test_decay_per_key_dim_accepted_only_for_gated_rules(L):
+    d = ctypes.c_void_p(16)
+    p = _p(update_rule="gated", feature_map="none", use_normalizer=False, decay_per_key_dim=True)
+    # valid parameters: only the missing decay is reported
+    assert L.la_forward_causal(ctypes.byref(p), d, d, d, None, None, None, d, None, None, None, 0,
+                               None) == la.LA_ERR_INVALID_ARG
+    assert "decay" in L.la_last_error().decode()
+    p = _p(decay_per_key_dim=True)
+    assert L.la_forward_causal(ctypes.byref(p), d, d, d, d, None, None, d, None, None, None, 0,
+                               None) == la.LA_ERR_INVALID_ARG
+    assert "gated" in L.la_last_error().decode()
