@@ -56,14 +56,15 @@
 extern "C" {
 #endif
 
-#define LINATTN_ABI_VERSION 2
+#define LINATTN_ABI_VERSION 3
 
 typedef enum la_status {
     LA_OK = 0,
     LA_ERR_INVALID_ARG = 1,  /* bad size, null pointer, bad enum, Hq % Hkv != 0 ... */
     LA_ERR_UNSUPPORTED = 2,  /* a valid combination the library does not implement */
     LA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than la_workspace_bytes() */
-    LA_ERR_CUDA = 4          /* a CUDA runtime error while enqueueing */
+    LA_ERR_CUDA = 4,         /* a CUDA runtime error while enqueueing */
+    LA_ERR_TIMEOUT = 5       /* la_device_status: a kernel gave up on a bounded wait */
 } la_status;
 
 typedef enum la_dtype { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
@@ -254,8 +255,10 @@ la_status la_backward_causal(const la_params* p, const void* q, const void* k, c
                              const float* Z0, const void* dy, void* dq, void* dk, void* dv, float* dS0, float* dZ0,
                              void* ws, size_t ws_bytes, la_stream_t stream);
 
-/* Static string for a status code. */
+/* Static string for a status code.  la_status_str is the same function
+ * under its short name. */
 const char* la_status_string(la_status s);
+const char* la_status_str(la_status s);
 
 /* One-line description of the last failure on this host thread ("" if none). */
 const char* la_last_error(void);
@@ -268,6 +271,27 @@ int la_abi_version(void);
  * bit instead of hanging); a nonzero value names the wait sites that timed
  * out.  Synchronous (device-to-host copy).  reset != 0 clears it. */
 unsigned la_device_error(int reset);
+
+/* The same check as a status: synchronises the current device, then
+ * LA_ERR_TIMEOUT when the error word is nonzero (la_last_error names the
+ * word), LA_ERR_CUDA when the device reports an error, else LA_OK.
+ * reset != 0 clears the word. */
+la_status la_device_status(int reset);
+
+/* Bits of the device error word set by la_check_bounded_wait. */
+#define LA_SELFTEST_WARP_WAIT (1u << 30)
+#define LA_SELFTEST_THREAD_WAIT (1u << 31)
+
+/* Failure-path check of the bounded waits (no counterpart on the pages: it
+ * tests the library's own failure detection).  Enqueues one small kernel
+ * whose two waits -- the warp-uniform form and the single-thread form that
+ * every pipeline wait of the tensor-core kernels uses -- poll an mbarrier
+ * that nothing ever completes, give up after limit_us microseconds (1 ..
+ * 1000000), set LA_SELFTEST_WARP_WAIT and LA_SELFTEST_THREAD_WAIT in the
+ * device error word (read and clear it with la_device_error) and return.
+ * The kernel holds no tensor memory and has no copy in flight, so the
+ * context stays usable.  LA_ERR_INVALID_ARG for a limit out of range. */
+la_status la_check_bounded_wait(uint32_t limit_us, la_stream_t stream);
 
 /* Number of CUDA kernels this library has enqueued in this process so far
  * (memsets and copies are not counted).  For accounting in benchmarks. */

@@ -10,7 +10,6 @@ or PyTorch fallback: if the library is missing every call raises.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 
 import torch
@@ -18,7 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblinattn.so")
 
-LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA = range(5)
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(6)
 LA_F32, LA_BF16 = 0, 1
 LA_NOALLOC_SCRATCH_BYTES = 16 << 20  # built-in scratch of la_forward_causal_noalloc
 FEATURE_MAPS = {"none": 0, "elu_plus_one": 1, "relu": 2}
@@ -62,10 +61,13 @@ _SIGNATURES = {
     "la_backward_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(la_params)]),
     "la_backward_causal": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 12 + [ctypes.c_size_t, _vp]),
     "la_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "la_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "la_device_status": (ctypes.c_int, [ctypes.c_int]),
     "la_last_error": (ctypes.c_char_p, []),
     "la_abi_version": (ctypes.c_int, []),
     "la_launch_count": (ctypes.c_uint64, []),
     "la_device_error": (ctypes.c_uint, [ctypes.c_int]),
+    "la_check_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _vp]),
 }
 
 _lib = None
@@ -353,5 +355,18 @@ def la_device_error(reset: bool = True) -> int:
     return int(lib().la_device_error(int(bool(reset))))
 
 
-def resolve_scale(scale: float, key_dim: int) -> float:
-    return 1.0 / math.sqrt(key_dim) if scale == 0.0 else scale
+LA_SELFTEST_WARP_WAIT = 1 << 30
+LA_SELFTEST_THREAD_WAIT = 1 << 31
+
+
+def la_check_bounded_wait(limit_us: int = 1000, stream=None) -> None:
+    """Enqueue the bounded-wait self-test: both wait forms give up after
+    ``limit_us`` on a barrier nothing completes and set their bits in the
+    device error word (read it with ``la_device_error``)."""
+    _check(lib().la_check_bounded_wait(int(limit_us), _stream(stream)))
+
+
+def la_device_status(reset: bool = True) -> int:
+    """Synchronise the device and return LA_OK, or LA_ERR_TIMEOUT when a
+    kernel gave up on a bounded wait (LA_ERR_CUDA on a device error)."""
+    return int(lib().la_device_status(int(bool(reset))))

@@ -125,23 +125,27 @@ la_status check_ws(const la::Problem& P, bool causal, void* ws, size_t ws_bytes)
 // library's device image, so using it needs no allocation at call time.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-
-// Device address of g_noalloc_scratch on the current device, looked up on
-// the first call per device and cached.
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// (cudaGetSymbolAddress, with the device current) on the first call per
+// device and cached; a device reset gives the device a new context, and the
+// first call in it looks the address up again.
 cudaError_t noalloc_scratch(void** out) {
     static std::mutex mu;
-    static void* addr[kMaxDevices] = {};
+    static void* addr[la::kMaxDevices] = {};
+    static uint64_t ctx_of[la::kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= la::kMaxDevices) return cudaErrorInvalidDevice;
+    const uint64_t ctx = la::current_context_id();
     std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || ctx == 0 || ctx_of[dev] != ctx) {
         void* ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
         addr[dev] = ptr;
+        ctx_of[dev] = la::current_context_id();
     }
     *out = addr[dev];
     return cudaSuccess;
@@ -157,6 +161,14 @@ uint64_t la_launch_count(void) { return la::g_launches.load(std::memory_order_re
 
 unsigned la_device_error(int reset) { return la::chunk_device_error(reset != 0); }
 
+la_status la_check_bounded_wait(uint32_t limit_us, la_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return fail(LA_ERR_INVALID_ARG, "limit_us must be in 1 .. 1000000");
+    cudaError_t e = la::bounded_wait_selftest(limit_us, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "la_check_bounded_wait");
+    g_last_error.clear();
+    return LA_OK;
+}
+
 const char* la_last_error(void) { return g_last_error.c_str(); }
 
 const char* la_status_string(la_status s) {
@@ -166,8 +178,21 @@ const char* la_status_string(la_status s) {
     case LA_ERR_UNSUPPORTED: return "unsupported";
     case LA_ERR_WORKSPACE: return "workspace missing or too small";
     case LA_ERR_CUDA: return "CUDA error";
+    case LA_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
     }
     return "unknown status";
+}
+
+const char* la_status_str(la_status s) { return la_status_string(s); }
+
+la_status la_device_status(int reset) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "la_device_status");
+    const unsigned w = la::chunk_device_error(reset != 0);
+    if (w == ~0u) return fail(LA_ERR_CUDA, "la_device_status: the error word could not be read");
+    if (w) return fail(LA_ERR_TIMEOUT, "bounded waits gave up: error word 0x%08x", w);
+    g_last_error.clear();
+    return LA_OK;
 }
 
 la_status la_get_initial_state(const la_params* p, float* S, float* Z, la_stream_t stream) {

@@ -52,7 +52,6 @@
 
 #include "chunk_args.h"
 #include "common.cuh"
-#include "trace.cuh"
 #include "umma.cuh"
 
 namespace la {
@@ -64,6 +63,12 @@ constexpr int kC = 64;  // tokens per chunk
 // per-stage decay block (gated rule), floats: [0, 64) inclusive cumulative log
 // decay G_j, [64, 128) exp(ref - G_j), then ref and the "factored" flag
 constexpr int kGCol = 64, kGRef = 128, kGFlag = 129;
+// Floor of a step's log decay (gated rule).  exp(-200) underflows to zero in
+// float32 (the smallest subnormal is ~exp(-103.3)), so a step at the floor
+// erases the earlier state exactly as -inf does, as long as the later steps
+// of its 64-token chunk do not add up to more than +97 (log decays are
+// log-sigmoid values, <= 0, in every workload of the pages).
+constexpr float kMinLogDecay = -200.f;
 constexpr int kThreads = 480;  // 15 warps; the two-issuer kernel adds warp 15
 template <bool SPLIT>
 constexpr int block_threads() { return SPLIT ? 512 : kThreads; }
@@ -267,10 +272,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
     uint64_t* upd_done = bars + 52;   // state update of a chunk complete (split issue)
     uint64_t* out_group = bars + 55;  // barrier among the four output warps (staged output tile)
     uint32_t ophase = 0;              // this thread's uses of out_group
-#ifdef LA_TRACE
-    unsigned* la_trace_ctr = reinterpret_cast<unsigned*>(bars + 46);
-    if (threadIdx.x < 8) la_trace_ctr[threadIdx.x] = 0;
-#endif
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x;
@@ -365,7 +366,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) LA_TR(0, 0, 0);
     // state pass: the causal pass that consumes its increments may launch now
     // (programmatic dependent launch); it waits for this grid's completion
     // only where it reads them
@@ -388,7 +388,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
         };
         const int sq = n % NQ1;
         if (!warp_wait(&full_q[sq], (n / NQ1) & 1, err, kErrFullQ)) return false;
-        if (qt == 0) LA_TR(2, 3, n);
         if (fmap != LA_FMAP_NONE || GATED || TF32) {
             const float* gc = Gc(i % NKV1);
             uint4 nxt = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(0));
@@ -423,7 +422,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(&conv_q[sq]);
-        if (qt == 0) LA_TR(2, 4, n);
         return true;
     };
     constexpr bool kQOnEpi = MODE == kCausal && !GATED && !split;
@@ -450,7 +448,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
         const int yb = m % NY;
         if (!warp_wait(&y_full[yb], (m / NY) & 1, err, kErrYFull)) return false;
         tc_fence_after();
-        if (quad == 0 && lane == 0) LA_TR(4, 3, m);
         const uint64_t okw = valid_word(t0);  // invalid steps get zero output rows
         // all 64 tokens of this lane in one round trip to TMEM; the buffer is
         // released before the stores.  Head size 64 with a staged tile: Y^T is
@@ -473,7 +470,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
         if (lane == 0) mbar_arrive(&y_empty[yb]);
         // scale/den of item m, written by the four score warps
         if (NORM && !warp_wait(&den_full[m & 3], (m >> 2) & 1, err, kErrYFull)) return false;
-        if (quad == 0 && lane == 0) LA_TR(4, 4, m);
         const float4* idn4 = reinterpret_cast<const float4*>(inv_den + (m & 3) * 64);
         const size_t tstride = (size_t)Hq * D;
         const size_t base = (((size_t)b * T + t0) * Hq + hk * G + r_head) * D + vrow;
@@ -538,7 +534,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                 }
             }
         }
-        if (quad == 0 && lane == 0) LA_TR(4, 5, m);
         return true;
     };
 
@@ -553,7 +548,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     const int s = i % NKV1;
                     if (i >= NKV) ok = mbar_wait(&empty_kv[s], ((i / NKV1) & 1) ^ 1, err, kErrEmptyKV);
                     if (!ok) break;
-                    LA_TR(0, 1, i);
                     mbar_arrive_expect_tx(&full_kv[s], 2 * Cf::kTile);
                     for (int kb = 0; kb < D / 64; ++kb) {
                         tma_load_4d(Kb(s) + kb * Cf::kKBlk, &mapK, &full_kv[s], kb * 64, hk, t0, b);
@@ -565,7 +559,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         const int n = i * G + r, s = n % NQ1;
                         if (n >= NQ) ok = mbar_wait(&empty_q[s], ((n / NQ1) & 1) ^ 1, err, kErrEmptyQ);
                         if (!ok) break;
-                        LA_TR(0, 2, n);
                         mbar_arrive_expect_tx(&full_q[s], Cf::kTile);
                         for (int kb = 0; kb < D / 64; ++kb)
                             tma_load_4d(Qb(s) + kb * 8192, &mapQ, &full_q[s], kb * 64, hk * G + r, t0, b);
@@ -611,12 +604,10 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         ok = warp_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
                         if (!ok) break;
                         tc_fence_after();
-                        if (lead) LA_TR(1, 1, i);
                     }
                     ok = warp_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ);
                     if (!ok) break;
                     tc_fence_after();
-                    if (lead) LA_TR(1, 2, n);
                     if (n >= NA) {
                         ok = warp_wait(&a_empty[ab], ((n / NA) & 1) ^ 1, err, kErrAEmpty);
                         if (!ok) break;
@@ -633,14 +624,12 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     }
                     mma_commit(&a_full[ab], lead);
                     mma_commit(&empty_q[sq], lead);  // this warp is done with the query slot
-                    if (lead) LA_TR(1, 3, n);
                     ok = warp_wait(&at_full[tb], (n / NAT) & 1, err, kErrATFull);
                     if (!ok) break;
                     // the read-out of item n (warp 14) starts this Y^T buffer: complete first
                     ok = warp_wait(&inter_cmp[yb], (n / NY) & 1, err, kErrStateDone);
                     if (!ok) break;
                     tc_fence_after();
-                    if (lead) LA_TR(1, 7, n);
                     const uint32_t tY = tmem + Cf::kColY + 64 * yb;
 #pragma unroll 1
                     for (int ks = 0; ks < kC / 16; ++ks) {
@@ -649,7 +638,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         if (ALO) mma_ss(tY, av, sdesc_sw128(smem_u32(ATl(tb) + ks * 32), 16, 1024), id_intra, 1, lead);
                     }
                     mma_commit(&y_full[yb], lead);
-                    if (lead) LA_TR(1, 8, n);
                     if (r == G - 1) mma_commit(&empty_kv[s], lead);  // this warp is done with the K/V slot
                 }
                 mma_commit(final_done, lead);  // every operation of this warp complete
@@ -660,7 +648,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     ok = warp_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
                     if (!ok) break;
                     tc_fence_after();
-                    if (lead) LA_TR(1, 1, i);
                 }
                 if (MODE == kState) {
                     if (GATED || i == 0) {
@@ -680,7 +667,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     ok = warp_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ);
                     if (!ok) break;
                     tc_fence_after();
-                    if (lead) LA_TR(1, 2, n);
                     uint8_t* qop = GATED ? Qd(sq) : Qb(sq);  // operand of the inter read-out
                     const uint32_t tA = tmem + Cf::kColA + 80 * ab;
                     if (MODE == kCausal || NORM) {
@@ -689,7 +675,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                             if (!ok) break;
                             tc_fence_after();
                         }
-                        if (lead) LA_TR(1, 10, n);
                         if (MODE == kCausal) {
                             // scores, and in columns 64..71 phi(q).[Z_hi; Z_lo] from the Z rows
 #pragma unroll 1
@@ -708,9 +693,7 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                                        ks > 0, lead);
                             }
                         }
-                        if (lead) LA_TR(1, 11, n);
                         mma_commit(&a_full[ab], lead);
-                        if (lead) LA_TR(1, 3, n);
                     }
                     if (r == 0 && (MODE == kCausal || i == 0)) {
                         if (TF32 && MODE == kCausal && i > 0)  // the update of chunk i-1 has completed
@@ -720,13 +703,11 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                                            kErrStateReady);
                         if (!ok) break;
                         tc_fence_after();
-                        if (lead) LA_TR(1, 4, i);
                     }
                     if (n >= NY) {
                         ok = warp_wait(&y_empty[yb], ((n / NY) & 1) ^ 1, err, kErrYEmpty);
                         if (!ok) break;
                         tc_fence_after();
-                        if (lead) LA_TR(1, 5, n);
                     }
                     // inter: Y^T = S_prev^T . Q^T (tf32 from the fp32 state, or hi + lo)
                     const uint32_t tY = tmem + Cf::kColY + 64 * yb;
@@ -747,21 +728,18 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         }
                     }
                     mma_commit(&empty_q[sq], lead);
-                    if (lead) LA_TR(1, 6, n);
                     if (MODE == kCausal) {
                         if (!TF32 && r == G - 1) {
                             // every read-out of this chunk is issued (from the hi/lo
                             // copy): update the state now
                             issue_state_update(s);
                             mma_commit(state_done, lead);
-                            if (lead) LA_TR(1, 9, i);
                         }
                         if (TF32 && r == G - 1) mma_commit(inter_done, lead);
                         const int tb = n % NAT;
                         ok = warp_wait(&at_full[tb], (n / NAT) & 1, err, kErrATFull);
                         if (!ok) break;
                         tc_fence_after();
-                        if (lead) LA_TR(1, 7, n);
                         // intra: Y^T += V^T . A^T (hi [+ lo])
 #pragma unroll 1
                         for (int ks = 0; ks < kC / 16; ++ks) {
@@ -772,7 +750,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         }
                     }
                     mma_commit(&y_full[yb], lead);
-                    if (lead) LA_TR(1, 8, n);
                     if (TF32 && MODE == kCausal && r == G - 1) {
                         // the update overwrites the state that this chunk's read-outs
                         // take as their A operand: only after they have completed
@@ -781,7 +758,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         tc_fence_after();
                         issue_state_update(s);
                         mma_commit(state_done, lead);
-                        if (lead) LA_TR(1, 9, i);
                     }
                 }
                 if (!ok) break;
@@ -920,10 +896,8 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     gtot = Gc(s)[kC - 1];
                 }
                 tc_fence_after();
-                if (st_t == 0) LA_TR(2, 5, i);
                 convert_state(GATED ? __expf(gtot) : 1.f, GATED);
                 publish_state();
-                if (st_t == 0) LA_TR(2, 6, i);
                 if (MODE == kState) gsum += gtot;
                 if (kOut && i > 0)
                     for (int r = max(0, G - 2); r < G && ok; ++r) ok = emit_y((i - 1) * G + r);
@@ -982,7 +956,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     ok = warp_wait(&a_full[ab], (n / NA) & 1, err, kErrAFull);
                     if (!ok) break;
                     tc_fence_after();
-                    if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 1, n);
                     const uint32_t tA = tmem + Cf::kColA + 80 * ab;
                     // The 64 x 64 score tile (M = 64: TMEM lanes 0-15 of each quadrant)
                     // read in the 16x256b shape, so that all 32 lanes work: this
@@ -1083,7 +1056,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         fence_proxy_async();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&at_full[n % NAT]);
-                        if (warp == kEpiWarp0 && lane == 0) LA_TR(3, 2, n);
                     }
                     if (NORM) {
                         // hand scale/den to the output stage (without the normalizer
@@ -1118,7 +1090,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                             : warp_wait(upd_done, (i - 1) & 1, err, kErrStateDone);
                 if (!ok) break;
                 tc_fence_after();
-                if (lead) LA_TR(5, 4, i);
                 int n = i * G;
                 for (int r = 0; r < G && ok; ++r) {
                     n = i * G + r;
@@ -1128,7 +1099,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     if (n >= NY) ok = warp_wait(&y_empty[yb], ((n / NY) & 1) ^ 1, err, kErrYEmpty);
                     if (!ok) break;
                     tc_fence_after();
-                    if (lead) LA_TR(5, 5, n);
                     const uint32_t tY = tmem + Cf::kColY + 64 * yb;
 #pragma unroll 1
                     for (int ks = 0; ks < D / 8; ++ks) {
@@ -1138,7 +1108,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     }
                     mma_commit(&empty_q[sq], lead);     // this warp is done with the query slot
                     mma_commit(&inter_cmp[yb], lead);   // the intra product may add to Y^T
-                    if (lead) LA_TR(5, 6, n);
                 }
                 if (!ok) break;
                 // the update overwrites S, which the read-outs take as their A
@@ -1157,7 +1126,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                 }
                 mma_commit(&empty_kv[s], lead);  // this warp is done with the K/V slot
                 mma_commit(upd_done, lead);
-                if (lead) LA_TR(5, 9, i);
             }
             mma_commit(final_done, lead);  // every operation of this warp complete
         }
@@ -1229,7 +1197,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
             // invalid steps (mask): their phi(k) and v rows become zero, so
             // they add nothing to the state, the key sum or any score
             const uint64_t okw = valid_bits(mb);
-            if (ct == 0) LA_TR(2, 1, i);
             float* gc = Gc(s);
             float gtot = 0.f;
             if (GATED) {
@@ -1238,10 +1205,15 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     float g0 = 0.f, g1 = 0.f;
                     const int j0 = 2 * ct, j1 = 2 * ct + 1;
                     // an invalid step (mask) keeps the state: no decay either
+                    // a log decay of -inf (or any value below kMinLogDecay) is
+                    // taken as kMinLogDecay: exp of it, and of every cumulative
+                    // difference that crosses it, is zero in float32 -- the same
+                    // "forget everything" restart -- while the differences of the
+                    // later steps of the chunk stay finite (no -inf - -inf)
                     if (j0 < valid && ((okw >> j0) & 1))
-                        g0 = __bfloat162float(decay[((size_t)b * T + t0 + j0) * Hkv + hk]);
+                        g0 = fmaxf(__bfloat162float(decay[((size_t)b * T + t0 + j0) * Hkv + hk]), kMinLogDecay);
                     if (j1 < valid && ((okw >> j1) & 1))
-                        g1 = __bfloat162float(decay[((size_t)b * T + t0 + j1) * Hkv + hk]);
+                        g1 = fmaxf(__bfloat162float(decay[((size_t)b * T + t0 + j1) * Hkv + hk]), kMinLogDecay);
                     const float sum = g0 + g1;
                     float incl = sum;
 #pragma unroll
@@ -1274,7 +1246,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                 gtot = gc[kC - 1];
             }
             const bool touch = GATED || SPLITK || NORM || fmap != LA_FMAP_NONE || mask;
-            if (ct == 0) LA_TR(2, 7, i);
             if (touch) {
                 float colsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 // A rolled loop: its body stays in the instruction cache across
@@ -1337,7 +1308,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                 } else {
                     conv_rows(BoolTag<true>{});
                 }
-                if (ct == 0) LA_TR(2, 8, i);
                 if (NORM) {
                     // partial column sums of this chunk, reduced after the tile is released
                     float* zp = zpart + zbuf * Cf::kZpart;
@@ -1357,12 +1327,10 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&conv_kv[s]);  // the tile goes to the tensor core
-            if (ct == 0) LA_TR(2, 2, i);
             if (touch && NORM) {
                 // Z += this chunk's column sums, off the path to the tensor core
                 const float* zp = zpart + zbuf * Cf::kZpart;
                 if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
-                if (ct == 0) LA_TR(2, 9, i);
                 if (ct < D) {
                     float add = 0.f;
 #pragma unroll
@@ -1403,7 +1371,6 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
 
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) LA_TR(0, 9, 0);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, Cf::kTmemCols);

@@ -8,6 +8,3 @@ cudaError_t chunk_run_causal_d128_bf16(const chunk::Launch& L, cudaStream_t st) 
 }
 }  // namespace la
 
-#ifdef LA_TRACE
-LA_TRACE_DUMP(la_trace_dump_d128)
-#endif

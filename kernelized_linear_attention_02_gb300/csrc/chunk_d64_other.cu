@@ -10,6 +10,3 @@ cudaError_t chunk_run_other_d64(const chunk::Launch& L, cudaStream_t st) {
 }
 }  // namespace la
 
-#ifdef LA_TRACE
-LA_TRACE_DUMP(la_trace_dump_d64_other)
-#endif

@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "chunk_args.h"
 #include "kernels.h"
@@ -23,28 +24,34 @@ __device__ unsigned int g_chunk_err = 0;
 
 namespace {
 
-constexpr int kMaxDev = 64;
 constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct DevInfo {
     int sms = 0;
     unsigned* err = nullptr;
+    uint64_t ctx = 0;  // context the entry was filled in
 };
 
+// SM count and error-word address of the current device, looked up once per
+// device and context (a device reset gives the device a new context, whose
+// symbol addresses are looked up again).
 bool dev_info(DevInfo* out) {
     static std::mutex mu;
-    static DevInfo info[kMaxDev];
+    static DevInfo info[kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    const uint64_t ctx = current_context_id();
     std::lock_guard<std::mutex> lk(mu);
-    if (!info[dev].err) {
+    if (!info[dev].err || ctx == 0 || info[dev].ctx != ctx) {
         int sms = 0;
         void* p = nullptr;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        // also makes the device's primary context current if none was
         if (cudaGetSymbolAddress(&p, g_chunk_err) != cudaSuccess) return false;
         info[dev].sms = sms;
         info[dev].err = static_cast<unsigned*>(p);
+        info[dev].ctx = current_context_id();
     }
     *out = info[dev];
     return true;
@@ -96,15 +103,15 @@ WsLayout ws_layout(const Problem& P, bool causal, int nseg) {
 // fixed order (deterministic).
 __global__ void segment_sum_kernel(const float* S_seg, const float* Z_seg, float* S_tot, float* Z_tot, int nseg,
                                    int D, int norm) {
-    const int64_t bh = blockIdx.y;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t bh = blockIdx.x;  // gridDim.x: up to 2^31 - 1 streams
+    const int e = blockIdx.y * blockDim.x + threadIdx.x;
     const int DD = D * D;
     if (e < DD) {
         float acc = 0.f;
         for (int p = 0; p < nseg; ++p) acc += S_seg[(bh * nseg + p) * DD + e];
         S_tot[bh * DD + e] = acc;
     }
-    if (norm && blockIdx.x == 0 && threadIdx.x < D) {
+    if (norm && blockIdx.y == 0 && threadIdx.x < D) {
         float acc = 0.f;
         for (int p = 0; p < nseg; ++p) acc += Z_seg[(bh * nseg + p) * D + threadIdx.x];
         Z_tot[bh * D + threadIdx.x] = acc;
@@ -163,6 +170,29 @@ chunk::Launch base_launch(const Problem& P, int mode, const DevInfo& di) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+uint64_t current_context_id() {
+    using GetCurrent = PFN_cuCtxGetCurrent_v4000;
+    using GetId = PFN_cuCtxGetId_v12000;
+    static const std::pair<GetCurrent, GetId> fns = [] {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &qa) != cudaSuccess ||
+            qa != cudaDriverEntryPointSuccess)
+            a = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+            qb != cudaDriverEntryPointSuccess)
+            b = nullptr;
+        return std::make_pair(reinterpret_cast<GetCurrent>(a), reinterpret_cast<GetId>(b));
+    }();
+    if (!fns.first || !fns.second) return 0;
+    CUcontext c = nullptr;
+    if (fns.first(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    if (fns.second(c, &id) != CUDA_SUCCESS) return 0;
+    return static_cast<uint64_t>(id);
+}
 
 bool chunk_supported(const Problem& P) {
     if (!P.io_bf16 || P.Dk != P.Dv || (P.Dk != 64 && P.Dk != 128)) return false;
@@ -271,7 +301,7 @@ cudaError_t chunk_noncausal(const Problem& P, const void* q, const void* k, cons
     cudaError_t e = run(L, D, st);
     if (e != cudaSuccess) return e;
     const int DD = D * D;
-    segment_sum_kernel<<<dim3((DD + 255) / 256, (unsigned)BH), 256, 0, st>>>(S_seg, Z_seg, S_tot, Z_tot, pl.nseg, D,
+    segment_sum_kernel<<<dim3((unsigned)BH, (DD + 255) / 256), 256, 0, st>>>(S_seg, Z_seg, S_tot, Z_tot, pl.nseg, D,
                                                                            P.norm);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -3,6 +3,8 @@
 // so the variants compile in parallel translation units).
 #pragma once
 
+#include <atomic>
+
 #include "chunk.cuh"
 #include "kernels.h"
 
@@ -13,14 +15,19 @@ template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUTBF, bool SPL
 cudaError_t run_one(const Launch& L, cudaStream_t st) {
     using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUTBF>;
     auto kern = chunk_kernel<D, MODE, NORM, FMAP, GATED, OUTBF, SPLIT, MASK>;
-    static int configured = -1;  // device on which the shared-memory limit was raised
+    // per device: the context in which the shared-memory limit of this
+    // instantiation was raised (0 = not yet); a new context (a device reset)
+    // raises it again.  Two threads may both raise it: the call is idempotent.
+    static std::atomic<uint64_t> configured[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured != dev) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const uint64_t ctx = current_context_id();
+    if (ctx == 0 || configured[dev].load(std::memory_order_acquire) != ctx) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
         if (e != cudaSuccess) return e;
-        configured = dev;
+        configured[dev].store(current_context_id(), std::memory_order_release);
     }
     if (L.pdl) {
         // may start while the previous kernel (the segment state pass) drains;
@@ -72,19 +79,3 @@ struct Dispatch {
 
 }  // namespace chunk
 }  // namespace la
-
-#ifdef LA_TRACE
-// Trace builds only: copy out (and reset) this unit's event buffer.
-#define LA_TRACE_DUMP(NAME)                                                                              \
-    extern "C" int NAME(unsigned* count, unsigned long long* times, unsigned* tags) {                   \
-        using namespace la::trace;                                                                      \
-        if (cudaDeviceSynchronize() != cudaSuccess) return -1;                                          \
-        cudaMemcpyFromSymbol(count, g_count, sizeof(unsigned) * kTraceCtas);                            \
-        cudaMemcpyFromSymbol(times, g_time, sizeof(unsigned long long) * kTraceCtas * kTraceEvents);    \
-        cudaMemcpyFromSymbol(tags, g_tag, sizeof(unsigned) * kTraceCtas * kTraceEvents);                \
-        unsigned long long zt[kTraceEvents] = {};                                                        \
-        for (int c = 0; c < kTraceCtas; ++c)                                                             \
-            cudaMemcpyToSymbol(g_time, zt, sizeof(zt), sizeof(zt) * c);                                  \
-        return 0;                                                                                       \
-    }
-#endif

@@ -7,6 +7,15 @@
 
 namespace la {
 
+// Devices the per-device caches of the library cover.
+constexpr int kMaxDevices = 64;
+// Identifier of the CUDA context current on the calling thread, unique for
+// the life of the process (cuCtxGetId), or 0 when none is current.  After a
+// device reset (cudaDeviceReset) the device gets a new context and so a new
+// identifier: the per-device caches of addresses and kernel attributes are
+// keyed by it and are rebuilt for the new context.
+uint64_t current_context_id();
+
 // CUDA-core recurrence (recurrent.cu): float32 path and uncovered shapes.
 size_t recurrent_smem_bytes(const Problem& P);
 // Scratch the causal recurrence uses to split a long sequence into segments
@@ -38,6 +47,11 @@ unsigned chunk_device_error(bool reset);
 // (0 / nullptr if they cannot be queried).
 int device_sm_count();
 unsigned* device_error_word();
+
+// Enqueues the bounded-wait self-test (selftest.cu): both wait forms give up
+// after limit_us on a barrier nothing completes and set their bits in the
+// device error word.
+cudaError_t bounded_wait_selftest(uint32_t limit_us, cudaStream_t st);
 
 // Gradients of the causal linear rule (backward.cu).
 size_t backward_workspace_bytes(const Problem& P);

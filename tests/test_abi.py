@@ -123,9 +123,15 @@ def test_workspace_too_small_rejected(L):
 
 
 def test_status_strings(L):
-    for s in range(5):
+    for s in range(6):
         assert L.la_status_string(s)
-    assert L.la_abi_version() == 2
+        assert L.la_status_str(s) == L.la_status_string(s)
+    assert L.la_abi_version() == 3
+
+
+def test_bounded_wait_selftest_rejects_bad_limits(L):
+    assert L.la_check_bounded_wait(0, None) == la.LA_ERR_INVALID_ARG
+    assert L.la_check_bounded_wait(1000001, None) == la.LA_ERR_INVALID_ARG
 
 
 # ---- entry points added with the masks, the delta rules and the backward pass:

@@ -40,7 +40,11 @@ def test_reference_arm_prints_one_contract_line():
     assert BASE_KEYS <= set(d)
     assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
     assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1
-    assert d["config"]["workload"] == "causal_prefill_B4_H8_T2048_D64_bf16"
+    sys.path.insert(0, ROOT)
+    import bench
+    # the same workload and the same config object as the GPU arm prints
+    assert d["config"] == bench.config_for(bench.HEADLINE, 1)
+    assert d["config"]["workload"] == "long_prefill_B8_H16_T8192_D128_bf16_relu"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     e2e = d["e2e"]

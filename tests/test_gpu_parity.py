@@ -1,9 +1,11 @@
 """GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
 
-Small cases are compared element by element over the whole output; they span
-several chunks of the tensor-core kernels and end on ragged tails.  The
-workloads at full size are compared on sampled (batch, kv-head) streams the
-oracle computes in full.  Tolerances are in tests/parity_utils.py.
+Small cases are compared over the whole output, norm-wise and row by row
+(every (token, head) output row and every state row against the same
+tolerance, tests/parity_utils.py); they span several chunks of the
+tensor-core kernels and end on ragged tails.  The workloads at full size are
+compared the same way on sampled (batch, kv-head) streams the oracle computes
+in full.
 """
 import itertools
 
@@ -67,6 +69,48 @@ def run_case(B, T, Hq, Hkv, Dk, Dv, dtype, out_dtype, fmap, norm, rule="linear",
     if norm:
         assert_close(to64(Z), Zr, 1e-5, "Z")
     return y, S, Z
+
+
+# ---------------------------------------------------------------------------
+# near-zero denominators (Keras request, Test Plan / Stability: "near-zero
+# denominators"; Mathematical definition: eps in the denominator).  Queries
+# far below zero make phi(q).Z tiny: with relu+eps every query feature is eps
+# itself, with elu+1 at q ~ -16 every feature is ~1e-7, so den = phi(q).Z + eps
+# comes within a few eps of eps on the first tokens.
+
+
+NEAR_ZERO = [  # fmap, query mean, query std
+    ("relu", -3.0, 1.0),
+    ("elu_plus_one", -16.0, 0.5),
+]
+
+
+@pytest.mark.parametrize("case", NEAR_ZERO, ids=lambda c: c[0])
+@pytest.mark.parametrize("cfg", [(torch.bfloat16, 64, 2, 2), (torch.bfloat16, 128, 4, 2), (torch.float32, 64, 2, 2)],
+                         ids=["bf16-d64", "bf16-d128-gqa", "f32-d64"])
+@pytest.mark.parametrize("carried", [False, True], ids=["zero-state", "carried-state"])
+def test_near_zero_denominator(case, cfg, carried):
+    fmap, qmean, qstd = case
+    dtype, D, Hq, Hkv = cfg
+    B, T = 2, 200
+    g = inputs.generator(77, DEV)
+    q = (inputs.normal((B, T, Hq, D), g, qstd, dtype=torch.float32, device=DEV) + qmean).to(dtype)
+    k = inputs.normal((B, T, Hkv, D), g, 0.5, dtype=dtype, device=DEV)
+    v = inputs.normal((B, T, Hkv, D), g, 1.0, dtype=dtype, device=DEV)
+    init = None
+    if carried:  # a small carried key sum keeps den close to eps on the first tokens
+        S0 = inputs.normal((B, Hkv, D, D), g, 1e-3, dtype=torch.float32, device=DEV)
+        Z0 = inputs.normal((B, Hkv, D), g, 1e-3, dtype=torch.float32, device=DEV).abs()
+        init = (S0, Z0)
+    y, (S, Z) = la.la_forward_causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map=fmap, use_normalizer=True,
+                                     epsilon=1e-6, initial_state=init, return_state=True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    yr, Sr, Zr = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map=fmap, use_normalizer=True, eps=1e-6,
+                               S0=None if init is None else init[0], Z0=None if init is None else init[1])
+    tol = tol_for(dtype, torch.float32)
+    assert_close(to64(y), yr, tol, "y")
+    assert_close(to64(S), Sr, tol, "S")
+    assert_close(to64(Z), Zr, 1e-5, "Z")
 
 
 # ---------------------------------------------------------------------------
@@ -159,6 +203,36 @@ def test_gated_strong_decay(shape):
     B, T, Hq, Hkv, Dk, Dv = shape
     run_case(B, T, Hq, Hkv, Dk, Dv, torch.bfloat16, torch.float32, "none", False, rule="gated", S0=True,
              scale=0.0, seed=11, decay_mean=-5.0)
+
+
+@pytest.mark.parametrize("shape", [(2, 200, 4, 2, 64, 64), (1, 257, 8, 2, 128, 128), (2, 300, 2, 2, 64, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_gated_infinite_decay(shape, dtype):
+    """A log decay of -inf forgets everything before its step (ONNX gated:
+    S_t = exp(g_t) S_{t-1} + k_t v_t^T with exp(-inf) = 0), inside a chunk,
+    on the first and last step of a chunk, and in later sequence segments."""
+    B, T, Hq, Hkv, Dk, Dv = shape
+    q = rand((B, T, Hq, Dk), 31, dtype)
+    k = rand((B, T, Hkv, Dk), 32, dtype)
+    v = rand((B, T, Hkv, Dv), 33, dtype)
+    x = rand((B, T, Hkv), 34, torch.float32) + 3.0
+    g = torch.nn.functional.logsigmoid(x)
+    for t, h in [(37, 0), (63, 1 % Hkv), (64, 0), (128, 1 % Hkv), (150, 0), (T - 1, 0)]:
+        g[:, t, h] = -float("inf")
+    g[1 % B, 100, :] = -float("inf")
+    decay = g.to(dtype)
+    S0 = rand((B, Hkv, Dk, Dv), 35, torch.float32)
+    y, (S, _) = la.la_forward_causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False,
+                                     scale=0.0, update_rule="gated", decay=decay, initial_state=(S0, None),
+                                     return_state=True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    yr, Sr, _ = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False,
+                              scale=0.0, rule="gated", decay=decay, S0=S0)
+    assert np.isfinite(yr).all() and np.isfinite(Sr).all()
+    tol = tol_for(dtype, torch.float32)
+    assert_close(to64(y), yr, tol, "y")
+    assert_close(to64(S), Sr, tol, "S")
 
 
 @pytest.mark.parametrize("shape", SHAPES[1:], ids=lambda s: "x".join(map(str, s)))
@@ -334,3 +408,31 @@ def test_calls_replay_in_a_cuda_graph():
     assert torch.equal(y, y_eager)
     yr, _, _ = oracle.causal(q2, k2, v2, q_heads=H, kv_heads=H)
     assert_close(to64(y), yr, tol_for(torch.bfloat16, torch.bfloat16), "graph replay")
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """Failure path of the bounded waits (no GPU fault): both wait forms poll
+    a barrier nothing completes, give up after 2 ms, set their bits in the
+    device error word and return; the context stays usable afterwards."""
+    assert la.la_device_error(reset=True) == 0
+    la.la_check_bounded_wait(2000)
+    assert la.la_device_status(reset=False) == la.LA_ERR_TIMEOUT
+    word = la.la_device_error(reset=True)
+    assert word == la.LA_SELFTEST_WARP_WAIT | la.LA_SELFTEST_THREAD_WAIT, hex(word)
+    assert la.la_device_status(reset=False) == la.LA_OK
+    # the context still runs the library's kernels correctly
+    run_case(2, 130, 4, 2, 64, 64, torch.bfloat16, torch.float32, "elu_plus_one", True, std=0.5)
+    assert la.la_device_error(reset=False) == 0
+
+
+def test_noncausal_more_streams_than_a_grid_row():
+    """More (batch, kv head) streams than gridDim.y allows (65535): every
+    kernel of the non-causal path takes the stream index from gridDim.x."""
+    B, T, H, D = 65540, 3, 1, 64
+    q = rand((B, T, H, D), 41, torch.bfloat16, 0.5)
+    k = rand((B, T, H, D), 42, torch.bfloat16, 0.5)
+    v = rand((B, T, H, D), 43, torch.bfloat16)
+    y = la.la_forward_noncausal(q, k, v, q_heads=H, kv_heads=H, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    yr = oracle.noncausal(q, k, v, q_heads=H, kv_heads=H)
+    assert_close(to64(y), yr, tol_for(torch.bfloat16, torch.float32), "non-causal")

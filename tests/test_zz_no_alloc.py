@@ -15,7 +15,7 @@ import torch
 
 import kernelized_linear_attention_02_gb300 as la
 import linattn_inputs as inputs
-from parity_utils import rel_err, to64, TOL_BF16, TOL_BF16_OUT
+from parity_utils import assert_close, to64, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -35,37 +35,42 @@ def _built():
     assert la.la_device_error(reset=True) == 0, "a tensor-core kernel gave up on a bounded wait"
 
 
-def _inputs(B, T, Hq, Hkv, D, seed, gated):
+def _inputs(B, T, Hq, Hkv, D, seed, gated, dtype=torch.bfloat16, per_dim=False):
     g = inputs.generator(seed, DEV)
-    q = inputs.normal((B, T, Hq, D), g, 1.0, dtype=torch.bfloat16, device=DEV)
-    k = inputs.normal((B, T, Hkv, D), g, 1.0, dtype=torch.bfloat16, device=DEV)
-    v = inputs.normal((B, T, Hkv, D), g, 1.0, dtype=torch.bfloat16, device=DEV)
+    q = inputs.normal((B, T, Hq, D), g, 1.0, dtype=dtype, device=DEV)
+    k = inputs.normal((B, T, Hkv, D), g, 1.0, dtype=dtype, device=DEV)
+    v = inputs.normal((B, T, Hkv, D), g, 1.0, dtype=dtype, device=DEV)
     decay = None
     if gated:
-        x = inputs.normal((B, T, Hkv), g, 1.0, dtype=torch.float32, device=DEV) + 3.0
-        decay = torch.nn.functional.logsigmoid(x).to(torch.bfloat16)
+        shape = (B, T, Hkv, D) if per_dim else (B, T, Hkv)
+        x = inputs.normal(shape, g, 1.0, dtype=torch.float32, device=DEV) + 3.0
+        decay = torch.nn.functional.logsigmoid(x).to(dtype)
     S0 = inputs.normal((B, Hkv, D, D), g, 1.0, dtype=torch.float32, device=DEV)
     Z0 = inputs.normal((B, Hkv, D), g, 1.0, dtype=torch.float32, device=DEV).abs() + 1.0
     return q, k, v, decay, S0, Z0
 
 
 CASES = [
-    # (B, T, Hq, Hkv, D, feature map, normalizer, rule, in-place state)
-    (1, 2048, 2, 2, 64, "elu_plus_one", True, "linear", False),
-    (2, 1000, 8, 2, 128, "none", False, "gated", True),
-    (1, 4097, 1, 1, 128, "relu", True, "linear", True),
+    # (B, T, Hq, Hkv, D, feature map, normalizer, rule, in-place state, io dtype, per-key-dim decay)
+    (1, 2048, 2, 2, 64, "elu_plus_one", True, "linear", False, torch.bfloat16, False),
+    (2, 1000, 8, 2, 128, "none", False, "gated", True, torch.bfloat16, False),
+    (1, 4097, 1, 1, 128, "relu", True, "linear", True, torch.bfloat16, False),
+    # the CUDA-core recurrence, split into sequence segments on the scratch
+    (1, 1500, 2, 2, 64, "elu_plus_one", True, "linear", True, torch.float32, False),
+    (1, 1200, 4, 2, 64, "none", False, "gated", False, torch.bfloat16, True),
 ]
 
 
-@pytest.mark.parametrize("B,T,Hq,Hkv,D,fmap,norm,rule,inplace", CASES)
-def test_noalloc_matches_workspace_call(B, T, Hq, Hkv, D, fmap, norm, rule, inplace):
+@pytest.mark.parametrize("B,T,Hq,Hkv,D,fmap,norm,rule,inplace,dtype,per_dim", CASES,
+                         ids=lambda x: str(x).replace("torch.", ""))
+def test_noalloc_matches_workspace_call(B, T, Hq, Hkv, D, fmap, norm, rule, inplace, dtype, per_dim):
     kw = dict(q_heads=Hq, kv_heads=Hkv, feature_map=fmap, use_normalizer=norm, update_rule=rule)
-    p = la.make_params(batch=B, seq_len=T, q_heads=Hq, kv_heads=Hkv, key_dim=D, value_dim=D,
-                       feature_map=fmap, use_normalizer=norm, update_rule=rule)
+    p = la.make_params(batch=B, seq_len=T, q_heads=Hq, kv_heads=Hkv, key_dim=D, value_dim=D, io_dtype=dtype,
+                       feature_map=fmap, use_normalizer=norm, update_rule=rule, decay_per_key_dim=per_dim)
     need = la.la_workspace_bytes(p, True)
     assert 0 < need <= la.LA_NOALLOC_SCRATCH_BYTES, need  # split into segments, fits the scratch
     for call, seed in enumerate((11, 23)):  # two calls in a row
-        q, k, v, decay, S0, Z0 = _inputs(B, T, Hq, Hkv, D, seed, rule == "gated")
+        q, k, v, decay, S0, Z0 = _inputs(B, T, Hq, Hkv, D, seed, rule == "gated", dtype, per_dim)
         Z0 = Z0 if norm else None
         y_ref, (S_ref, Z_ref) = la.la_forward_causal(q, k, v, decay=decay, initial_state=(S0, Z0),
                                                      return_state=True, **kw)
@@ -80,13 +85,10 @@ def test_noalloc_matches_workspace_call(B, T, Hq, Hkv, D, fmap, norm, rule, inpl
             la.la_forward_causal_noalloc(q, k, v, decay=decay, initial_state=(S0, Z0), out=y,
                                          state_out=(S, Z), **kw)
         torch.cuda.synchronize()
-        ey = rel_err(to64(y), to64(y_ref))
-        eS = rel_err(to64(S), to64(S_ref))
-        assert ey <= TOL_BF16_OUT, f"call {call}: y rel err {ey:.3e}"
-        assert eS <= TOL_BF16, f"call {call}: S rel err {eS:.3e}"
+        assert_close(to64(y), to64(y_ref), tol_for(dtype, dtype), f"call {call}: y")
+        assert_close(to64(S), to64(S_ref), tol_for(dtype, torch.float32), f"call {call}: S")
         if norm:
-            eZ = rel_err(to64(Z), to64(Z_ref))
-            assert eZ <= TOL_BF16, f"call {call}: Z rel err {eZ:.3e}"
+            assert_close(to64(Z), to64(Z_ref), tol_for(dtype, torch.float32), f"call {call}: Z")
 
 
 def test_scratch_size_covers_every_causal_problem_on_this_device():
@@ -97,8 +99,15 @@ def test_scratch_size_covers_every_causal_problem_on_this_device():
     m = re.search(r"#define LA_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", header)
     assert m and int(m.group(1)) << int(m.group(2)) == la.LA_NOALLOC_SCRATCH_BYTES
     worst = 0
-    for bh in range(1, 2 * torch.cuda.get_device_properties(0).multi_processor_count + 1):
-        p = la.make_params(batch=bh, seq_len=1 << 20, q_heads=1, kv_heads=1, key_dim=128, value_dim=128,
-                           feature_map="relu", use_normalizer=True)
-        worst = max(worst, la.la_workspace_bytes(p, True))
+    # the tensor-core path (bf16, head size 128) and the CUDA-core recurrence
+    # (float32 io; per-key-dimension decay), whose segment scratch is sized
+    # differently (a segment cap plus a copy of the initial state)
+    kinds = [dict(io_dtype=torch.bfloat16, feature_map="relu", use_normalizer=True),
+             dict(io_dtype=torch.float32, feature_map="relu", use_normalizer=True),
+             dict(io_dtype=torch.bfloat16, feature_map="none", use_normalizer=False, update_rule="gated",
+                  decay_per_key_dim=True)]
+    for kind in kinds:
+        for bh in range(1, 2 * torch.cuda.get_device_properties(0).multi_processor_count + 1):
+            p = la.make_params(batch=bh, seq_len=1 << 20, q_heads=1, kv_heads=1, key_dim=128, value_dim=128, **kind)
+            worst = max(worst, la.la_workspace_bytes(p, True))
     assert 0 < worst <= la.LA_NOALLOC_SCRATCH_BYTES, worst
