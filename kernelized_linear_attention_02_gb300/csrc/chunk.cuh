@@ -60,15 +60,58 @@ namespace chunk {
 using namespace umma;
 
 constexpr int kC = 64;  // tokens per chunk
-// per-stage decay block (gated rule), floats: [0, 64) inclusive cumulative log
-// decay G_j, [64, 128) exp(ref - G_j), then ref and the "factored" flag
-constexpr int kGCol = 64, kGRef = 128, kGFlag = 129;
+// Per-stage decay block of the gated rule (floats).  G_j is the inclusive
+// cumulative log decay inside the chunk.  A step whose log decay is at most
+// kRestartLogDecay (a -inf "forget everything" step, taken as kMinLogDecay)
+// starts a new group: every weight exp(G_i - G_j) across it is zero in
+// float32.  Each group has a reference ref_g in the middle of its G range.
+// When every group's range is moderate (the "exact" chunks: spread below 60,
+// top below 30) the chunk's read-out takes undecayed queries: the state warps
+// hand the tensor core a hi/lo copy of exp(ref_0) S, the intra weights are
+// exp(ref_g(j) - G_j) (column factors; zero across groups) and output row i is
+// multiplied by exp(G_i - ref_g(i)), so no decayed operand is rounded to
+// bf16.  Rows after the first restart read nothing of S (their query rows in
+// the read-out copy are zero).  Other chunks take the decayed queries
+// exp(G_i) q in bf16 and per-element weights exp(G_i - G_j).
+//   [0, 64)   exact: exp(G_i - ref_g(i)) (output factors); else G_i
+//   [64, 128) exact: exp(ref_g(j) - G_j) (column factors of the intra weights)
+//   kGRef ref_0, kGRefLast ref of the last group, kGTot the chunk's total log
+//   decay, kGWord0/1 the 64-bit word of restart steps (bit patterns),
+//   kGFlag 0 (not exact), 1 (exact, one group), 2 (exact, several groups)
+constexpr int kGCol = 64, kGRef = 128, kGFlag = 129, kGTot = 130, kGRefLast = 131, kGWord0 = 132, kGWord1 = 133;
 // Floor of a step's log decay (gated rule).  exp(-200) underflows to zero in
 // float32 (the smallest subnormal is ~exp(-103.3)), so a step at the floor
 // erases the earlier state exactly as -inf does, as long as the later steps
 // of its 64-token chunk do not add up to more than +97 (log decays are
 // log-sigmoid values, <= 0, in every workload of the pages).
 constexpr float kMinLogDecay = -200.f;
+// A step with a log decay at or below this starts a new group of its chunk
+// (see the decay block): exp(-100) is below float32's smallest normal number.
+constexpr float kRestartLogDecay = -100.f;
+
+// Restart steps of a chunk as a 64-bit word (bit j = step j) from the
+// per-lane flags of steps 2 lane (even) and 2 lane + 1 (odd); warp-collective.
+__device__ __forceinline__ uint64_t restart_word(bool even, bool odd) {
+    auto spread = [](uint64_t x) {  // bit i -> bit 2i
+        x = (x | (x << 16)) & 0x0000FFFF0000FFFFull;
+        x = (x | (x << 8)) & 0x00FF00FF00FF00FFull;
+        x = (x | (x << 4)) & 0x0F0F0F0F0F0F0F0Full;
+        x = (x | (x << 2)) & 0x3333333333333333ull;
+        x = (x | (x << 1)) & 0x5555555555555555ull;
+        return x;
+    };
+    const uint32_t e = __ballot_sync(0xffffffffu, even), o = __ballot_sync(0xffffffffu, odd);
+    return spread(e) | (spread(o) << 1);
+}
+// No restart step in (j, i] (0 <= j <= i <= 63): steps j and i are in one group.
+__device__ __forceinline__ bool same_group(uint64_t word, int j, int i) {
+    if (i == j) return true;
+    const uint64_t span = (i - j == 64) ? ~0ull : ((1ull << (i - j)) - 1);
+    return ((word >> (j + 1)) & span) == 0;
+}
+__device__ __forceinline__ uint64_t gc_word(const float* gc) {
+    return (uint64_t)__float_as_uint(gc[kGWord0]) | ((uint64_t)__float_as_uint(gc[kGWord1]) << 32);
+}
 constexpr int kThreads = 480;  // 15 warps; the two-issuer kernel adds warp 15
 template <bool SPLIT>
 constexpr int block_threads() { return SPLIT ? 512 : kThreads; }
@@ -76,10 +119,13 @@ constexpr int kStateWarp0 = 2, kEpiWarp0 = 6, kFeatWarp0 = 10, kMmaSWarp = 14;  
 
 template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16>
 struct Cfg {
-    // the gated state update takes its decayed keys as bf16 hi + lo; the
-    // linear rule's keys enter as bf16 alone (phi(k) of elu+1 is rounded: its
-    // effect on the output stays near 1e-4 relative)
-    static constexpr bool kSplitK = GATED;
+    // the state update takes its key operand as bf16 hi + lo wherever that
+    // operand is not exactly a bf16 value: the gated rule's decayed keys, and
+    // phi(k) of elu+1 (x + 1 or exp(x); rounded to bf16 alone it would carry
+    // up to 2^-8 of relative error into every state row).  relu + eps of a bf16
+    // input rounds back to the input (eps is far below its ulp) and the
+    // identity map is exact, so those keys enter as one bf16 part.
+    static constexpr bool kSplitK = GATED || FMAP == LA_FMAP_ELU_PLUS_ONE;
     static constexpr bool kHasKV = MODE != kApply;
     static constexpr bool kHasQ = MODE != kState;
     static constexpr int kTile = D * 128;  // 64 rows x D bf16 (D/64 swizzled blocks of 8 KB)
@@ -114,9 +160,10 @@ struct Cfg {
     static constexpr bool kSplitMma = kTf32 && MODE == kCausal;
     static constexpr int kQf = (kHasQ && kTf32) ? 2 * kTile : 0;
     static constexpr int kQStage = kHasQ ? kTile * (GATED ? 2 : 1) + kQf : 0;
-    // masked scores as bf16 hi + lo (one bf16 part suffices without the
-    // normalizer, where its rounding stays within ~5e-4 of the output)
-    static constexpr bool kALo = NORM || GATED;
+    // masked scores as bf16 hi + lo (~16 significant bits): one bf16 part
+    // would put up to 2^-9 of relative error on single output rows (the first
+    // token of a sequence is one score times one value row)
+    static constexpr bool kALo = true;
     // one buffer of masked scores: the epilogue writes item n's once the intra
     // product of item n - 1 (which read the previous ones) has completed
     static constexpr int kNAT = MODE == kCausal ? 1 : 0;
@@ -149,12 +196,13 @@ struct Cfg {
         return 1024 + nkv * kKvStage + nq * kQStage + kAT + kZrApply + kYS + kMisc + nkv * kGStage;
     }
     static constexpr int kLimit = 227 * 1024;
-    // ring depths: the deepest of (4,4), (3,3), (3,2), (2,2) that shared
-    // memory holds (key/value and query stages), else fewer
+    // ring depths: the deepest of (4,4), (4,3), (3,3), (3,2), (2,2) that
+    // shared memory holds (key/value and query stages), else fewer
     static constexpr bool fits(int nkv, int nq) {
         return bytes(kHasKV ? nkv : 0, kHasQ ? nq : 0) <= kLimit;
     }
-    static constexpr int kNKV0 = fits(4, 4) ? 4 : fits(3, 3) ? 3 : fits(3, 2) ? 3 : fits(2, 2) ? 2 : fits(2, 1) ? 2 : 1;
+    static constexpr int kNKV0 = fits(4, 4) ? 4 : fits(4, 3) ? 4 : fits(3, 3) ? 3 : fits(3, 2) ? 3 : fits(2, 2) ? 2
+                                 : fits(2, 1) ? 2 : 1;
     static constexpr int kNQ0 = fits(kNKV0, 4) ? 4 : fits(kNKV0, 3) ? 3 : fits(kNKV0, 2) ? 2 : 1;
     static constexpr int kNKV = kHasKV ? kNKV0 : 0;
     static constexpr int kNQ = kHasQ ? kNQ0 : 0;
@@ -388,8 +436,13 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
         };
         const int sq = n % NQ1;
         if (!warp_wait(&full_q[sq], (n / NQ1) & 1, err, kErrFullQ)) return false;
-        if (fmap != LA_FMAP_NONE || GATED || TF32) {
+        // gated rule, exact chunk of one group: the read-out takes the queries
+        // as they are; with restarts it takes a copy whose rows after the
+        // first restart are zero
+        const float qflag = GATED ? Gc(i % NKV1)[kGFlag] : 0.f;
+        if ((fmap != LA_FMAP_NONE || GATED || TF32) && qflag != 1.f) {
             const float* gc = Gc(i % NKV1);
+            const uint64_t qword = qflag == 2.f ? gc_word(gc) : 0ull;
             uint4 nxt = *reinterpret_cast<const uint4*>(Qb(sq) + chunk_off(0));
 #pragma unroll 1
             for (int m = 0; m < kPer; ++m) {
@@ -398,7 +451,9 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                 float f[8];
                 bf8_to_f(cur, f);
                 if (GATED) {
-                    const float w = __expf(gc[rbase + kRowStep * m]);
+                    const int row = rbase + kRowStep * m;
+                    const float w = qflag == 2.f ? (same_group(qword, 0, row) && !(qword & 1ull) ? 1.f : 0.f)
+                                                 : __expf(gc[row]);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] *= w;
                     *reinterpret_cast<uint4*>(Qd(sq) + chunk_off(m)) = f_to_bf8(f);
@@ -437,7 +492,18 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
     // Output of item m (query head m % G of chunk m / G): Y^T from TMEM times
     // scale/den, stored to global memory.  Run by four warps, one per TMEM lane
     // quadrant: the state warps (linear rule) or the epilogue warps (gated).
-    auto emit_y = [&](int m) -> bool {
+    // gated rule, exact chunk (gexact): output row x is also multiplied by
+    // exp(G_x - ref), lane l of the warp holding that factor for rows l (eo_lo)
+    // and l + 32 (eo_hi); tok_f(x) gives row x's whole factor (warp-collective)
+    auto emit_y = [&](int m, float eo_lo = 1.f, float eo_hi = 1.f, bool gexact = false) -> bool {
+        auto tok_f = [&](int x) -> float {
+            if constexpr (GATED) {
+                const float e = __shfl_sync(0xffffffffu, x < 32 ? eo_lo : eo_hi, x & 31);
+                return gexact ? scale * e : scale;
+            } else {
+                return scale;
+            }
+        };
         const int quad = warp & 3;
         const bool m64 = D == 64;
         const int vrow = m64 ? (quad * 16 + lane) : (quad * 32 + lane);  // value index of this Y^T lane
@@ -484,18 +550,25 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                     const int x = 8 * g + cq;
-                    const float2 f = NORM ? *reinterpret_cast<const float2*>(idn + x) : make_float2(scale, scale);
+                    const float2 f = NORM ? *reinterpret_cast<const float2*>(idn + x) : make_float2(tok_f(x), tok_f(x + 1));
                     ys[x * P + v1] = __float2bfloat16_rn(f.x * __uint_as_float(y0[4 * g]));
                     ys[(x + 1) * P + v1] = __float2bfloat16_rn(f.y * __uint_as_float(y0[4 * g + 1]));
                     ys[x * P + v2] = __float2bfloat16_rn(f.x * __uint_as_float(y0[4 * g + 2]));
                     ys[(x + 1) * P + v2] = __float2bfloat16_rn(f.y * __uint_as_float(y0[4 * g + 3]));
                 }
-            } else if (vrow_ok) {
+            } else {
+                static_assert(D == 128, "the staged 32-lane path covers head size 128 (every lane a value row)");
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
-                    const float4 fa = NORM ? idn4[2 * g] : make_float4(scale, scale, scale, scale);
-                    const float4 fb = NORM ? idn4[2 * g + 1] : fa;
-                    const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+                    float f[8];
+                    if constexpr (NORM) {
+                        const float4 fa = idn4[2 * g], fb = idn4[2 * g + 1];
+                        f[0] = fa.x, f[1] = fa.y, f[2] = fa.z, f[3] = fa.w, f[4] = fb.x, f[5] = fb.y, f[6] = fb.z,
+                        f[7] = fb.w;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = tok_f(g * 8 + e);
+                    }
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int x = g * 8 + e;
@@ -515,17 +588,25 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         (okw >> x) & 1 ? *reinterpret_cast<const uint4*>(ys + x * P + cc * 8) : make_uint4(0, 0, 0, 0);
             }
             if (!group_sync(out_group, ophase, err, kErrYFull)) return false;  // tile free again
-        } else if (vrow_ok) {
+        } else {
+            // every lane runs the loop (the row factors are warp-collective);
+            // lanes without a value row store nothing
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
-                const float4 fa = NORM ? idn4[2 * g] : make_float4(scale, scale, scale, scale);
-                const float4 fb = NORM ? idn4[2 * g + 1] : fa;
-                const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+                float f[8];
+                if constexpr (NORM) {
+                    const float4 fa = idn4[2 * g], fb = idn4[2 * g + 1];
+                    f[0] = fa.x, f[1] = fa.y, f[2] = fa.z, f[3] = fa.w, f[4] = fb.x, f[5] = fb.y, f[6] = fb.z,
+                    f[7] = fb.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = tok_f(g * 8 + e);
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int x = g * 8 + e;
                     const float o = (okw >> x) & 1 ? f[e] * __uint_as_float(x < 32 ? y0[x] : y1[x - 32]) : 0.f;
-                    if (x < valid) {
+                    if (vrow_ok && x < valid) {
                         if (OUT_BF16)
                             reinterpret_cast<__nv_bfloat16*>(yout)[base + x * tstride] = __float2bfloat16_rn(o);
                         else
@@ -667,7 +748,9 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     ok = warp_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ);
                     if (!ok) break;
                     tc_fence_after();
-                    uint8_t* qop = GATED ? Qd(sq) : Qb(sq);  // operand of the inter read-out
+                    // operand of the inter read-out: the queries (linear rule, gated exact
+                    // chunk of one group) or the copy (decayed, or zero after a restart)
+                    uint8_t* qop = (GATED && Gc(s)[kGFlag] != 1.f) ? Qd(sq) : Qb(sq);
                     const uint32_t tA = tmem + Cf::kColA + 80 * ab;
                     if (MODE == kCausal || NORM) {
                         if (n >= NA) {
@@ -822,7 +905,8 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
         float gsum = 0.f;  // gated, state mode: total log decay of the segment
 
         // ---- state hi/lo (and, gated, the decay of the fp32 state in place)
-        auto convert_state = [&](float decay_mul, bool write_back) {
+        // hi/lo copy of hl_mul * S for the read-out; S <- decay_mul * S in place
+        auto convert_state = [&](float decay_mul, bool write_back, float hl_mul = 1.f) {
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 64) {
                 uint32_t r0[32], r1[32];
@@ -835,8 +919,8 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     uint32_t h0[16], l0[16], h1[16], l1[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
-                        split2(__uint_as_float(r0[2 * x]), __uint_as_float(r0[2 * x + 1]), h0[x], l0[x]);
-                        split2(__uint_as_float(r1[2 * x]), __uint_as_float(r1[2 * x + 1]), h1[x], l1[x]);
+                        split2(hl_mul * __uint_as_float(r0[2 * x]), hl_mul * __uint_as_float(r0[2 * x + 1]), h0[x], l0[x]);
+                        split2(hl_mul * __uint_as_float(r1[2 * x]), hl_mul * __uint_as_float(r1[2 * x + 1]), h1[x], l1[x]);
                     }
                     tmem_st16(tmem_addr(tmem + Cf::kColHi, quad * 32, c0 / 2), h0);
                     tmem_st16(tmem_addr(tmem + Cf::kColHi, quad * 32, c0 / 2 + 16), h1);
@@ -878,32 +962,45 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
             // of its last head, which needs the Y buffer of head G-3 released
             // first, so those outputs must come before the conversion.
             constexpr bool kOut = MODE == kCausal;
+            // output row factors of exact chunks (two per lane), for the chunk
+            // being converted (cur) and the one before it (prev), whose outputs
+            // are emitted around this conversion
+            float eo_cur_lo = 1.f, eo_cur_hi = 1.f, eo_prev_lo = 1.f, eo_prev_hi = 1.f;
+            bool ex_cur = false, ex_prev = false;
             for (int i = 0; i < nck && ok; ++i) {
+                // (cur still holds chunk i - 1 here)
                 if (kOut && i > 0)
-                    for (int r = 0; r < G - 2 && ok; ++r) ok = emit_y((i - 1) * G + r);
+                    for (int r = 0; r < G - 2 && ok; ++r) ok = emit_y((i - 1) * G + r, eo_cur_lo, eo_cur_hi, ex_cur);
                 if (!ok) break;
                 // S(i): after the update of chunk i-1 and every read-out that used S_prev
                 if (i > 0) {
                     ok = warp_wait(state_done, (i - 1) & 1, err, kErrStateDone);
                     if (!ok) break;
                 }
-                float gtot = 0.f;
+                float gtot = 0.f, hl_mul = 1.f;
                 if (GATED) {
                     // the decay of chunk i comes with its converted keys
                     const int s = i % NKV1;
                     ok = warp_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
                     if (!ok) break;
-                    gtot = Gc(s)[kC - 1];
+                    const float* gc = Gc(s);
+                    gtot = gc[kGTot];
+                    eo_prev_lo = eo_cur_lo, eo_prev_hi = eo_cur_hi, ex_prev = ex_cur;
+                    ex_cur = gc[kGFlag] != 0.f;
+                    eo_cur_lo = ex_cur ? gc[lane] : 1.f;
+                    eo_cur_hi = ex_cur ? gc[lane + 32] : 1.f;
+                    if (ex_cur) hl_mul = __expf(gc[kGRef]);
                 }
                 tc_fence_after();
-                convert_state(GATED ? __expf(gtot) : 1.f, GATED);
+                convert_state(GATED ? __expf(gtot) : 1.f, GATED, hl_mul);
                 publish_state();
                 if (MODE == kState) gsum += gtot;
                 if (kOut && i > 0)
-                    for (int r = max(0, G - 2); r < G && ok; ++r) ok = emit_y((i - 1) * G + r);
+                    for (int r = max(0, G - 2); r < G && ok; ++r)
+                        ok = emit_y((i - 1) * G + r, eo_prev_lo, eo_prev_hi, ex_prev);
             }
             if (kOut && nck > 0)
-                for (int r = 0; r < G && ok; ++r) ok = emit_y((nck - 1) * G + r);
+                for (int r = 0; r < G && ok; ++r) ok = emit_y((nck - 1) * G + r, eo_cur_lo, eo_cur_hi, ex_cur);
         }
         if (TF32 && MODE != kState) {
             // linear rule: the state needs no per-chunk work here, so these
@@ -1037,14 +1134,20 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                             }
                         };
                         if constexpr (GATED) {
-                            const float g1 = gc[r1], g2 = gc[r2];
-                            if (gc[kGFlag] != 0.f) {
-                                // exp(G_i - G_j) = exp(G_i - ref) * exp(ref - G_j): one exp
-                                // per row and the column factors of the feature warps
-                                const float e1 = __expf(g1 - gc[kGRef]), e2 = __expf(g2 - gc[kGRef]);
+                            if (gc[kGFlag] == 1.f) {
+                                // exact chunk: exp(G_i - G_j) = exp(G_i - ref) * exp(ref - G_j);
+                                // the row factor is applied to the output row, so the
+                                // weights are the column factors of the feature warps
                                 const float* ef = gc + kGCol;
-                                mask_rows([&](int j) { return e1 * ef[j]; }, [&](int j) { return e2 * ef[j]; });
+                                mask_rows([&](int j) { return ef[j]; }, [&](int j) { return ef[j]; });
+                            } else if (gc[kGFlag] == 2.f) {
+                                // exact chunk with restarts: zero across groups
+                                const float* ef = gc + kGCol;
+                                const uint64_t word = gc_word(gc);
+                                mask_rows([&](int j) { return same_group(word, j, r1) ? ef[j] : 0.f; },
+                                          [&](int j) { return same_group(word, j, r2) ? ef[j] : 0.f; });
                             } else {
+                                const float g1 = gc[r1], g2 = gc[r2];
                                 mask_rows([&](int j) { return __expf(g1 - gc[j]); },
                                           [&](int j) { return __expf(g2 - gc[j]); });
                             }
@@ -1117,12 +1220,14 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                 ok = warp_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV);
                 if (!ok) break;
                 tc_fence_after();
-                // S^T += V^T . phi(K)
+                // S^T += V^T . phi(K) (+ V^T . phi(K)_lo)
 #pragma unroll 1
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
                     mma_ss(tS, av, sdesc_sw128(smem_u32(Kb(s) + ks * 2048), (uint32_t)Cf::kKBlk, 1024), id_state, 1,
                            lead);
+                    if (SPLITK)
+                        mma_ss(tS, av, sdesc_sw128(smem_u32(Klo(s) + ks * 2048), 8192, 1024), id_state, 1, lead);
                 }
                 mma_commit(&empty_kv[s], lead);  // this warp is done with the K/V slot
                 mma_commit(upd_done, lead);
@@ -1199,6 +1304,9 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
             const uint64_t okw = valid_bits(mb);
             float* gc = Gc(s);
             float gtot = 0.f;
+            bool gx = false;     // exact chunk (kGFlag)
+            float e_tr = 0.f;    // exact chunk: exp(gtot - ref of the last group)
+            uint64_t gword = 0;  // exact chunk: restart steps
             if (GATED) {
                 // inclusive cumulative log decay inside the chunk (first converter warp)
                 if (ct < 32) {
@@ -1222,28 +1330,53 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         if (lane >= o) incl += t;
                     }
                     const float c0 = incl - sum + g0, c1 = incl;
-                    gc[j0] = c0;
-                    gc[j1] = c1;
-                    // factored weights for the score epilogue: a reference in the
-                    // middle of the chunk's range, usable when both factors stay
-                    // below e^80 (spread < 160)
-                    float mx = fmaxf(c0, c1), mn = fminf(c0, c1);
+                    // groups split at restart steps; a reference in the middle of each
+                    // group's range; an exact chunk (every factor exp(+-(G - ref_g))
+                    // within e^30, every ref below 30) keeps the factors instead of G
+                    // (see kGCol)
+                    const uint64_t word = restart_word(g0 <= kRestartLogDecay, g1 <= kRestartLogDecay);
+                    const int ngroups = __popcll(word) + 1;
+                    const uint64_t m0 = (2ull << j0) - 1, m1 = j1 == 63 ? ~0ull : (2ull << j1) - 1;
+                    const int grp0 = __popcll(word & m0), grp1 = __popcll(word & m1);
+                    bool exact = true;
+                    float ref0 = 0.f, ref1 = 0.f, ref_first = 0.f, ref_last = 0.f;
+#pragma unroll 1
+                    for (int g = 0; g < ngroups; ++g) {
+                        float mx = fmaxf(grp0 == g ? c0 : -INFINITY, grp1 == g ? c1 : -INFINITY);
+                        float mn = fminf(grp0 == g ? c0 : INFINITY, grp1 == g ? c1 : INFINITY);
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                        for (int o = 16; o > 0; o >>= 1) {
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                        }
+                        if (mx < mn) continue;  // empty group (a restart on step 0)
+                        exact = exact && (mx - mn) < 60.f && mx < 30.f;
+                        const float ref = 0.5f * (mx + mn);
+                        if (grp0 == g) ref0 = ref;
+                        if (grp1 == g) ref1 = ref;
+                        if (g == 0) ref_first = ref;
+                        ref_last = ref;
                     }
-                    const float ref = 0.5f * (mx + mn);
-                    const bool fac = (mx - mn) < 160.f;
-                    gc[kGCol + j0] = fac ? __expf(ref - c0) : 0.f;
-                    gc[kGCol + j1] = fac ? __expf(ref - c1) : 0.f;
+                    gc[j0] = exact ? __expf(c0 - ref0) : c0;
+                    gc[j1] = exact ? __expf(c1 - ref1) : c1;
+                    gc[kGCol + j0] = exact ? __expf(ref0 - c0) : 0.f;
+                    gc[kGCol + j1] = exact ? __expf(ref1 - c1) : 0.f;
                     if (ct == 0) {
-                        gc[kGRef] = ref;
-                        gc[kGFlag] = fac ? 1.f : 0.f;
+                        gc[kGRef] = ref_first;
+                        gc[kGRefLast] = ref_last;
+                        gc[kGFlag] = exact ? (ngroups > 1 ? 2.f : 1.f) : 0.f;
+                        gc[kGWord0] = __uint_as_float((uint32_t)word);
+                        gc[kGWord1] = __uint_as_float((uint32_t)(word >> 32));
                     }
+                    if (ct == 31) gc[kGTot] = c1;  // G of the chunk's last step
                 }
                 if (!group_sync(conv_group, gphase, err, kErrStateReady)) return false;
-                gtot = gc[kC - 1];
+                gtot = gc[kGTot];
+                gx = gc[kGFlag] != 0.f;
+                if (gx) {
+                    e_tr = __expf(gtot - gc[kGRefLast]);
+                    gword = gc_word(gc);
+                }
             }
             const bool touch = GATED || SPLITK || NORM || fmap != LA_FMAP_NONE || mask;
             if (touch) {
@@ -1271,7 +1404,10 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     bf8_to_f(cur, f);
                     uint4 hi, lo;
                     if (GATED) {
-                        const float w = __expf(gtot - gc[row]);
+                        // exp(G_C - G_row): from the column factor in an exact chunk
+                        // (zero for steps before the chunk's last restart)
+                        const float w = gx ? (same_group(gword, row, kC - 1) ? e_tr * gc[kGCol + row] : 0.f)
+                                           : __expf(gtot - gc[row]);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) f[e] = drop ? 0.f : f[e] * w;
                         split8(f, hi, lo);
@@ -1300,10 +1436,8 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         const uint4 z = make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4*>(Kb(s) + chunk_off(m, Cf::kKBlk)) = z;
                         *reinterpret_cast<uint4*>(Vb(s) + chunk_off(m)) = z;
-                        if (GATED) {
-                            *reinterpret_cast<uint4*>(Kd(s) + chunk_off(m)) = z;
-                            *reinterpret_cast<uint4*>(Klo(s) + chunk_off(m)) = z;
-                        }
+                        if (GATED) *reinterpret_cast<uint4*>(Kd(s) + chunk_off(m)) = z;
+                        if (SPLITK) *reinterpret_cast<uint4*>(Klo(s) + chunk_off(m)) = z;
                     }
                 } else {
                     conv_rows(BoolTag<true>{});

@@ -93,8 +93,16 @@ def assert_close(got, ref, tol, what=""):
     worst = int(np.argmax(rows)) if rows.size else 0
     row_max = float(rows[worst]) if rows.size else 0.0
     abs_max = float(np.max(np.abs(got - ref))) if got.size else 0.0
-    RECORDS.append({"what": what, "tol": tol, "norm_rel": e, "row_rel_max": row_max, "abs_max": abs_max,
-                    "rows": int(rows.size), "shape": list(ref.shape)})
+    rec = {"what": what, "tol": tol, "norm_rel": e, "row_rel_max": row_max, "abs_max": abs_max,
+           "rows": int(rows.size), "shape": list(ref.shape)}
+    if rows.size:
+        r2 = ref.reshape(-1, ref.shape[-1])
+        rn = np.linalg.norm(r2, axis=1)
+        rms = float(np.sqrt(np.mean(rn ** 2)))
+        rec["worst_row"] = worst
+        rec["worst_row_ref_over_rms"] = float(rn[worst] / rms) if rms > 0 else 0.0
+        rec["rows_over_tol"] = int(np.sum(rows > tol))
+    RECORDS.append(rec)
     assert e <= tol, f"{what}: rel err {e:.3e} > {tol:.3e} (max abs diff {abs_max:.3e})"
     if rows.size:
         idx = np.unravel_index(worst, ref.shape[:-1]) if ref.ndim > 1 else (worst,)

@@ -205,6 +205,17 @@ def test_gated_strong_decay(shape):
              scale=0.0, seed=11, decay_mean=-5.0)
 
 
+@pytest.mark.parametrize("shape", [(80, 200, 8, 2, 64, 64), (40, 300, 16, 4, 128, 128)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32out", "bf16out"])
+def test_gated_grouped_heads_several_chunks_per_cta(shape, out_dtype):
+    """At least one CTA per SM without sequence segments, so every CTA walks
+    several chunks with four query heads per kv head: the state warps emit
+    each chunk's outputs around the next chunk's state conversion."""
+    B, T, Hq, Hkv, Dk, Dv = shape
+    run_case(B, T, Hq, Hkv, Dk, Dv, torch.bfloat16, out_dtype, "none", False, rule="gated", S0=True, scale=0.0,
+             seed=13)
+
+
 @pytest.mark.parametrize("shape", [(2, 200, 4, 2, 64, 64), (1, 257, 8, 2, 128, 128), (2, 300, 2, 2, 64, 64)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
