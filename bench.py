@@ -345,7 +345,8 @@ def time_workload(la, w, steps, warmup, stream, causal=True):
     p = la.make_params(batch=w.B, seq_len=w.T, q_heads=w.q_heads, kv_heads=w.kv_heads, key_dim=w.Dk,
                        value_dim=w.Dv, io_dtype=w.dtype, feature_map=w.feature_map,
                        use_normalizer=w.use_normalizer, epsilon=w.eps, scale=w.scale, update_rule=w.rule)
-    ws = torch.empty(max(1, la.la_workspace_bytes(p, causal)), dtype=torch.uint8, device="cuda")
+    need = la.la_delta_workspace_bytes(p) if w.rule in ("delta", "gated_delta") else la.la_workspace_bytes(p, causal)
+    ws = torch.empty(max(1, need), dtype=torch.uint8, device="cuda")
 
     def step(i):
         q, k, v, d, y, m, bt = sets[i % nsets]

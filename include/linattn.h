@@ -229,11 +229,32 @@ la_status la_decode_step_masked(const la_params* p, const void* q, const void* k
  *              beta_per_head = 1, (B, T, 1) when 0.
  *   mask       (B, T) uint8 validity or NULL (as la_forward_causal_masked).
  *   S0, S_out  as la_forward_causal (Z is not used by these rules).
- * The update is not additive in S, so every (batch, kv head) stream runs as
- * one token-by-token recurrence on CUDA cores.  No workspace is needed. */
+ * This entry point runs every (batch, kv head) stream as one token-by-token
+ * recurrence on CUDA cores and needs no workspace; la_forward_causal_delta_ws
+ * is the chunk-parallel tensor-core form. */
 la_status la_forward_causal_delta(const la_params* p, const void* q, const void* k, const void* v,
                                   const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
                                   const float* S0, void* y, float* S_out, la_stream_t stream);
+
+/* The delta rules in chunk-parallel form on the tensor cores (the operator
+ * page's "chunk-parallel WY decomposition during prefill"): arguments,
+ * results and errors as la_forward_causal_delta, plus a workspace.  Per
+ * chunk of 64 steps the rule is solved in closed form -- a unit
+ * lower-triangular system gives the chunk's updates U = U' - W S0, its
+ * outputs and its state transition S <- M S + N -- and a scan carries the
+ * state from chunk to chunk.  Covers bf16 io with key_dim = value_dim = 128
+ * and one decay per kv head (la_delta_workspace_bytes > 0); other shapes run
+ * the token-by-token recurrence of la_forward_causal_delta and need no
+ * workspace.
+ *   ws   workspace of ws_bytes >= la_delta_workspace_bytes(p): about
+ *        263 KB per (batch, kv head, 64-step chunk), 256-byte aligned, not
+ *        shared with a call that may run at the same time.
+ * S_out may alias S0. */
+size_t la_delta_workspace_bytes(const la_params* p);
+la_status la_forward_causal_delta_ws(const la_params* p, const void* q, const void* k, const void* v,
+                                     const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
+                                     const float* S0, void* y, float* S_out, void* ws, size_t ws_bytes,
+                                     la_stream_t stream);
 
 /* One token per sequence with a delta rule (seq_len must be 1): S is read
  * and updated in place; beta (B, 1, Hkv) or (B, 1, 1); mask (B,) or NULL. */

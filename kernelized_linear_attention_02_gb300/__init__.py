@@ -58,6 +58,9 @@ _SIGNATURES = {
     "la_forward_causal_delta": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 5 + [ctypes.c_int]
                                 + [_vp] * 4 + [_vp]),
     "la_decode_step_delta": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 5 + [ctypes.c_int] + [_vp] * 4),
+    "la_delta_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(la_params)]),
+    "la_forward_causal_delta_ws": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 5 + [ctypes.c_int]
+                                   + [_vp] * 4 + [_vp, ctypes.c_size_t, _vp]),
     "la_backward_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(la_params)]),
     "la_backward_causal": (ctypes.c_int, [ctypes.POINTER(la_params)] + [_vp] * 12 + [ctypes.c_size_t, _vp]),
     "la_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -228,8 +231,16 @@ def la_forward_causal(q, k, v, *, q_heads, kv_heads, feature_map="elu_plus_one",
     if update_rule in DELTA_RULES:
         bph = _beta(beta, B, T, kv_heads)
         m = _mask(mask, B, T) if mask is not None else None
-        _check(lib().la_forward_causal_delta(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta), bph,
-                                             _ptr(m), _ptr(S0), _ptr(y), _ptr(S), _stream(stream)))
+        need = int(lib().la_delta_workspace_bytes(ctypes.byref(p)))
+        if need > 0:  # the chunk-parallel tensor-core form
+            if workspace is None or workspace.numel() * workspace.element_size() < need:
+                workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            _check(lib().la_forward_causal_delta_ws(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta),
+                                                    bph, _ptr(m), _ptr(S0), _ptr(y), _ptr(S), _ptr(workspace),
+                                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+        else:
+            _check(lib().la_forward_causal_delta(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta),
+                                                 bph, _ptr(m), _ptr(S0), _ptr(y), _ptr(S), _stream(stream)))
         return (y, (S, None)) if return_state else y
     ws, ws_bytes = _workspace(p, True, q.device, workspace)
     if mask is not None:
@@ -370,3 +381,8 @@ def la_device_status(reset: bool = True) -> int:
     """Synchronise the device and return LA_OK, or LA_ERR_TIMEOUT when a
     kernel gave up on a bounded wait (LA_ERR_CUDA on a device error)."""
     return int(lib().la_device_status(int(bool(reset))))
+
+
+def la_delta_workspace_bytes(params: la_params) -> int:
+    """Workspace of la_forward_causal_delta_ws (0: the shape runs the recurrence)."""
+    return int(lib().la_delta_workspace_bytes(ctypes.byref(params)))

@@ -399,6 +399,40 @@ la_status la_forward_causal_delta(const la_params* p, const void* q, const void*
     return LA_OK;
 }
 
+size_t la_delta_workspace_bytes(const la_params* p) {
+    la::Problem P;
+    if (make_problem(p, Call::kDelta, &P) != LA_OK) return 0;
+    return la::delta_chunk_workspace_bytes(P);
+}
+
+la_status la_forward_causal_delta_ws(const la_params* p, const void* q, const void* k, const void* v,
+                                     const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
+                                     const float* S0, void* y, float* S_out, void* ws, size_t ws_bytes,
+                                     la_stream_t stream) {
+    la::Problem P;
+    la_status st = make_problem(p, Call::kDelta, &P);
+    if (st != LA_OK) return st;
+    if (beta_per_head != 0 && beta_per_head != 1) return fail(LA_ERR_INVALID_ARG, "beta_per_head must be 0 or 1");
+    P.mask = mask;
+    const size_t need = la::delta_chunk_workspace_bytes(P);
+    if (P.T == 0 || need == 0)  // no chunk form for this shape: the recurrence, which needs no workspace
+        return la_forward_causal_delta(p, q, k, v, decay, beta, beta_per_head, mask, S0, y, S_out, stream);
+    if (!q || !k || !v || !y || !beta) return fail(LA_ERR_INVALID_ARG, "q, k, v, beta and y are required");
+    if (P.gated && !decay) return fail(LA_ERR_INVALID_ARG, "gated_delta needs decay");
+    if (!ws || ws_bytes < need)
+        return fail(LA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, ws ? ws_bytes : 0);
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(LA_ERR_WORKSPACE, "workspace must be %zu-byte aligned", kAlign);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (la::chunk_pointers_ok(q, k, v, y))
+        e = la::delta_chunk_causal(P, q, k, v, P.gated ? decay : nullptr, beta, beta_per_head, S0, y, S_out, ws, s);
+    else
+        e = la::recurrent_delta(P, q, k, v, P.gated ? decay : nullptr, beta, beta_per_head, S0, y, S_out, s);
+    if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal_delta_ws");
+    g_last_error.clear();
+    return LA_OK;
+}
+
 la_status la_decode_step_delta(const la_params* p, const void* q, const void* k, const void* v,
                                const void* decay, const void* beta, int beta_per_head, const uint8_t* mask,
                                float* S, void* y, la_stream_t stream) {

@@ -32,6 +32,14 @@ cudaError_t recurrent_delta(const Problem& P, const void* q, const void* k, cons
                             const void* beta, int beta_per_head, const float* S0, void* y, float* S_out,
                             cudaStream_t st);
 
+// Delta rules in chunk-parallel (WY) form on the tensor cores (delta_chunk.cu):
+// bf16 inputs, Dk == Dv == 128, one log decay per kv head.
+bool delta_chunk_supported(const Problem& P);
+size_t delta_chunk_workspace_bytes(const Problem& P);
+cudaError_t delta_chunk_causal(const Problem& P, const void* q, const void* k, const void* v, const void* decay,
+                               const void* beta, int beta_per_head, const float* S0, void* y, float* S_out,
+                               void* ws, cudaStream_t st);
+
 // Tensor-core chunk path (chunk_host.cu): bf16 inputs, Dk == Dv in {64, 128}.
 bool chunk_supported(const Problem& P);
 bool chunk_pointers_ok(const void* q, const void* k, const void* v, const void* y);

@@ -163,3 +163,83 @@ def test_gated_delta_workload_sampled_slices():
                                  scale=w.scale, rule=w.rule, decay=d[b:b + 1, :, hk:hk + 1],
                                  beta=beta[b:b + 1, :, hk:hk + 1])
         assert_close(to64(y[b:b + 1, :, hk * G:(hk + 1) * G]), yr, tol_for(w.dtype, w.dtype), f"slice {b},{hk}")
+
+
+# ---------------------------------------------------------------------------
+# the chunk-parallel (WY) tensor-core form: bf16, Dk = Dv = 128, decay per kv head
+
+TC_CASES = [  # B, T, Hq, Hkv, rule, beta heads (Hkv or 1)
+    (2, 300, 4, 2, "gated_delta", 2),
+    (1, 257, 6, 2, "delta", 1),
+    (3, 130, 3, 1, "gated_delta", 1),
+    (1, 64, 1, 1, "delta", 1),
+    (2, 1000, 8, 8, "gated_delta", 8),
+    (1, 513, 2, 1, "gated_delta", 1),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: "x".join(map(str, c[:4])) + f"-{c[4]}-b{c[5]}")
+@pytest.mark.parametrize("masked", [False, True], ids=["nomask", "mask"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32out", "bf16out"])
+def test_delta_tensor_core_form(case, masked, out_dtype):
+    B, T, Hq, Hkv, rule, bh = case
+    D = 128
+    q, k, v, beta, decay = delta_inputs(B, T, Hq, Hkv, D, D, torch.bfloat16, rule, False, bh, 31)
+    S0 = rand((B, Hkv, D, D), 35, torch.float32)
+    mask = inputs.validity_mask("gaps", B, T, 36, DEV) if masked else None
+    p = la.make_params(batch=B, seq_len=T, q_heads=Hq, kv_heads=Hkv, key_dim=D, value_dim=D, feature_map="none",
+                       use_normalizer=False, update_rule=rule)
+    assert la.la_delta_workspace_bytes(p) > 0  # this shape takes the tensor-core form
+    n0 = la.la_launch_count()
+    y, (S, _) = la.la_forward_causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False,
+                                     scale=0.0, update_rule=rule, decay=decay, beta=beta, initial_state=(S0, None),
+                                     return_state=True, out_dtype=out_dtype, mask=mask)
+    torch.cuda.synchronize()
+    assert la.la_launch_count() - n0 == 3  # prep, scan, out
+    yr, Sr, _ = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False, scale=0.0,
+                              rule=rule, decay=decay, beta=beta, S0=S0, mask=mask)
+    assert_close(to64(y), yr, tol_for(torch.bfloat16, out_dtype), "y")
+    assert_close(to64(S), Sr, tol_for(torch.bfloat16, torch.float32), "S")
+    if masked:
+        assert torch.count_nonzero(y[~mask]).item() == 0
+
+
+def test_delta_tensor_core_form_in_place_state_and_restarts():
+    """The final state written over the initial one, and log decays of -inf
+    (forget everything) inside and on the edges of chunks."""
+    B, T, Hq, Hkv, D = 2, 400, 4, 2, 128
+    q, k, v, beta, decay = delta_inputs(B, T, Hq, Hkv, D, D, torch.bfloat16, "gated_delta", False, Hkv, 41)
+    d = decay.float()
+    for t, h in [(10, 0), (63, 1), (64, 0), (200, 1), (399, 0)]:
+        d[:, t, h] = -float("inf")
+    decay = d.to(torch.bfloat16)
+    S0 = rand((B, Hkv, D, D), 45, torch.float32)
+    S = S0.clone()
+    y, _ = la.la_forward_causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False,
+                                scale=0.0, update_rule="gated_delta", decay=decay, beta=beta, initial_state=(S, None),
+                                return_state=True, state_out=(S, None), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    yr, Sr, _ = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False, scale=0.0,
+                              rule="gated_delta", decay=decay, beta=beta, S0=S0)
+    assert np.isfinite(yr).all()
+    assert_close(to64(y), yr, tol_for(torch.bfloat16, torch.float32), "y")
+    assert_close(to64(S), Sr, tol_for(torch.bfloat16, torch.float32), "S")
+
+
+def test_delta_tensor_core_form_chunked_calls_equal_one_call():
+    """Calls over consecutive pieces with the state carried equal one call."""
+    B, T, Hq, Hkv, D = 1, 600, 4, 2, 128
+    q, k, v, beta, decay = delta_inputs(B, T, Hq, Hkv, D, D, torch.bfloat16, "gated_delta", False, 1, 51)
+    kw = dict(q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False, update_rule="gated_delta",
+              out_dtype=torch.float32)
+    S = torch.zeros(B, Hkv, D, D, device=DEV)
+    ys = []
+    for a0, a1 in [(0, 100), (100, 164), (164, 600)]:
+        c = lambda x: x[:, a0:a1].contiguous()
+        ys.append(la.la_forward_causal(c(q), c(k), c(v), decay=c(decay), beta=c(beta), initial_state=(S, None),
+                                       return_state=True, state_out=(S, None), **kw)[0])
+    torch.cuda.synchronize()
+    yr, Sr, _ = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False,
+                              rule="gated_delta", decay=decay, beta=beta)
+    assert_close(to64(torch.cat(ys, 1)), yr, tol_for(torch.bfloat16, torch.float32), "chunked y")
+    assert_close(to64(S), Sr, tol_for(torch.bfloat16, torch.float32), "chunked S")
