@@ -105,14 +105,28 @@ la_status make_problem(const la_params* p, Call call, la::Problem* P) {
 size_t state_bytes(const la::Problem& P) { return sizeof(float) * (size_t)P.B * P.Hkv * P.Dk * P.Dv; }
 size_t key_state_bytes(const la::Problem& P) { return sizeof(float) * (size_t)P.B * P.Hkv * P.Dk; }
 
+size_t recurrent_need(const la::Problem& P, bool causal) {
+    return causal ? la::recurrent_workspace_bytes(P) : round_up(state_bytes(P)) + round_up(key_state_bytes(P));
+}
+
+// Workspace that lets the call take its fastest path (la_workspace_bytes).
 size_t workspace_bytes(const la::Problem& P, bool causal) {
-    const size_t rec = causal ? la::recurrent_workspace_bytes(P) : round_up(state_bytes(P)) + round_up(key_state_bytes(P));
+    const size_t rec = recurrent_need(P, causal);
+    if (causal && P.decay_dim) return std::max(rec, la::perdim_chunk_workspace_bytes(P));
     if (!la::chunk_supported(P)) return rec;
     return std::max(rec, la::chunk_workspace_bytes(P, causal));
 }
 
+// Smallest workspace the call accepts.  With one decay per key dimension
+// that is the recurrence's: the tensor-core form runs when the workspace
+// also holds its chunk tiles (workspace_bytes).
+size_t required_workspace_bytes(const la::Problem& P, bool causal) {
+    if (causal && P.decay_dim) return recurrent_need(P, causal);
+    return workspace_bytes(P, causal);
+}
+
 la_status check_ws(const la::Problem& P, bool causal, void* ws, size_t ws_bytes) {
-    const size_t need = workspace_bytes(P, causal);
+    const size_t need = required_workspace_bytes(P, causal);
     if (need == 0) return LA_OK;
     if (!ws || ws_bytes < need)
         return fail(LA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, ws ? ws_bytes : 0);
@@ -240,10 +254,14 @@ la_status la_forward_causal_masked(const la_params* p, const void* q, const void
     if (P.gated && !decay) return fail(LA_ERR_INVALID_ARG, "the gated rule needs decay");
     if ((st = check_ws(P, true, ws, ws_bytes)) != LA_OK) return st;
     cudaError_t e;
-    // per-key-dimension decay: the CUDA-core recurrence (the chunk kernel
-    // factors one decay per kv head)
+    // per-key-dimension decay: its own tensor-core form when the workspace
+    // holds its chunk tiles, else the CUDA-core recurrence
+    const size_t pd_need = P.decay_dim ? la::perdim_chunk_workspace_bytes(P) : 0;
     if (!P.decay_dim && la::chunk_supported(P) && la::chunk_pointers_ok(q, k, v, y))
         e = la::chunk_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, ws, s);
+    else if (pd_need > 0 && ws && ws_bytes >= pd_need && la::chunk_pointers_ok(q, k, v, y) &&
+             reinterpret_cast<uintptr_t>(decay) % 16 == 0)
+        e = la::perdim_chunk_causal(P, q, k, v, decay, S0, y, S_out, ws, s);
     else
         e = la::recurrent_causal(P, q, k, v, P.gated ? decay : nullptr, S0, Z0, y, S_out, Z_out, s, ws, ws_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "la_forward_causal");
@@ -264,7 +282,10 @@ la_status la_forward_causal_noalloc(const la_params* p, const void* q, const voi
     la_status st = make_problem(p, Call::kCausal, &P);
     if (st != LA_OK) return st;
     if (P.T == 0) return la_forward_causal(p, q, k, v, decay, S0, Z0, y, S_out, Z_out, nullptr, 0, stream);
-    const size_t need = workspace_bytes(P, true);
+    // the fastest path that fits the scratch (with one decay per key
+    // dimension the recurrence when the tensor-core tiles do not fit)
+    const size_t full = workspace_bytes(P, true);
+    const size_t need = full <= LA_NOALLOC_SCRATCH_BYTES ? full : required_workspace_bytes(P, true);
     if (need > LA_NOALLOC_SCRATCH_BYTES)
         return fail(LA_ERR_WORKSPACE,
                     "la_forward_causal_noalloc: this problem needs %zu bytes of scratch, more than the %zu "

@@ -37,7 +37,9 @@
 #include <atomic>
 #include <cstring>
 
+#include "delta_args.h"
 #include "kernels.h"
+#include "tiles.cuh"
 #include "tma_host.h"
 #include "umma.cuh"
 
@@ -45,6 +47,7 @@ namespace la {
 namespace delta {
 
 using namespace umma;
+using namespace tile;
 
 constexpr int kC = 64;   // steps per chunk
 constexpr int kD = 128;  // Dk = Dv
@@ -55,74 +58,7 @@ constexpr float kMinLogDecay = -200.f;
 // error bits of the delta kernels' bounded waits
 enum : unsigned { kErrLoad = 1u << 16, kErrMma = 1u << 17 };
 
-// Workspace of one chunk (bytes).  Tiles are stored in the shared-memory
-// operand layout they are used in (128-byte swizzled K-major rows), so the
-// consumer loads them with plain bulk copies.
-struct Ws {
-    static constexpr size_t kW = 0;        // W as B operand: rows t (64), K = k in 2 blocks of 8 KB; hi, lo
-    static constexpr size_t kU = 32768;    // U' fp32 [t][v]
-    static constexpr size_t kM = 65536;    // M as B operand: rows k' (128), K = k in 2 blocks of 16 KB; hi, lo
-    static constexpr size_t kN = 131072;   // N fp32 [k][v]
-    static constexpr size_t kS = 196608;   // start state S^T as A operand: rows v (128), K = k; hi, lo
-    static constexpr size_t kG = 262144;   // G_t (64 floats), then the step-validity word (2 floats)
-    static constexpr size_t kChunk = 263168;
-};
 
-struct Args {
-    int B, T, Hq, Hkv, G, nc;  // nc: chunks per stream
-    int gated, beta_per_head, out_bf16;
-    float scale;
-    const __nv_bfloat16* decay;  // (B, T, Hkv), log space
-    const __nv_bfloat16* beta;   // (B, T, Hkv) or (B, T)
-    const uint8_t* mask;         // (B, T) or null
-    const float* S0;             // (B*Hkv, Dk, Dv) or null (zeros)
-    float* S_out;                // (B*Hkv, Dk, Dv) or null
-    void* y;                     // (B, T, Hq, Dv)
-    uint8_t* ws;
-    unsigned* err;
-};
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
-}
-// byte offset of 16-byte chunk cc (8 bf16) of row r in a 128-byte swizzled block
-__device__ __forceinline__ uint32_t swc(int r, int cc) {
-    return static_cast<uint32_t>(r * 128 + (((cc ^ (r & 7))) << 4));
-}
-// byte offset of bf16 element (r, col) (col < 64) in a 128-byte swizzled block
-__device__ __forceinline__ uint32_t swe(int r, int col) { return swc(r, col >> 3) + ((col & 7) << 1); }
-
-__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t*>(&h); }
-// x = hi + lo, hi = bf16(x), lo = bf16(x - hi), for a pair
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    const float2 hf = __bfloat1622float2(h);
-    hi = bf2_bits(h);
-    lo = bf2_bits(__floats2bfloat162_rn(x0 - hf.x, x1 - hf.y));
-}
-// hi and lo parts of 8 values as two 16-byte words
-__device__ __forceinline__ void split8(const float* f, uint4& hi, uint4& lo) {
-    split2(f[0], f[1], hi.x, lo.x);
-    split2(f[2], f[3], hi.y, lo.y);
-    split2(f[4], f[5], hi.z, lo.z);
-    split2(f[6], f[7], hi.w, lo.w);
-}
-__device__ __forceinline__ void st16(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
-
-// 64-bit word from the flags of steps 2 lane (even) and 2 lane + 1 (odd);
-// warp-collective
-__device__ __forceinline__ uint64_t step_word(bool even, bool odd) {
-    auto spread = [](uint64_t x) {  // bit i -> bit 2i
-        x = (x | (x << 16)) & 0x0000FFFF0000FFFFull;
-        x = (x | (x << 8)) & 0x00FF00FF00FF00FFull;
-        x = (x | (x << 4)) & 0x0F0F0F0F0F0F0F0Full;
-        x = (x | (x << 2)) & 0x3333333333333333ull;
-        x = (x | (x << 1)) & 0x5555555555555555ull;
-        return x;
-    };
-    const uint32_t e = __ballot_sync(0xffffffffu, even), o = __ballot_sync(0xffffffffu, odd);
-    return spread(e) | (spread(o) << 1);
-}
 
 // Decay and update rate of steps 2 lane and 2 lane + 1 of chunk t0 (one warp):
 // writes the inclusive cumulative log decay G_t and b_t (zero for steps that
@@ -882,32 +818,6 @@ __global__ void __launch_bounds__(256, 1)
     }
 }
 
-// (D, H, T, B) view of a bf16 activation, 64 x 64 boxes, 128-byte swizzle
-bool act_map(CUtensorMap* m, const void* base, int H, int64_t T, int64_t B) {
-    const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)H, (uint64_t)T, (uint64_t)B};
-    const uint64_t str[3] = {kD * 2, (uint64_t)H * kD * 2, (uint64_t)T * H * kD * 2};
-    const uint32_t box[4] = {64, 1, 64, 1};
-    return make_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, 4, dims, str, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-// Raises the dynamic shared-memory limit of a kernel once per device and
-// context.
-template <typename K>
-cudaError_t configure(K kern, int bytes, std::atomic<uint64_t>* flags) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    const uint64_t ctx = current_context_id();
-    if (ctx == 0 || flags[dev].load(std::memory_order_acquire) != ctx) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        flags[dev].store(current_context_id(), std::memory_order_release);
-    }
-    return cudaSuccess;
-}
-
 }  // namespace delta
 
 bool delta_chunk_supported(const Problem& P) {
@@ -956,6 +866,7 @@ cudaError_t delta_chunk_causal(const Problem& P, const void* q, const void* k, c
     a.y = y;
     a.ws = static_cast<uint8_t*>(ws);
     a.err = err;
+    if (!a.beta || !a.y || !a.ws || (a.gated && !a.decay)) return cudaErrorInvalidValue;  // every pointer the kernels use
     const unsigned streams = (unsigned)(P.B * P.Hkv);
     const unsigned chunks = streams * (unsigned)a.nc;
     delta_prep_kernel<<<chunks, 256, PrepSmem::kBytes, st>>>(a, mk, mv);
@@ -964,5 +875,16 @@ cudaError_t delta_chunk_causal(const Problem& P, const void* q, const void* k, c
     note_launch(3);
     return cudaGetLastError();
 }
+
+namespace delta {
+cudaError_t scan(const Args& a, unsigned streams, cudaStream_t st) {
+    static std::atomic<uint64_t> cfg[kMaxDevices];
+    cudaError_t e = tile::configure(delta_scan_kernel, ScanSmem::kBytes, cfg);
+    if (e != cudaSuccess) return e;
+    delta_scan_kernel<<<streams, 128, ScanSmem::kBytes, st>>>(a);
+    note_launch();
+    return cudaGetLastError();
+}
+}  // namespace delta
 
 }  // namespace la

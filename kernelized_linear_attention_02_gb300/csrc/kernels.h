@@ -40,6 +40,13 @@ cudaError_t delta_chunk_causal(const Problem& P, const void* q, const void* k, c
                                const void* beta, int beta_per_head, const float* S0, void* y, float* S_out,
                                void* ws, cudaStream_t st);
 
+// The gated rule with one log decay per key dimension in chunk-parallel form on
+// the tensor cores (perdim_chunk.cu): bf16 inputs, Dk == Dv == 128.
+bool perdim_chunk_supported(const Problem& P);
+size_t perdim_chunk_workspace_bytes(const Problem& P);
+cudaError_t perdim_chunk_causal(const Problem& P, const void* q, const void* k, const void* v, const void* decay,
+                                const float* S0, void* y, float* S_out, void* ws, cudaStream_t st);
+
 // Tensor-core chunk path (chunk_host.cu): bf16 inputs, Dk == Dv in {64, 128}.
 bool chunk_supported(const Problem& P);
 bool chunk_pointers_ok(const void* q, const void* k, const void* v, const void* y);

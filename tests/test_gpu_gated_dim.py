@@ -126,3 +126,69 @@ def test_per_key_dim_workload_sampled_slices():
                                  q_heads=G, kv_heads=1, feature_map=w.feature_map, use_normalizer=w.use_normalizer,
                                  scale=w.scale, rule="gated", decay=d[b:b + 1, :, hk:hk + 1].reshape(1, w.T, w.Dk))
         assert_close(to64(y[b:b + 1, :, hk * G:(hk + 1) * G]), yr, tol_for(w.dtype, w.dtype), f"slice {b},{hk}")
+
+
+# ---------------------------------------------------------------------------
+# the chunk-parallel tensor-core form (bf16, Dk = Dv = 128)
+
+TC_SHAPES = [  # B, T, Hq, Hkv
+    (2, 300, 4, 2),
+    (1, 257, 3, 1),
+    (3, 130, 1, 1),
+    (1, 640, 8, 1),
+]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mean", [3.0, -1.0, -4.0], ids=["mild", "strong", "very-strong"])
+@pytest.mark.parametrize("masked", [False, True], ids=["nomask", "mask"])
+def test_per_key_dim_tensor_core_form(shape, mean, masked):
+    """Mild decays factor in every chunk; strong ones (cumulative decay below
+    -80 inside a chunk) make those chunks compute their scores on CUDA cores."""
+    B, T, Hq, Hkv = shape
+    D = 128
+    q = rand((B, T, Hq, D), 31, torch.bfloat16)
+    k = rand((B, T, Hkv, D), 32, torch.bfloat16)
+    v = rand((B, T, Hkv, D), 33, torch.bfloat16)
+    d = perdim_decay(B, T, Hkv, D, 34, torch.bfloat16, mean)
+    S0 = rand((B, Hkv, D, D), 35, torch.float32)
+    mask = inputs.validity_mask("gaps", B, T, 36, DEV) if masked else None
+    p = la.make_params(batch=B, seq_len=T, q_heads=Hq, kv_heads=Hkv, key_dim=D, value_dim=D, feature_map="none",
+                       use_normalizer=False, update_rule="gated", decay_per_key_dim=True)
+    assert la.la_workspace_bytes(p, True) > 0
+    kw = dict(q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False, scale=0.0, update_rule="gated")
+    n0 = la.la_launch_count()
+    y, (S, _) = la.la_forward_causal(q, k, v, decay=d, initial_state=(S0, None), return_state=True, mask=mask,
+                                     out_dtype=torch.float32, **kw)
+    torch.cuda.synchronize()
+    assert la.la_launch_count() - n0 == 3  # prep, scan, out
+    yr, Sr, _ = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False,
+                              scale=0.0, rule="gated", decay=d.reshape(B, T, Hkv * D), S0=S0, mask=mask)
+    tol = tol_for(torch.bfloat16, torch.float32)
+    assert_close(to64(y), yr, tol, "y")
+    assert_close(to64(S), Sr, tol, "S")
+    if masked:
+        assert torch.count_nonzero(y[~mask]).item() == 0
+
+
+def test_per_key_dim_tensor_core_form_bf16_out_chunked_in_place():
+    """bf16 output, and calls over consecutive pieces with the state carried
+    in place equal one call."""
+    B, T, Hq, Hkv, D = 2, 500, 4, 2, 128
+    q = rand((B, T, Hq, D), 41, torch.bfloat16)
+    k = rand((B, T, Hkv, D), 42, torch.bfloat16)
+    v = rand((B, T, Hkv, D), 43, torch.bfloat16)
+    d = perdim_decay(B, T, Hkv, D, 44, torch.bfloat16)
+    kw = dict(q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False, update_rule="gated",
+              out_dtype=torch.bfloat16)
+    S = torch.zeros(B, Hkv, D, D, device=DEV)
+    ys = []
+    for a0, a1 in [(0, 64), (64, 199), (199, 500)]:
+        c = lambda x: x[:, a0:a1].contiguous()
+        ys.append(la.la_forward_causal(c(q), c(k), c(v), decay=c(d), initial_state=(S, None), return_state=True,
+                                       state_out=(S, None), **kw)[0])
+    torch.cuda.synchronize()
+    yr, Sr, _ = oracle.causal(q, k, v, q_heads=Hq, kv_heads=Hkv, feature_map="none", use_normalizer=False,
+                              rule="gated", decay=d.reshape(B, T, Hkv * D))
+    assert_close(to64(torch.cat(ys, 1)), yr, tol_for(torch.bfloat16, torch.bfloat16), "chunked y")
+    assert_close(to64(S), Sr, tol_for(torch.bfloat16, torch.float32), "chunked S")

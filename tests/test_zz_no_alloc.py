@@ -7,8 +7,9 @@ zero).  Shapes are chosen so the sequence is split into several segments:
 the scratch is then really used.  This file sorts last so that it also runs
 after every other test in one session; it passes on its own as well.
 """
-import re
+import ctypes
 import os
+import re
 
 import pytest
 import torch
@@ -104,10 +105,21 @@ def test_scratch_size_covers_every_causal_problem_on_this_device():
     # differently (a segment cap plus a copy of the initial state)
     kinds = [dict(io_dtype=torch.bfloat16, feature_map="relu", use_normalizer=True),
              dict(io_dtype=torch.float32, feature_map="relu", use_normalizer=True),
-             dict(io_dtype=torch.bfloat16, feature_map="none", use_normalizer=False, update_rule="gated",
+             dict(io_dtype=torch.float32, feature_map="none", use_normalizer=False, update_rule="gated",
                   decay_per_key_dim=True)]
     for kind in kinds:
         for bh in range(1, 2 * torch.cuda.get_device_properties(0).multi_processor_count + 1):
             p = la.make_params(batch=bh, seq_len=1 << 20, q_heads=1, kv_heads=1, key_dim=128, value_dim=128, **kind)
             worst = max(worst, la.la_workspace_bytes(p, True))
     assert 0 < worst <= la.LA_NOALLOC_SCRATCH_BYTES, worst
+    # bf16 with one decay per key dimension: its tensor-core form wants more
+    # than the scratch on long sequences, and the call then takes the
+    # recurrence, which fits: it gets past the scratch check to the pointer
+    # check (nothing is launched)
+    L = la.lib()
+    for bh in (1, 8, 76, 152):
+        p = la.make_params(batch=bh, seq_len=1 << 20, q_heads=1, kv_heads=1, key_dim=128, value_dim=128,
+                           feature_map="none", use_normalizer=False, update_rule="gated", decay_per_key_dim=True)
+        assert la.la_workspace_bytes(p, True) > la.LA_NOALLOC_SCRATCH_BYTES
+        st = L.la_forward_causal_noalloc(ctypes.byref(p), None, None, None, None, None, None, None, None, None, None)
+        assert st == la.LA_ERR_INVALID_ARG, (bh, st)
