@@ -597,6 +597,8 @@ def run_only(args):
     w = getattr(inputs, args.only)
     if args.batch:
         w = dataclasses.replace(w, B=args.batch)
+    if args.seq_len:
+        w = dataclasses.replace(w, T=args.seq_len)
     stream = torch.cuda.Stream()
     if args.backward:
         ms, lpc, alg = time_backward(la, w, args.steps, args.warmup, stream)
@@ -609,7 +611,7 @@ def run_only(args):
     ms, lpc = time_workload(la, w, args.steps, args.warmup, stream, causal)
     alg = prefill_alg_bytes(w)
     gbs = alg / (ms * 1e-3) / 1e9
-    print(json.dumps({"workload": w.name, "B": w.B, "mode": "causal" if causal else "noncausal", "ms": ms,
+    print(json.dumps({"workload": w.name, "B": w.B, "T": w.T, "mode": "causal" if causal else "noncausal", "ms": ms,
                       "tokens_per_s": w.B * w.T / (ms * 1e-3), "alg_bytes": alg, "achieved_GBps": gbs,
                       "roofline_frac": gbs / peaks()["hbm_gbs"], "launches_per_call": lpc}), flush=True)
 
@@ -647,6 +649,7 @@ def main():
     ap.add_argument("--skip-sweep", action="store_true", help="skip the per-workload roofline sweep")
     ap.add_argument("--only", default=None, help="time one workload of linattn_inputs (e.g. LONG_8K) alone")
     ap.add_argument("--batch", type=int, default=0, help="with --only: batch size override")
+    ap.add_argument("--seq-len", type=int, default=0, help="with --only: sequence length override")
     ap.add_argument("--noncausal", action="store_true", help="with --only: the non-causal pass")
     ap.add_argument("--backward", action="store_true", help="with --only: the backward pass (linear rule)")
     ap.add_argument("--decode-only", action="store_true", help="time the decode step alone (see --prompt)")
