@@ -1,6 +1,5 @@
 // delta_args.h -- workspace layout and arguments of the chunk-parallel tile
-// kernels (delta_chunk.cu, perdim_chunk.cu), and the chunk-to-chunk state scan
-// they share.
+// kernels (delta_chunk.cu, perdim_chunk.cu).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -17,10 +16,11 @@ namespace delta {
 struct Ws {
     static constexpr size_t kW = 0;        // W as B operand: rows t (64), K = k in 2 blocks of 8 KB; hi, lo
     static constexpr size_t kU = 32768;    // U' fp32 [t][v]
-    static constexpr size_t kM = 65536;    // M as B operand: rows k' (128), K = k in 2 blocks of 16 KB; hi, lo
+    static constexpr size_t kM = 65536;    // M as A operand: rows k' (128), K = k in 2 blocks of 16 KB; hi, lo
     static constexpr size_t kN = 131072;   // N fp32 [k][v]
     static constexpr size_t kS = 196608;   // start state S^T as A operand: rows v (128), K = k; hi, lo
-    static constexpr size_t kG = 262144;   // G_t (64 floats), then the step-validity word (2 floats)
+    static constexpr size_t kG = 262144;   // delta: G_t (64 floats), then the step-validity word (2 floats);
+                                           // per key dimension: the transition diagonal e^{G_C[k]} (128 floats)
     static constexpr size_t kChunk = 263168;
 };
 
@@ -37,12 +37,6 @@ struct Args {
     uint8_t* ws;
     unsigned* err;
 };
-
-// The state scan S_{c+1} = M_c S_c + N_c over the chunks of every stream (one
-// CTA per stream, tensor cores): reads M_c and N_c from each chunk's
-// workspace, writes the start state of every chunk there (kS) and the final
-// state to a.S_out; uses a.nc, a.S0, a.S_out, a.ws and a.err.
-cudaError_t scan(const Args& a, unsigned streams, cudaStream_t st);
 
 }  // namespace delta
 }  // namespace la

@@ -25,8 +25,9 @@
 // Three kernels, in stream order:
 //   prep  one CTA per chunk, all chunks at once: T (blocked forward
 //         substitution on CUDA cores), then W, U', M and N on the tensor cores
-//   scan  one CTA per stream: S_{c+1} = M_c S_c + N_c, chunk after chunk; the
-//         start state of every chunk goes to the workspace
+//   scan  S_{c+1} = M_c S_c + N_c, chunk after chunk, each stream's value
+//         columns split over four CTAs; the start state of every chunk goes
+//         to the workspace
 //   out   one CTA per chunk: U and the outputs of every query head
 // Every fp32 operand enters the tensor cores as bf16 hi + lo (about 16
 // significant bits; products of the two lo parts are dropped); keys, values
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(256, 1)
             // K = k), and f_t W[t][k] as this row k of the B operand of M
             __nv_bfloat16* wh = reinterpret_cast<__nv_bfloat16*>(wsc + Ws::kW);
             const int kb = row >> 6, kc = row & 63;
-#pragma unroll 4
+#pragma unroll
             for (int t = 0; t < 64; ++t) {
                 const float x = val(t);
                 const __nv_bfloat16 h = __float2bfloat16_rn(x);
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(256, 1)
         } else {
             // U'[t][v] to the workspace, and f_t U'[t][v] as row v of the A operand of N^T
             float* up = reinterpret_cast<float*>(wsc + Ws::kU);
-#pragma unroll 8
+#pragma unroll
             for (int t = 0; t < 64; ++t) up[t * kD + row] = val(t);
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(256, 1)
         const int quad = warp & 3, row = quad * 32 + lane;
         const float gammaC = __expf(Gs[kC - 1]);
         if (warp < 4) {
-            // row k' of M = gamma_C I - D, to the workspace (B operand of the
+            // row k' of M = gamma_C I - D, to the workspace (A operand of the
             // scan: rows k', K = k), hi + lo
             uint8_t* mt = wsc + Ws::kM;
 #pragma unroll 1
@@ -439,39 +440,45 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 // ------------------------------------------------------------------ scan
+// The columns of the state are independent under S <- M S + N (M acts on the
+// key dimension), so each stream's scan is split over kScanSplit CTAs of
+// kScanV value columns each: per chunk the CTA computes its block of M_c S_c
+// (M = 128 keys, N = kScanV values, K = 128) on the tensor cores, adds N_c in
+// fp32 and writes the next start state as the B operand of the next chunk's
+// product.  The smaller product and epilogue shorten the chunk-to-chunk chain.
+constexpr int kScanV = 32;                 // value columns per CTA
+constexpr int kScanSplit = kD / kScanV;    // CTAs per stream
 struct ScanSmem {
-    static constexpr int kM = 0;            // two M stages of 64 KB (hi 32 KB, lo 32 KB)
-    static constexpr int kN = 131072;       // N fp32 [k][v]
-    static constexpr int kBar = kN + 65536;  // mfull[2], nfull, mma, TMEM slot
+    static constexpr int kM = 0;           // two M stages of 64 KB (A operand, rows k'; hi 32 KB, lo 32 KB)
+    static constexpr int kB = 131072;      // S block as B operand (rows v, K = k): hi 8 KB, lo 8 KB
+    static constexpr int kBar = kB + 16384;  // mfull[2], mma, TMEM slot
     static constexpr int kBytes = kBar + 64 + 1024;
 };
-constexpr uint32_t kScanHi = 0, kScanLo = 64, kScanD = 128;
 
 __global__ void __launch_bounds__(128, 1) delta_scan_kernel(const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* Mr = sm + ScanSmem::kM;
-    const float* Nb = reinterpret_cast<const float*>(sm + ScanSmem::kN);
+    uint8_t* Bt = sm + ScanSmem::kB;
     uint64_t* mfull = reinterpret_cast<uint64_t*>(sm + ScanSmem::kBar);  // [2]
-    uint64_t* nfull = mfull + 2;
-    uint64_t* bar_mma = mfull + 3;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mfull + 4);
+    uint64_t* bar_mma = mfull + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mfull + 3);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x, nc = a.nc;
-    const int v = tid;  // value row of S^T held by this thread (TMEM lane)
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int bh = blockIdx.x / kScanSplit, v0 = kScanV * (blockIdx.x - bh * kScanSplit);
+    const int nc = a.nc;
+    const int kr = tid;  // key row k' of the product held by this thread (TMEM lane)
     uint8_t* ws0 = a.ws + (size_t)bh * nc * Ws::kChunk;
     unsigned* err = a.err;
 
     if (tid == 0) {
         mbar_init(&mfull[0], 1);
         mbar_init(&mfull[1], 1);
-        mbar_init(nfull, 1);
         mbar_init(bar_mma, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
-        tmem_alloc(tslot, 256);
+        tmem_alloc(tslot, 32);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -483,96 +490,107 @@ __global__ void __launch_bounds__(128, 1) delta_scan_kernel(const __grid_constan
             mbar_arrive_expect_tx(&mfull[c], 65536);
             bulk_load(Mr + c * 65536, ws0 + (size_t)c * Ws::kChunk + Ws::kM, 65536, &mfull[c]);
         }
-        mbar_arrive_expect_tx(nfull, 65536);
-        bulk_load(sm + ScanSmem::kN, ws0 + Ws::kN, 65536, nfull);
     }
-
-    // row v of S^T (32 columns k at a time): hi/lo into TMEM, and to the
-    // workspace as row v of chunk c's start state (A operand of the output kernel)
-    auto put_state = [&](const float (&s)[32], int p, int c) {
-        uint32_t h[16], l[16];
+    // S[k'][v0 .. v0 + 31] as column k' of the B tile (row v, K = k'), hi and lo
+    auto put_block = [&](const float (&s)[kScanV]) {
+        const uint32_t base = (kr >> 6) * 4096;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) split2(s[2 * x], s[2 * x + 1], h[x], l[x]);
-        tmem_st16(tmem_addr(tmem + kScanHi, warp * 32, 16 * p), h);
-        tmem_st16(tmem_addr(tmem + kScanLo, warp * 32, 16 * p), l);
-        if (c < nc) {
-            uint8_t* st = ws0 + (size_t)c * Ws::kChunk + Ws::kS;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int k0 = 32 * p + 8 * q4;
-                const uint32_t off = (k0 >> 6) * 16384 + swc(v, (k0 & 63) >> 3);
-                st16(st + off, make_uint4(h[4 * q4], h[4 * q4 + 1], h[4 * q4 + 2], h[4 * q4 + 3]));
-                st16(st + 32768 + off, make_uint4(l[4 * q4], l[4 * q4 + 1], l[4 * q4 + 2], l[4 * q4 + 3]));
-            }
+        for (int x = 0; x < kScanV; ++x) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(s[x]);
+            const uint32_t off = base + swe(x, kr & 63);
+            *reinterpret_cast<__nv_bfloat16*>(Bt + off) = h;
+            *reinterpret_cast<__nv_bfloat16*>(Bt + 8192 + off) = __float2bfloat16_rn(s[x] - __bfloat162float(h));
         }
     };
-#pragma unroll 1
-    for (int p = 0; p < 4; ++p) {
-        float s[32];
+    auto load_row = [&](const float* src, float (&s)[kScanV]) {  // 32 consecutive floats, 16-byte aligned
 #pragma unroll
-        for (int x = 0; x < 32; ++x) s[x] = a.S0 ? a.S0[(size_t)bh * kD * kD + (size_t)(32 * p + x) * kD + v] : 0.f;
-        put_state(s, p, 0);
+        for (int x = 0; x < kScanV; x += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(src + x);
+            s[x] = f.x, s[x + 1] = f.y, s[x + 2] = f.z, s[x + 3] = f.w;
+        }
+    };
+    {
+        float s[kScanV];  // (the state pointers are only 4-byte aligned)
+        const float* s0 = a.S0 ? a.S0 + (size_t)bh * kD * kD + (size_t)kr * kD + v0 : nullptr;
+#pragma unroll
+        for (int x = 0; x < kScanV; ++x) s[x] = s0 ? s0[x] : 0.f;
+        put_block(s);
     }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
     bool ok = true;
-    constexpr uint32_t id = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t id = idesc_bf16(128, kScanV, false, false);
 #pragma unroll 1
     for (int c = 0; c < nc; ++c) {
-        tmem_st_wait();
-        tc_fence_before();
-        ok = __syncthreads_and(ok);  // every exit below is taken by the whole block
-        if (!ok) break;
+        uint8_t* wsc = ws0 + (size_t)c * Ws::kChunk;
+        bool mok = true;  // M_c arrived (thread 0)
         if (tid == 0) {
             tc_fence_after();
-            // S_{c+1}^T - N^T = S_c^T M_c^T: A = S_c^T (TMEM, hi/lo), B = M_c (rows k')
-            if (mbar_wait(&mfull[c & 1], (c >> 1) & 1, err, kErrLoad)) {
+            // the start state of chunk c (rows v0 .. v0 + 31 of each K block of its S^T tile)
+#pragma unroll
+            for (int part = 0; part < 4; ++part) {  // (hi, lo) x K block
+                const int kb = part & 1, lo = part >> 1;
+                bulk_store(wsc + Ws::kS + lo * 32768 + kb * 16384 + v0 * 128, Bt + lo * 8192 + kb * 4096, 4096);
+            }
+            bulk_commit_group();
+            // M_c S_c: A = M_c (rows k', K = k), B = S_c block (rows v, K = k)
+            mok = mbar_wait(&mfull[c & 1], (c >> 1) & 1, err, kErrLoad);
+            if (mok) {
                 const uint8_t* mt = Mr + (c & 1) * 65536;
 #pragma unroll 1
                 for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    const uint64_t bh_ = sdesc_sw128(smem_u32(mt + off), 16, 1024);
-                    const uint64_t bl_ = sdesc_sw128(smem_u32(mt + 32768 + off), 16, 1024);
-                    mma_ts(tmem + kScanD, tmem + kScanHi + ks * 8, bh_, id, ks > 0);
-                    mma_ts(tmem + kScanD, tmem + kScanHi + ks * 8, bl_, id, 1);
-                    mma_ts(tmem + kScanD, tmem + kScanLo + ks * 8, bh_, id, 1);
+                    const uint32_t ao = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    const uint32_t bo = (ks >> 2) * 4096 + (ks & 3) * 32;
+                    const uint64_t ah = sdesc_sw128(smem_u32(mt + ao), 16, 1024);
+                    const uint64_t al = sdesc_sw128(smem_u32(mt + 32768 + ao), 16, 1024);
+                    const uint64_t bh_ = sdesc_sw128(smem_u32(Bt + bo), 16, 1024);
+                    const uint64_t bl_ = sdesc_sw128(smem_u32(Bt + 8192 + bo), 16, 1024);
+                    mma_ss(tmem, ah, bh_, id, ks > 0);
+                    mma_ss(tmem, ah, bl_, id, 1);
+                    mma_ss(tmem, al, bh_, id, 1);
                 }
             }
             mma_commit(bar_mma);
         }
-        ok = warp_wait(bar_mma, c & 1, err, kErrMma);
-        tc_fence_after();
-        if (tid == 0 && ok && c + 2 < nc) {  // stage c & 1 is free: M of chunk c + 2
-            mbar_arrive_expect_tx(&mfull[c & 1], 65536);
-            bulk_load(Mr + (c & 1) * 65536, ws0 + (size_t)(c + 2) * Ws::kChunk + Ws::kM, 65536, &mfull[c & 1]);
-        }
-        ok = ok && warp_wait(nfull, c & 1, err, kErrLoad);
-#pragma unroll 1
-        for (int p = 0; p < 4 && ok; ++p) {
-            uint32_t r[32];
-            tmem_ld32(tmem_addr(tmem + kScanD, warp * 32, 32 * p), r);
-            tmem_ld_wait();
-            reg_fence(r);
-            float s[32];
-#pragma unroll
-            for (int x = 0; x < 32; ++x) s[x] = __uint_as_float(r[x]) + Nb[(32 * p + x) * kD + v];
-            put_state(s, p, c + 1);
-            if (c == nc - 1 && a.S_out) {
-#pragma unroll
-                for (int x = 0; x < 32; ++x) a.S_out[(size_t)bh * kD * kD + (size_t)(32 * p + x) * kD + v] = s[x];
+        // N_c[k'][v0 .. v0 + 31] while the product runs
+        float n[kScanV];
+        load_row(reinterpret_cast<const float*>(wsc + Ws::kN) + (size_t)kr * kD + v0, n);
+        ok = warp_wait(bar_mma, c & 1, err, kErrMma) && mok;
+        if (tid == 0) {
+            if (ok && c + 2 < nc) {  // stage c & 1 is free: M of chunk c + 2
+                mbar_arrive_expect_tx(&mfull[c & 1], 65536);
+                bulk_load(Mr + (c & 1) * 65536, ws0 + (size_t)(c + 2) * Ws::kChunk + Ws::kM, 65536, &mfull[c & 1]);
             }
+            bulk_wait_group_read<0>();  // the B tile has been copied out
         }
-        ok = __syncthreads_and(ok);  // N of chunk c consumed
+        ok = __syncthreads_and(ok);  // every exit below is taken by the whole block
         if (!ok) break;
-        if (tid == 0 && c + 1 < nc) {
-            mbar_arrive_expect_tx(nfull, 65536);
-            bulk_load(sm + ScanSmem::kN, ws0 + (size_t)(c + 1) * Ws::kChunk + Ws::kN, 65536, nfull);
+        tc_fence_after();
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tmem, warp * 32, 0), r);
+        tmem_ld_wait();
+        reg_fence(r);
+        float s[kScanV];
+#pragma unroll
+        for (int x = 0; x < kScanV; ++x) s[x] = __uint_as_float(r[x]) + n[x];
+        if (c + 1 < nc) {
+            put_block(s);
+        } else if (a.S_out) {
+            float* dst = a.S_out + (size_t)bh * kD * kD + (size_t)kr * kD + v0;
+#pragma unroll
+            for (int x = 0; x < kScanV; ++x) dst[x] = s[x];
         }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
     }
-    tmem_st_wait();
+    if (tid == 0) bulk_wait_group<0>();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 32);
     }
 }
 
@@ -793,10 +811,10 @@ __global__ void __launch_bounds__(256, 1)
                 reg_fence(rx);
                 reg_fence(ry);
                 if (hq < G) {
-#pragma unroll 4
+#pragma unroll
                     for (int x = 0; x < 32; ++x) {
                         const int t = 32 * half + x;
-                        if (t0 + t >= a.T) break;
+                        if (t0 + t >= a.T) continue;
                         const float o = ((vword >> t) & 1)
                                             ? a.scale * (__expf(Gs[t]) * __uint_as_float(rx[x]) + __uint_as_float(ry[x]))
                                             : 0.f;
@@ -824,7 +842,7 @@ bool delta_chunk_supported(const Problem& P) {
     if (!P.delta || !P.io_bf16 || P.Dk != delta::kD || P.Dv != delta::kD || P.decay_dim) return false;
     if (P.T < 1 || P.T > 0x7fffffffLL - 64) return false;
     const int64_t nc = (P.T + 63) / 64;
-    return P.B * P.Hkv * nc <= 0x7fffffffLL && P.B * P.Hkv <= 0x7fffffffLL;
+    return P.B * P.Hkv * nc <= 0x7fffffffLL && P.B * P.Hkv * delta::kScanSplit <= 0x7fffffffLL;
 }
 
 size_t delta_chunk_workspace_bytes(const Problem& P) {
@@ -870,21 +888,11 @@ cudaError_t delta_chunk_causal(const Problem& P, const void* q, const void* k, c
     const unsigned streams = (unsigned)(P.B * P.Hkv);
     const unsigned chunks = streams * (unsigned)a.nc;
     delta_prep_kernel<<<chunks, 256, PrepSmem::kBytes, st>>>(a, mk, mv);
-    delta_scan_kernel<<<streams, 128, ScanSmem::kBytes, st>>>(a);
+    delta_scan_kernel<<<streams * kScanSplit, 128, ScanSmem::kBytes, st>>>(a);
     delta_out_kernel<<<chunks, 256, OutSmem::kBytes, st>>>(a, mq, mk);
     note_launch(3);
     return cudaGetLastError();
 }
 
-namespace delta {
-cudaError_t scan(const Args& a, unsigned streams, cudaStream_t st) {
-    static std::atomic<uint64_t> cfg[kMaxDevices];
-    cudaError_t e = tile::configure(delta_scan_kernel, ScanSmem::kBytes, cfg);
-    if (e != cudaSuccess) return e;
-    delta_scan_kernel<<<streams, 128, ScanSmem::kBytes, st>>>(a);
-    note_launch();
-    return cudaGetLastError();
-}
-}  // namespace delta
 
 }  // namespace la

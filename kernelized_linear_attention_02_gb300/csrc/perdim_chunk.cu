@@ -19,10 +19,12 @@
 //
 // Three kernels, in stream order: prep (one CTA per chunk: Khat and
 // N = Khat^T V on the tensor cores, and the chunk's transition diag(e^{G_C})
-// as the M tile of the shared state scan), the state scan of the delta rules
-// (S_{c+1} = M_c S_c + N_c, delta_chunk.cu), and out (one CTA per chunk: the
-// outputs of every query head).  Every fp32 operand enters the tensor cores
-// as bf16 hi + lo; keys, values and queries that enter unscaled are exact.
+// as a vector), scan (S_{c+1} = diag(e^{G_C}) S_c + N_c element by element:
+// the transition is diagonal, so each state element is its own scalar
+// recurrence and the scan spreads over every element of every stream), and
+// out (one CTA per chunk: the outputs of every query head).  Every fp32
+// operand enters the tensor cores as bf16 hi + lo; keys, values and queries
+// that enter unscaled are exact.
 #include <algorithm>
 #include <atomic>
 #include <cstring>
@@ -66,7 +68,8 @@ __device__ __forceinline__ float load_g(const Args& a, int b, int hk, int t, int
 struct PrepSmem {
     static constexpr int kKh = 0;       // Khat, rows l (64), k in 2 blocks of 8 KB: hi 16 KB, lo 16 KB
     static constexpr int kV = 32768;    // V, rows l, v in 2 blocks of 8 KB
-    static constexpr int kW = 49152;    // validity word
+    static constexpr int kG = 49152;    // G fp32 [64][128]
+    static constexpr int kW = kG + 32768;  // validity word
     static constexpr int kBar = kW + 64;
     static constexpr int kBytes = kBar + 64 + 1024;
 };
@@ -108,44 +111,45 @@ __global__ void __launch_bounds__(128, 1)
         // key dimension k = tid: cumulative decay down the chunk, then
         // Khat[l][k] = k_l[k] e^{G_C[k] - G_l[k]} into the (rows l) tile
         const int k = tid;
-        float Gr[kC];
+        float* Gs = reinterpret_cast<float*>(sm + PrepSmem::kG);  // column k is this thread's
         float G = 0.f;
+#pragma unroll 1
+        for (int t16 = 0; t16 < kC; t16 += 16) {
+            float g[16];  // sixteen steps' decays in flight, then their running sum
 #pragma unroll
-        for (int t = 0; t < kC; ++t) {
-            if ((vw >> t) & 1) G += load_g(a, b, hk, t0 + t, k);
-            Gr[t] = G;
+            for (int u = 0; u < 16; ++u) g[u] = ((vw >> (t16 + u)) & 1) ? load_g(a, b, hk, t0 + t16 + u, k) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                G += g[u];
+                Gs[(t16 + u) * kD + k] = G;
+            }
         }
         const int kb = k >> 6, kc = k & 63;
-#pragma unroll 8
-        for (int t = 0; t < kC; ++t) {
-            const bool ok = (vw >> t) & 1;
-            const size_t row = ((size_t)b * a.T + t0 + t) * a.Hkv + hk;
-            const float x = ok ? __bfloat162float(kin[row * kD + k]) * __expf(G - Gr[t]) : 0.f;
-            const __nv_bfloat16 h = __float2bfloat16_rn(x);
-            const uint32_t off = kb * 8192 + swe(t, kc);
-            *reinterpret_cast<__nv_bfloat16*>(Kh + off) = h;
-            *reinterpret_cast<__nv_bfloat16*>(Kh + 16384 + off) = __float2bfloat16_rn(x - __bfloat162float(h));
-            // value v = tid, exact (zero for invalid steps)
-            const __nv_bfloat16 vv = ok ? vin[row * kD + k] : __float2bfloat16_rn(0.f);
-            *reinterpret_cast<__nv_bfloat16*>(Vt + off) = vv;
-        }
-        // the chunk's transition: M = diag(e^{G_C}), row k of the (rows k', K = k) tile
-        uint8_t* mt = wsc + Ws::kM;
-        const float gam = __expf(G);
-        const __nv_bfloat16 gh = __float2bfloat16_rn(gam);
-        const __nv_bfloat16 gl = __float2bfloat16_rn(gam - __bfloat162float(gh));
+#pragma unroll 1
+        for (int t8 = 0; t8 < kC; t8 += 8) {
+            // eight steps' key and value elements in flight, then their tiles
+            __nv_bfloat16 kk[8], vv[8];
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-            const uint32_t off = (cc >> 3) * 16384 + swc(k, cc & 7);
-            uint4 zh = make_uint4(0, 0, 0, 0), zl = make_uint4(0, 0, 0, 0);
-            if ((k >> 3) == cc) {
-                const int e = k & 7;  // element of the chunk on the diagonal
-                reinterpret_cast<__nv_bfloat16*>(&zh)[e] = gh;
-                reinterpret_cast<__nv_bfloat16*>(&zl)[e] = gl;
+            for (int u = 0; u < 8; ++u) {
+                const int t = t8 + u;
+                const size_t row = ((size_t)b * a.T + t0 + t) * a.Hkv + hk;
+                const bool ok = (vw >> t) & 1;
+                kk[u] = ok ? kin[row * kD + k] : __float2bfloat16_rn(0.f);
+                vv[u] = ok ? vin[row * kD + k] : __float2bfloat16_rn(0.f);  // value v = tid, exact
             }
-            *reinterpret_cast<uint4*>(mt + off) = zh;
-            *reinterpret_cast<uint4*>(mt + 32768 + off) = zl;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t8 + u;
+                const float x = __bfloat162float(kk[u]) * __expf(G - Gs[t * kD + k]);
+                const __nv_bfloat16 h = __float2bfloat16_rn(x);
+                const uint32_t off = kb * 8192 + swe(t, kc);
+                *reinterpret_cast<__nv_bfloat16*>(Kh + off) = h;
+                *reinterpret_cast<__nv_bfloat16*>(Kh + 16384 + off) = __float2bfloat16_rn(x - __bfloat162float(h));
+                *reinterpret_cast<__nv_bfloat16*>(Vt + off) = vv[u];
+            }
         }
+        // the chunk's transition is diagonal: gamma[k] = e^{G_C[k]}, fp32
+        reinterpret_cast<float*>(wsc + Ws::kG)[k] = __expf(G);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -182,6 +186,64 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 128);
+    }
+}
+
+// ------------------------------------------------------------------ scan
+// Thread (v, kg) of a stream carries S[8 kg .. 8 kg + 7][v] in fp32 through the
+// chunks.  Per chunk it writes the start state into the chunk's S^T tile (row
+// v, the 16-byte group of keys 8 kg .. 8 kg + 7, hi and lo), then applies
+// S <- gamma o S + N.  Loads run kScanDepth chunks ahead of the recurrence.
+constexpr int kScanThreads = 256;  // 32 values x 8 key groups
+constexpr int kScanCtas = 8;       // per stream: 4 value blocks x 2 key-group halves
+constexpr int kScanDepth = 4;
+
+__global__ void __launch_bounds__(kScanThreads) perdim_scan_kernel(const __grid_constant__ Args a) {
+    const int bh = blockIdx.x / kScanCtas, j = blockIdx.x - bh * kScanCtas;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int v = 32 * (j & 3) + lane, k0 = 8 * (8 * (j >> 2) + warp);
+    const int nc = a.nc;
+    uint8_t* ws0 = a.ws + (size_t)bh * nc * Ws::kChunk;
+    const uint32_t soff = (k0 >> 6) * 16384 + swc(v, (k0 & 63) >> 3);
+
+    float S[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) S[i] = a.S0 ? a.S0[(size_t)bh * kD * kD + (size_t)(k0 + i) * kD + v] : 0.f;
+
+    float nb[kScanDepth][8], gb[kScanDepth][8];
+    auto load = [&](int c, float (&n)[8], float (&g)[8]) {
+        const uint8_t* w = ws0 + (size_t)c * Ws::kChunk;
+        const float* nt = reinterpret_cast<const float*>(w + Ws::kN);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) n[i] = nt[(k0 + i) * kD + v];
+        const float4 g0 = *reinterpret_cast<const float4*>(w + Ws::kG + 4 * k0);
+        const float4 g1 = *reinterpret_cast<const float4*>(w + Ws::kG + 4 * k0 + 16);
+        g[0] = g0.x, g[1] = g0.y, g[2] = g0.z, g[3] = g0.w;
+        g[4] = g1.x, g[5] = g1.y, g[6] = g1.z, g[7] = g1.w;
+    };
+#pragma unroll
+    for (int i = 0; i < kScanDepth; ++i)
+        if (i < nc) load(i, nb[i], gb[i]);
+#pragma unroll 1
+    for (int c0 = 0; c0 < nc; c0 += kScanDepth) {
+#pragma unroll
+        for (int i = 0; i < kScanDepth; ++i) {
+            const int c = c0 + i;
+            if (c < nc) {
+                uint4 hi, lo;
+                split8(S, hi, lo);
+                uint8_t* st = ws0 + (size_t)c * Ws::kChunk + Ws::kS;
+                st16(st + soff, hi);
+                st16(st + 32768 + soff, lo);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) S[x] = fmaf(gb[i][x], S[x], nb[i][x]);
+                if (c + kScanDepth < nc) load(c + kScanDepth, nb[i], gb[i]);
+            }
+        }
+    }
+    if (a.S_out) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a.S_out[(size_t)bh * kD * kD + (size_t)(k0 + i) * kD + v] = S[i];
     }
 }
 
@@ -259,18 +321,25 @@ __global__ void __launch_bounds__(256, 1)
         // key dimension k: cumulative decay down the chunk into G[t][k]
         const int k = tid - 128;
         float G_ = 0.f, mn = 0.f, mx = 0.f;
-#pragma unroll 8
-        for (int t = 0; t < kC; ++t) {
-            if ((vw >> t) & 1) G_ += load_g(a, b, hk, t0 + t, k);
-            Gs[t * kD + k] = G_;
-            mn = fminf(mn, G_);
-            mx = fmaxf(mx, G_);
+#pragma unroll 1
+        for (int t8 = 0; t8 < kC; t8 += 16) {
+            float g[16];  // sixteen steps' decays in flight, then their running sum
+#pragma unroll
+            for (int u = 0; u < 16; ++u) g[u] = ((vw >> (t8 + u)) & 1) ? load_g(a, b, hk, t0 + t8 + u, k) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                G_ += g[u];
+                Gs[(t8 + u) * kD + k] = G_;
+                mn = fminf(mn, G_);
+                mx = fmaxf(mx, G_);
+            }
         }
         fac = mn > -kFactorRange && mx < kFactorRange;
     }
     fac = __syncthreads_and(fac);  // G complete; the whole chunk factors (or not)
 
     // Kbar (only when the chunk factors) and V, rows l
+#pragma unroll
     for (int e = tid; e < kC * 16; e += 256) {
         const int l = e >> 4, cc = e & 15, k0 = 8 * cc;
         const bool ok = (vw >> l) & 1;
@@ -303,6 +372,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll 1
     for (int pr = 0; pr < npairs && ok; ++pr) {
         // Qbar of query heads 2 pr and 2 pr + 1: rows (r, t), q o e^{G_t}
+#pragma unroll 4
         for (int e = tid; e < 128 * 16; e += 256) {
             const int row = e >> 4, cc = e & 15, k0 = 8 * cc, r = row >> 6, t = row & 63;
             const int hq = 2 * pr + r;
@@ -369,12 +439,12 @@ __global__ void __launch_bounds__(256, 1)
                 for (int l = 0; l < 64; ++l) s[l] = 0.f;
                 if (hq < G && ((vw >> t) & 1)) {
                     const __nv_bfloat16* qr = q + (((size_t)b * a.T + t0 + t) * a.Hq + (size_t)hk * G + hq) * kD;
-#pragma unroll 1
-                    for (int l = 0; l <= t; ++l) {
-                        if (!((vw >> l) & 1)) continue;
+#pragma unroll
+                    for (int l = 0; l < 64; ++l) {
+                        if (l > t || !((vw >> l) & 1)) continue;
                         const __nv_bfloat16* kr = kin + (((size_t)b * a.T + t0 + l) * a.Hkv + hk) * kD;
                         float acc = 0.f;
-#pragma unroll 4
+#pragma unroll 1
                         for (int k = 0; k < kD; ++k)
                             acc = fmaf(__bfloat162float(qr[k]) * __bfloat162float(kr[k]),
                                        __expf(Gs[t * kD + k] - Gs[l * kD + k]), acc);
@@ -420,10 +490,10 @@ __global__ void __launch_bounds__(256, 1)
                 reg_fence(rx);
                 reg_fence(ry);
                 if (hq < G) {
-#pragma unroll 4
+#pragma unroll
                     for (int x = 0; x < 32; ++x) {
                         const int t = 32 * half + x;
-                        if (t0 + t >= a.T) break;
+                        if (t0 + t >= a.T) continue;
                         const float o =
                             ((vw >> t) & 1) ? a.scale * (__uint_as_float(rx[x]) + __uint_as_float(ry[x])) : 0.f;
                         const size_t idx = (((size_t)b * a.T + t0 + t) * a.Hq + (size_t)hk * G + hq) * kD + v;
@@ -452,7 +522,7 @@ bool perdim_chunk_supported(const Problem& P) {
     if (!P.gated || P.delta || !P.decay_dim || !P.io_bf16 || P.Dk != perdim::kD || P.Dv != perdim::kD) return false;
     if (P.T < 1 || P.T > 0x7fffffffLL - 64) return false;
     const int64_t nc = (P.T + 63) / 64;
-    return P.B * P.Hkv * nc <= 0x7fffffffLL;
+    return P.B * P.Hkv * nc <= 0x7fffffffLL && P.B * P.Hkv * perdim::kScanCtas <= 0x7fffffffLL;
 }
 
 size_t perdim_chunk_workspace_bytes(const Problem& P) {
@@ -494,7 +564,9 @@ cudaError_t perdim_chunk_causal(const Problem& P, const void* q, const void* k, 
                                                               static_cast<const __nv_bfloat16*>(v));
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = delta::scan(a, streams, st)) != cudaSuccess) return e;
+    perdim_scan_kernel<<<streams * kScanCtas, kScanThreads, 0, st>>>(a);
+    note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     perdim_out_kernel<<<chunks, 256, OutSmem::kBytes, st>>>(a, static_cast<const __nv_bfloat16*>(q),
                                                             static_cast<const __nv_bfloat16*>(k),
                                                             static_cast<const __nv_bfloat16*>(v));
