@@ -405,11 +405,19 @@ BwdLayout bwd_layout(const Problem& P, int nseg) {
 
 }  // namespace
 
-size_t backward_workspace_bytes(const Problem& P) { return bwd_layout(P, bwd_segments(P)).total; }
+size_t backward_workspace_bytes(const Problem& P) {
+    // covers both paths: the chunk form runs unless the pointers are not 16-byte aligned
+    return std::max(bwd_layout(P, bwd_segments(P)).total, backward_chunk_workspace_bytes(P));
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 cudaError_t backward_causal(const Problem& P, const void* q, const void* k, const void* v, const float* S0,
                             const float* Z0, const void* dy, void* dq, void* dk, void* dv, float* dS0, float* dZ0,
                             void* ws, cudaStream_t st) {
+    if (backward_chunk_supported(P) && aligned16(q) && aligned16(k) && aligned16(v) && aligned16(dy) &&
+        aligned16(dq) && aligned16(dk) && aligned16(dv) && aligned16(ws))
+        return backward_chunk_causal(P, q, k, v, S0, Z0, dy, dq, dk, dv, dS0, dZ0, ws, st);
     BwdArgs a{};
     a.q = q, a.k = k, a.v = v, a.S0 = S0, a.Z0 = P.norm ? Z0 : nullptr, a.dy = dy;
     a.dq = dq, a.dk = dk, a.dv = dv, a.dS0 = dS0, a.dZ0 = P.norm ? dZ0 : nullptr;

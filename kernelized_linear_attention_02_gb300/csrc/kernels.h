@@ -74,6 +74,14 @@ cudaError_t backward_causal(const Problem& P, const void* q, const void* k, cons
                             const float* Z0, const void* dy, void* dq, void* dk, void* dv, float* dS0, float* dZ0,
                             void* ws, cudaStream_t st);
 
+// The same gradients in chunk-parallel form on the tensor cores (bwd_chunk.cu):
+// bf16 inputs, Dk == Dv in {64, 128}.
+bool backward_chunk_supported(const Problem& P);
+size_t backward_chunk_workspace_bytes(const Problem& P);
+cudaError_t backward_chunk_causal(const Problem& P, const void* q, const void* k, const void* v, const float* S0,
+                                  const float* Z0, const void* dy, void* dq, void* dk, void* dv, float* dS0,
+                                  float* dZ0, void* ws, cudaStream_t st);
+
 // Decode step (decode.cu).
 bool decode_supported(const Problem& P);
 cudaError_t decode_step(const Problem& P, const void* q, const void* k, const void* v,
