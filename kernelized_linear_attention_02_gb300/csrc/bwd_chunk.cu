@@ -118,21 +118,27 @@ __device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
 // 64 token rows (t0 .. t0 + 63, rows at or past nvalid zero) of one head of a
 // (B, T, H, D) bf16 tensor into a 64-row tile; kMode 0: as they are, 1: phi
 // as one bf16 part, 2: phi as hi (tile) and lo (tile + 128 D).
+// 128 threads; every load is issued before the first store.
 template <int D, int kMode>
 __device__ __forceinline__ void load_rows(uint8_t* tile, const __nv_bfloat16* src, int64_t row0, int64_t rstride,
-                                          int nvalid, int fmap, float eps, int tid, int nthr) {
-    constexpr int kCpr = D / 8;
-#pragma unroll 4
-    for (int e = tid; e < kC * kCpr; e += nthr) {
-        const int t = e / kCpr, cc = e - t * kCpr;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (t < nvalid) raw = *reinterpret_cast<const uint4*>(src + (row0 + t * rstride) * D + 8 * cc);
+                                          int nvalid, int fmap, float eps, int tid) {
+    constexpr int kCpr = D / 8, kIter = kC * kCpr / 128;
+    uint4 raw[kIter];
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int e = tid + 128 * i, t = e / kCpr, cc = e - t * kCpr;
+        raw[i] = t < nvalid ? *reinterpret_cast<const uint4*>(src + (row0 + t * rstride) * D + 8 * cc)
+                            : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int e = tid + 128 * i, t = e / kCpr, cc = e - t * kCpr;
         const uint32_t off = toff<64>(t, cc);
         if (kMode == 0) {
-            st16(tile + off, raw);
+            st16(tile + off, raw[i]);
         } else {
             float f[8];
-            unpack8(raw, f);
+            unpack8(raw[i], f);
 #pragma unroll
             for (int x = 0; x < 8; ++x) f[x] = t < nvalid ? phi_f(fmap, f[x], eps) : 0.f;
             uint4 hi, lo;
@@ -218,8 +224,8 @@ __global__ void __launch_bounds__(128, 1) bwd_kv_kernel(const __grid_constant__ 
         tmem_relinquish();
     }
     const int64_t row0 = ((int64_t)b * a.T + t0) * a.Hkv + hk;
-    load_rows<D, kSplit ? 2 : 1>(Kt, a.k, row0, a.Hkv, nvalid, a.fmap, a.eps, tid, 128);
-    load_rows<D, 0>(Vt, a.v, row0, a.Hkv, nvalid, a.fmap, a.eps, tid, 128);
+    load_rows<D, kSplit ? 2 : 1>(Kt, a.k, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
+    load_rows<D, 0>(Vt, a.v, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -276,40 +282,44 @@ __global__ void __launch_bounds__(128, 1) bwd_kv_kernel(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ scan
-// Thread (v, key group of 8) of a stream carries M[8 g .. 8 g + 7][v] (and,
+// Thread (v, key group of 4) of a stream carries M[4 g .. 4 g + 3][v] (and,
 // for g = 0, the vector element v) through the chunks: forward, the start
 // states S_c = S0 + sum_{c'<c} dS_c' and z_c; reverse, R_{c+1} = sum_{c'>c} dR_c'
 // and r_{c+1}, then dS0 = R_0 and dZ0 = r_0.  Each chunk's matrix goes to its
-// tile (rows v, k contiguous, hi and lo) and its vector to kV.
+// tile (rows v, k contiguous, hi and lo) and its vector to kV.  Loads run
+// kScanDepth chunks ahead of the additions.
 constexpr int kScanThreads = 256;
-constexpr int kScanDepth = 4;
+constexpr int kScanRows = 4;
+constexpr int kScanDepth = 8;
 template <int D>
-constexpr int scan_ctas() { return D * D / 8 / kScanThreads; }
+constexpr int scan_ctas() { return D * D / kScanRows / kScanThreads; }
 
 template <int D, bool kRev>
 __global__ void __launch_bounds__(kScanThreads) bwd_scan_kernel(const __grid_constant__ BArgs a) {
     using L = Lay<D>;
     constexpr int kCtas = scan_ctas<D>();
+    constexpr int R = kScanRows;
     const int bh = blockIdx.x / kCtas;
     const int g = (blockIdx.x - bh * kCtas) * kScanThreads + threadIdx.x;
-    const int v = g % D, k0 = 8 * (g / D);
+    const int v = g % D, k0 = R * (g / D);
     const bool vec = a.norm && g < D;  // also carries vector element v
     const int nc = a.nc;
     uint8_t* ws0 = a.ws + (size_t)bh * nc * L::kChunk;
-    const uint32_t soff = (k0 >> 6) * (D * 128) + swc(v, (k0 & 63) >> 3);
+    // 8-byte half of the 16-byte chunk that holds keys k0 .. k0 + 3 of row v
+    const uint32_t soff = (k0 >> 6) * (D * 128) + swc(v, (k0 & 63) >> 3) + ((k0 & 4) ? 8 : 0);
 
-    float m[8], mv = 0.f;
+    float m[R], mv = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = (!kRev && a.S0) ? a.S0[(size_t)bh * D * D + (size_t)(k0 + i) * D + v] : 0.f;
+    for (int i = 0; i < R; ++i) m[i] = (!kRev && a.S0) ? a.S0[(size_t)bh * D * D + (size_t)(k0 + i) * D + v] : 0.f;
     if (!kRev && vec && a.Z0) mv = a.Z0[(size_t)bh * D + v];
 
-    float nb[kScanDepth][8], nv[kScanDepth];
+    float nb[kScanDepth][R], nv[kScanDepth];
     auto chunk_of = [&](int i) { return kRev ? nc - 1 - i : i; };
-    auto load = [&](int i, float (&n)[8], float& x) {
+    auto load = [&](int i, float (&n)[R], float& x) {
         const uint8_t* w = ws0 + (size_t)chunk_of(i) * L::kChunk;
         const float* d = reinterpret_cast<const float*>(w + L::kDS);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) n[q] = d[(k0 + q) * D + v];
+        for (int q = 0; q < R; ++q) n[q] = d[(k0 + q) * D + v];
         x = vec ? reinterpret_cast<const float*>(w + L::kDZ)[v] : 0.f;
     };
 #pragma unroll
@@ -322,13 +332,14 @@ __global__ void __launch_bounds__(kScanThreads) bwd_scan_kernel(const __grid_con
             const int i = i0 + j;
             if (i < nc) {
                 uint8_t* w = ws0 + (size_t)chunk_of(i) * L::kChunk;
-                uint4 hi, lo;
-                split8(m, hi, lo);
-                st16(w + L::kT + soff, hi);
-                st16(w + L::kT + 2 * D * D + soff, lo);
+                uint32_t hi[R / 2], lo[R / 2];
+#pragma unroll
+                for (int x = 0; x < R / 2; ++x) split2(m[2 * x], m[2 * x + 1], hi[x], lo[x]);
+                *reinterpret_cast<uint2*>(w + L::kT + soff) = make_uint2(hi[0], hi[1]);
+                *reinterpret_cast<uint2*>(w + L::kT + 2 * D * D + soff) = make_uint2(lo[0], lo[1]);
                 if (vec) reinterpret_cast<float*>(w + L::kV)[v] = mv;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) m[q] += nb[j][q];
+                for (int q = 0; q < R; ++q) m[q] += nb[j][q];
                 mv += nv[j];
                 if (i + kScanDepth < nc) load(i + kScanDepth, nb[j], nv[j]);
             }
@@ -337,7 +348,7 @@ __global__ void __launch_bounds__(kScanThreads) bwd_scan_kernel(const __grid_con
     if (kRev) {
         if (a.dS0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a.dS0[(size_t)bh * D * D + (size_t)(k0 + i) * D + v] = m[i];
+            for (int i = 0; i < R; ++i) a.dS0[(size_t)bh * D * D + (size_t)(k0 + i) * D + v] = m[i];
         }
         if (vec && a.dZ0) a.dZ0[(size_t)bh * D + v] = mv;
     }
@@ -410,8 +421,8 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
         tmem_relinquish();
     }
     const int64_t krow0 = ((int64_t)b * a.T + t0) * a.Hkv + hk;
-    load_rows<D, kSplit ? 2 : 1>(Kt, a.k, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid, 128);
-    load_rows<D, 0>(Vt, a.v, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid, 128);
+    load_rows<D, kSplit ? 2 : 1>(Kt, a.k, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
+    load_rows<D, 0>(Vt, a.v, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
     if (tid < D) {
         const float z = norm ? reinterpret_cast<const float*>(wsc + L::kV)[tid] : 0.f;
         const __nv_bfloat16 h = __float2bfloat16_rn(z);
@@ -461,8 +472,8 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
     for (int r = 0; r < G && ok; ++r) {
         const int hq = hk * G + r;
         const int64_t qrow0 = ((int64_t)b * a.T + t0) * a.Hq + hq;
-        load_rows<D, kSplit ? 2 : 1>(Qt, a.q, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid, 128);
-        load_rows<D, 0>(Yt, a.dy, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid, 128);
+        load_rows<D, kSplit ? 2 : 1>(Qt, a.q, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid);
+        load_rows<D, 0>(Yt, a.dy, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid);
 
         // (a) P = a kt^T and a . z_c
         ok = mma_round([&] {
@@ -666,11 +677,14 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
                 tmem_ld_wait();
                 reg_fence(rd);
                 if (tv) {
+                    uint4 qraw[4];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) qraw[q4] = *reinterpret_cast<const uint4*>(qr + 32 * c32 + 8 * q4);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         const int k0 = 32 * c32 + 8 * q4;
                         float qx[8], o[8];
-                        unpack8(*reinterpret_cast<const uint4*>(qr + k0), qx);
+                        unpack8(qraw[q4], qx);
 #pragma unroll
                         for (int x = 0; x < 8; ++x)
                             o[x] = (__uint_as_float(rd[8 * q4 + x]) + (norm ? dd * zc[k0 + x] : 0.f)) *
@@ -788,8 +802,8 @@ __global__ void __launch_bounds__(128, 1) bwd_kvgrad_kernel(const __grid_constan
         tmem_relinquish();
     }
     const int64_t row0 = ((int64_t)b * a.T + t0) * a.Hkv + hk;
-    load_rows<D, kSplit ? 2 : 1>(Kt, a.k, row0, a.Hkv, nvalid, a.fmap, a.eps, tid, 128);
-    load_rows<D, 0>(Vt, a.v, row0, a.Hkv, nvalid, a.fmap, a.eps, tid, 128);
+    load_rows<D, kSplit ? 2 : 1>(Kt, a.k, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
+    load_rows<D, 0>(Vt, a.v, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
     if (tid < D) rv[tid] = a.norm ? reinterpret_cast<const float*>(wsc + L::kV)[tid] : 0.f;
     bool ok = warp_wait(bar_ld, 0, a.err, kErrLoad);
     fence_proxy_async();
@@ -832,14 +846,24 @@ __global__ void __launch_bounds__(128, 1) bwd_kvgrad_kernel(const __grid_constan
             reg_fence(xv);
             if (row >= 0) {
                 const float rr = rv[row];
+                // every load of the 32 steps first, then the stores
+                float fk[32], fpk[32], fpv[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    const int j = 32 * h + x;
+                    const bool jv = j < nvalid;
+                    fk[x] = jv ? __bfloat162float(a.k[(row0 + (int64_t)j * a.Hkv) * D + row]) : 0.f;
+                    fpk[x] = jv ? pk[j * D + row] : 0.f;
+                    fpv[x] = jv ? pv[j * D + row] : 0.f;
+                }
 #pragma unroll
                 for (int x = 0; x < 32; ++x) {
                     const int j = 32 * h + x;
                     if (j < nvalid) {
                         const int64_t idx = (row0 + (int64_t)j * a.Hkv) * D + row;
-                        const float dkt = __uint_as_float(xk[x]) + pk[j * D + row] + rr;
-                        const float gk = dkt * dphi_f(a.fmap, __bfloat162float(a.k[idx]));
-                        const float gv = __uint_as_float(xv[x]) + pv[j * D + row];
+                        const float dkt = __uint_as_float(xk[x]) + fpk[x] + rr;
+                        const float gk = dkt * dphi_f(a.fmap, fk[x]);
+                        const float gv = __uint_as_float(xv[x]) + fpv[x];
                         if (a.out_bf16) {
                             static_cast<__nv_bfloat16*>(a.dk)[idx] = __float2bfloat16_rn(gk);
                             static_cast<__nv_bfloat16*>(a.dv)[idx] = __float2bfloat16_rn(gv);
