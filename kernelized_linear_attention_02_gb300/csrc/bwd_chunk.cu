@@ -109,6 +109,12 @@ __device__ __forceinline__ float dphi_f(int fmap, float x) {
     if (fmap == LA_FMAP_RELU_EPS) return x > 0.f ? 1.f : 0.f;
     return 1.f;
 }
+// phi' with the fast exponential (about 2 ulp), for the tensor-core path's bar
+__device__ __forceinline__ float dphi_fast(int fmap, float x) {
+    if (fmap == LA_FMAP_ELU_PLUS_ONE) return x > 0.f ? 1.f : __expf(x);
+    if (fmap == LA_FMAP_RELU_EPS) return x > 0.f ? 1.f : 0.f;
+    return 1.f;
+}
 __device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
     const __nv_bfloat16* p = reinterpret_cast<const __nv_bfloat16*>(&raw);
 #pragma unroll
@@ -118,21 +124,23 @@ __device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
 // 64 token rows (t0 .. t0 + 63, rows at or past nvalid zero) of one head of a
 // (B, T, H, D) bf16 tensor into a 64-row tile; kMode 0: as they are, 1: phi
 // as one bf16 part, 2: phi as hi (tile) and lo (tile + 128 D).
-// 128 threads; every load is issued before the first store.
-template <int D, int kMode>
+// kNT threads; every load is issued before the first store.  With az, each
+// row's phi (as the tile holds it) . z is added into az[row] (shared atomics).
+template <int D, int kMode, int kNT = 128>
 __device__ __forceinline__ void load_rows(uint8_t* tile, const __nv_bfloat16* src, int64_t row0, int64_t rstride,
-                                          int nvalid, int fmap, float eps, int tid) {
-    constexpr int kCpr = D / 8, kIter = kC * kCpr / 128;
+                                          int nvalid, int fmap, float eps, int tid, float* az = nullptr,
+                                          const float* zc = nullptr) {
+    constexpr int kCpr = D / 8, kIter = kC * kCpr / kNT;
     uint4 raw[kIter];
 #pragma unroll
     for (int i = 0; i < kIter; ++i) {
-        const int e = tid + 128 * i, t = e / kCpr, cc = e - t * kCpr;
+        const int e = tid + kNT * i, t = e / kCpr, cc = e - t * kCpr;
         raw[i] = t < nvalid ? *reinterpret_cast<const uint4*>(src + (row0 + t * rstride) * D + 8 * cc)
                             : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < kIter; ++i) {
-        const int e = tid + 128 * i, t = e / kCpr, cc = e - t * kCpr;
+        const int e = tid + kNT * i, t = e / kCpr, cc = e - t * kCpr;
         const uint32_t off = toff<64>(t, cc);
         if (kMode == 0) {
             st16(tile + off, raw[i]);
@@ -145,6 +153,15 @@ __device__ __forceinline__ void load_rows(uint8_t* tile, const __nv_bfloat16* sr
             split8(f, hi, lo);
             st16(tile + off, hi);
             if (kMode == 2) st16(tile + kC * D * 2 + off, lo);
+            if (az && t < nvalid) {
+                const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&hi);
+                const __nv_bfloat16* l = reinterpret_cast<const __nv_bfloat16*>(&lo);
+                float d = 0.f;
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    d = fmaf(__bfloat162float(h[x]) + (kMode == 2 ? __bfloat162float(l[x]) : 0.f), zc[8 * cc + x], d);
+                atomicAdd(az + t, d);
+            }
         }
     }
 }
@@ -360,26 +377,27 @@ struct MidSmem {
     static constexpr int kTok = kC * D * 2;       // one bf16 part of a 64-row tile of D columns
     static constexpr int kPart = kC * kC * 2;     // one bf16 part of the 64 x 64 weights
     static constexpr int kK = 0;                  // phi(k): rows j; hi, lo
-    static constexpr int kZ = kK + 2 * kTok;      // z_c: rows 0 (hi), 1 (lo), 2-15 zero; K = k
-    static constexpr int kV = kZ + 16 * D * 2;    // v: rows j
+    static constexpr int kV = kK + 2 * kTok;      // v: rows j
     static constexpr int kS = kV + kTok;          // S_c: rows v, k contiguous; hi, lo
     static constexpr int kQ = kS + 4 * D * D;     // phi(q) of the head: rows t; hi, lo
     static constexpr int kY = kQ + 2 * kTok;      // dy of the head: rows t
     static constexpr int kP = kY + kTok;          // P, then Pd: rows t, j contiguous; hi, mid, lo
     static constexpr int kDs = kP + 3 * kPart;    // ds: rows t, v contiguous; hi, mid
-    static constexpr int kF = kDs + 2 * kTok;     // fp32: z_c [D], den [64], dd [64]
-    static constexpr int kBar = kF + 4 * (D + 128);
+    static constexpr int kF = kDs + 2 * kTok;     // fp32: z_c [D], den [64], dd [64], phi(q) . z_c [64]
+    static constexpr int kBar = kF + 4 * (D + 192);
     static constexpr int kBytes = kBar + 64 + 1024;
 };
-// TMEM columns: token-row products (a)-(d) share kTokAcc; dR, the intra d v^T
-// and the intra d kt^T accumulate over the query heads
+// TMEM columns: token-row products (a)-(d) share kTokAcc (D columns); dR,
+// the intra d v^T and the intra d kt^T accumulate over the query heads.  256
+// columns at D = 64, so two CTAs share an SM.
 template <int D>
 struct MidTmem {
-    static constexpr uint32_t kTokAcc = 0, kR = 128, kF = 128 + D, kG = 192 + D;
+    static constexpr uint32_t kTokAcc = 0, kR = D, kF = 2 * D, kG = 2 * D + 64;
+    static constexpr uint32_t kCols = D == 64 ? 256 : 512;
 };
 
 template <int D, bool kSplit>
-__global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__ BArgs a) {
+__global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __grid_constant__ BArgs a) {
     using L = Lay<D>;
     using S = MidSmem<D>;
     using TM = MidTmem<D>;
@@ -387,7 +405,6 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* Kt = sm + S::kK;
-    uint8_t* Zt = sm + S::kZ;
     uint8_t* Vt = sm + S::kV;
     uint8_t* St = sm + S::kS;
     uint8_t* Qt = sm + S::kQ;
@@ -397,6 +414,7 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
     float* zc = reinterpret_cast<float*>(sm + S::kF);
     float* den_s = zc + D;
     float* dd_s = den_s + 64;
+    float* az = dd_s + 64;
     uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + S::kBar);
     uint64_t* bar_mma = bar_ld + 1;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_ld + 2);
@@ -417,22 +435,16 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
         bulk_load(St, wsc + L::kT, 4 * D * D, bar_ld);
     }
     if (warp == 0) {
-        tmem_alloc(tslot, 512);
+        tmem_alloc(tslot, TM::kCols);
         tmem_relinquish();
     }
     const int64_t krow0 = ((int64_t)b * a.T + t0) * a.Hkv + hk;
     load_rows<D, kSplit ? 2 : 1>(Kt, a.k, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
     load_rows<D, 0>(Vt, a.v, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
     if (tid < D) {
-        const float z = norm ? reinterpret_cast<const float*>(wsc + L::kV)[tid] : 0.f;
-        const __nv_bfloat16 h = __float2bfloat16_rn(z);
-        const __nv_bfloat16 l = __float2bfloat16_rn(z - __bfloat162float(h));
-        zc[tid] = __bfloat162float(h) + __bfloat162float(l);  // z_c as the products see it
-        *reinterpret_cast<__nv_bfloat16*>(Zt + toff_e<16>(0, tid)) = h;
-        *reinterpret_cast<__nv_bfloat16*>(Zt + toff_e<16>(1, tid)) = l;
-#pragma unroll
-        for (int r = 2; r < 16; ++r) *reinterpret_cast<__nv_bfloat16*>(Zt + toff_e<16>(r, tid)) = __float2bfloat16_rn(0.f);
+        zc[tid] = norm ? reinterpret_cast<const float*>(wsc + L::kV)[tid] : 0.f;
     }
+    if (tid < 64) az[tid] = 0.f;
     bool ok = warp_wait(bar_ld, 0, err, kErrLoad);
     tc_fence_before();
     ok = __syncthreads_and(ok);
@@ -441,7 +453,6 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
     const uint32_t tTok = tmem + TM::kTokAcc;
 
     constexpr uint32_t idA = idesc_bf16(64, 64, false, false);  // P = a kt^T
-    constexpr uint32_t idZ = idesc_bf16(64, 16, false, false);  // a z_c (z rows)
     constexpr uint32_t idQS = idesc_bf16(64, D, false, false);  // a S_c: B = S^T rows v, K = k
     constexpr uint32_t idPV = idesc_bf16(64, D, false, true);   // P v: B = v MN-major
     constexpr uint32_t idDV = idesc_bf16(64, 64, false, false); // ds v^T: B = v rows j, K = v
@@ -472,7 +483,7 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
     for (int r = 0; r < G && ok; ++r) {
         const int hq = hk * G + r;
         const int64_t qrow0 = ((int64_t)b * a.T + t0) * a.Hq + hq;
-        load_rows<D, kSplit ? 2 : 1>(Qt, a.q, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid);
+        load_rows<D, kSplit ? 2 : 1>(Qt, a.q, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid, norm ? az : nullptr, zc);
         load_rows<D, 0>(Yt, a.dy, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid);
 
         // (a) P = a kt^T and a . z_c
@@ -487,22 +498,16 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
                     mma_ss(tTok, ql, kh, idA, 1);
                     mma_ss(tTok, ql, kl, idA, 1);
                 }
-                if (norm) {
-                    mma_ss(tTok + 64, qh, kdesc<16>(Zt, ks), idZ, ks > 0);
-                    if (kSplit) mma_ss(tTok + 64, kdesc<64>(Qt + kTok, ks), kdesc<16>(Zt, ks), idZ, 1);
-                }
             }
         });
         if (!ok) break;
         {
-            uint32_t r0[32], r1[32], rz[16];
+            uint32_t r0[32], r1[32];
             tmem_ld32(tmem_addr(tTok, 32 * warp, 0), r0);
             tmem_ld32(tmem_addr(tTok, 32 * warp, 32), r1);
-            if (norm) tmem_ld16(tmem_addr(tTok + 64, 32 * warp, 0), rz);
             tmem_ld_wait();
             reg_fence(r0);
             reg_fence(r1);
-            reg_fence(rz);
             if (has_row) {
                 const bool tv = trow < nvalid;
                 float rs = 0.f;
@@ -523,7 +528,8 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
                 }
                 // the row sum of the weights exactly as the product P v sees them, so
                 // that y = num / den is the weighted mean the gradient's sums assume
-                den_s[trow] = norm ? rs + __uint_as_float(rz[0]) + __uint_as_float(rz[1]) + a.eps : 1.f;
+                den_s[trow] = norm ? rs + az[trow] + a.eps : 1.f;
+                az[trow] = 0.f;  // for the next head (its loader runs after three barriers)
             }
         }
         // (b) num = a S_c + P v
@@ -552,6 +558,7 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
             // ds = scale dy / den in three bf16 parts (hi and mid in Dt, lo over
             // dy's own row of Yt once it is read), dd = -scale (dy . num) / den^2
             const float den = has_row ? den_s[trow] : 1.f;
+            const float sden = a.scale / den;
             const bool tv = has_row && trow < nvalid;
             float dot = 0.f;
 #pragma unroll 1
@@ -569,7 +576,7 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
 #pragma unroll
                         for (int x = 0; x < 8; ++x) {
                             dot = fmaf(dyv[x], __uint_as_float(rn[8 * q4 + x]), dot);
-                            dsv[x] = tv ? a.scale * dyv[x] / den : 0.f;
+                            dsv[x] = tv ? sden * dyv[x] : 0.f;
                         }
                         uint4 hi, mid, lo;
                         split8x3(dsv, hi, mid, lo);
@@ -756,7 +763,7 @@ __global__ void __launch_bounds__(128, 1) bwd_mid_kernel(const __grid_constant__
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, TM::kCols);
     }
 }
 
@@ -772,7 +779,7 @@ struct KgSmem {
 };
 
 template <int D, bool kSplit>
-__global__ void __launch_bounds__(128, 1) bwd_kvgrad_kernel(const __grid_constant__ BArgs a) {
+__global__ void __launch_bounds__(256, 1) bwd_kvgrad_kernel(const __grid_constant__ BArgs a) {
     using L = Lay<D>;
     using S = KgSmem<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -798,12 +805,12 @@ __global__ void __launch_bounds__(128, 1) bwd_kvgrad_kernel(const __grid_constan
         bulk_load(Rt, wsc + L::kT, 4 * D * D, bar_ld);
     }
     if (warp == 0) {
-        tmem_alloc(tslot, 128);
+        tmem_alloc(tslot, 2 * D);
         tmem_relinquish();
     }
     const int64_t row0 = ((int64_t)b * a.T + t0) * a.Hkv + hk;
-    load_rows<D, kSplit ? 2 : 1>(Kt, a.k, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
-    load_rows<D, 0>(Vt, a.v, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
+    load_rows<D, kSplit ? 2 : 1, 256>(Kt, a.k, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
+    load_rows<D, 0, 256>(Vt, a.v, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
     if (tid < D) rv[tid] = a.norm ? reinterpret_cast<const float*>(wsc + L::kV)[tid] : 0.f;
     bool ok = warp_wait(bar_ld, 0, a.err, kErrLoad);
     fence_proxy_async();
@@ -813,19 +820,20 @@ __global__ void __launch_bounds__(128, 1) bwd_kvgrad_kernel(const __grid_constan
     const uint32_t tmem = *tslot;
     if (ok) {
         if (tid == 0) {
-            // X_k = R v^T (rows k): A = R (M = k, K = v) MN-major, B = v (N = j, K = v)
-            // X_v = R^T kt^T (rows v): A = R^T (M = v, K = k) K-major, B = kt (N = j, K = k)
-            constexpr uint32_t idK = idesc_bf16(D, 64, true, false);
-            constexpr uint32_t idV = idesc_bf16(D, 64, false, false);
+            // token-row products (rows j, M = 64):
+            //   d kt = v R^T:  A = v (rows j, K = v), B = R as (N = k, K = v): MN-major
+            //   d v  = kt R:   A = kt (rows j, K = k), B = R^T as (N = v, K = k): K-major
+            constexpr uint32_t idK = idesc_bf16(64, D, false, true);
+            constexpr uint32_t idV = idesc_bf16(64, D, false, false);
 #pragma unroll 1
             for (int ks = 0; ks < D / 16; ++ks) {
-                const uint64_t bv = kdesc<64>(Vt, ks);
-                mma_ss(tmem, mdesc<D>(Rt, ks), bv, idK, ks > 0);
-                mma_ss(tmem, mdesc<D>(Rt + 2 * D * D, ks), bv, idK, 1);
+                const uint64_t av = kdesc<64>(Vt, ks);
+                mma_ss(tmem, av, mdesc<D>(Rt, ks), idK, ks > 0);
+                mma_ss(tmem, av, mdesc<D>(Rt + 2 * D * D, ks), idK, 1);
                 const uint64_t kh = kdesc<64>(Kt, ks), rh = kdesc<D>(Rt, ks);
-                mma_ss(tmem + 64, rh, kh, idV, ks > 0);
-                mma_ss(tmem + 64, kdesc<D>(Rt + 2 * D * D, ks), kh, idV, 1);
-                if (kSplit) mma_ss(tmem + 64, rh, kdesc<64>(Kt + kC * D * 2, ks), idV, 1);
+                mma_ss(tmem + D, kh, rh, idV, ks > 0);
+                mma_ss(tmem + D, kh, kdesc<D>(Rt + 2 * D * D, ks), idV, 1);
+                if (kSplit) mma_ss(tmem + D, kdesc<64>(Kt + kC * D * 2, ks), rh, idV, 1);
             }
             mma_commit(bar_mma);
         }
@@ -833,45 +841,43 @@ __global__ void __launch_bounds__(128, 1) bwd_kvgrad_kernel(const __grid_constan
         tc_fence_after();
     }
     if (ok) {
-        const int row = acc_row<D>(warp, lane);  // key k of d kt and value v of d v
-        const float* pk = reinterpret_cast<const float*>(wsc + L::kPK);
-        const float* pv = reinterpret_cast<const float*>(wsc + L::kPV);
+        // warps 0-3: row j of d kt (+ its intra part + r) o phi'(k) -> dk;
+        // warps 4-7: row j of d v (+ its intra part) -> dv.  16-byte accesses.
+        const bool vside = warp >= 4;
+        const int quarter = warp & 3, j = 16 * quarter + (lane & 15);
+        const bool jv = lane < 16 && j < nvalid;
+        const float* part = reinterpret_cast<const float*>(wsc + (vside ? L::kPV : L::kPK)) + j * D;
+        const int64_t grow = (row0 + (int64_t)(jv ? j : 0) * a.Hkv) * D;
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-            uint32_t xk[32], xv[32];
-            tmem_ld32(tmem_addr(tmem, 32 * warp, 32 * h), xk);
-            tmem_ld32(tmem_addr(tmem + 64, 32 * warp, 32 * h), xv);
+        for (int c32 = 0; c32 < D / 32; ++c32) {
+            uint32_t x[32];
+            tmem_ld32(tmem_addr(tmem + (vside ? D : 0), 32 * quarter, 32 * c32), x);
             tmem_ld_wait();
-            reg_fence(xk);
-            reg_fence(xv);
-            if (row >= 0) {
-                const float rr = rv[row];
-                // every load of the 32 steps first, then the stores
-                float fk[32], fpk[32], fpv[32];
+            reg_fence(x);
+            if (jv) {
+                float4 pp[8];
+                uint4 kr[4];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int j = 32 * h + x;
-                    const bool jv = j < nvalid;
-                    fk[x] = jv ? __bfloat162float(a.k[(row0 + (int64_t)j * a.Hkv) * D + row]) : 0.f;
-                    fpk[x] = jv ? pk[j * D + row] : 0.f;
-                    fpv[x] = jv ? pv[j * D + row] : 0.f;
+                for (int q = 0; q < 8; ++q) pp[q] = reinterpret_cast<const float4*>(part + 32 * c32)[q];
+                if (!vside) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) kr[q] = *reinterpret_cast<const uint4*>(a.k + grow + 32 * c32 + 8 * q);
                 }
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int j = 32 * h + x;
-                    if (j < nvalid) {
-                        const int64_t idx = (row0 + (int64_t)j * a.Hkv) * D + row;
-                        const float dkt = __uint_as_float(xk[x]) + fpk[x] + rr;
-                        const float gk = dkt * dphi_f(a.fmap, fk[x]);
-                        const float gv = __uint_as_float(xv[x]) + fpv[x];
-                        if (a.out_bf16) {
-                            static_cast<__nv_bfloat16*>(a.dk)[idx] = __float2bfloat16_rn(gk);
-                            static_cast<__nv_bfloat16*>(a.dv)[idx] = __float2bfloat16_rn(gv);
-                        } else {
-                            static_cast<float*>(a.dk)[idx] = gk;
-                            static_cast<float*>(a.dv)[idx] = gv;
-                        }
+                for (int q = 0; q < 4; ++q) {
+                    float g[8], kx[8];
+                    const float* pq = reinterpret_cast<const float*>(&pp[2 * q]);
+                    if (!vside) unpack8(kr[q], kx);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        g[u] = __uint_as_float(x[8 * q + u]) + pq[u];
+                        if (!vside) g[u] = (g[u] + rv[32 * c32 + 8 * q + u]) * dphi_fast(a.fmap, kx[u]);
                     }
+                    const int64_t o = grow + 32 * c32 + 8 * q;
+                    if (a.out_bf16)
+                        store8(static_cast<__nv_bfloat16*>(vside ? a.dv : a.dk) + o, g);
+                    else
+                        store8(static_cast<float*>(vside ? a.dv : a.dk) + o, g);
                 }
             }
         }
@@ -880,7 +886,7 @@ __global__ void __launch_bounds__(128, 1) bwd_kvgrad_kernel(const __grid_constan
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 2 * D);
     }
 }
 
@@ -897,7 +903,7 @@ cudaError_t run(const BArgs& a, unsigned streams, cudaStream_t st) {
     bwd_scan_kernel<D, false><<<scan_grid, kScanThreads, 0, st>>>(a);
     bwd_mid_kernel<D, kSplit><<<chunks, 128, MidSmem<D>::kBytes, st>>>(a);
     bwd_scan_kernel<D, true><<<scan_grid, kScanThreads, 0, st>>>(a);
-    bwd_kvgrad_kernel<D, kSplit><<<chunks, 128, KgSmem<D>::kBytes, st>>>(a);
+    bwd_kvgrad_kernel<D, kSplit><<<chunks, 256, KgSmem<D>::kBytes, st>>>(a);
     note_launch(5);
     return cudaGetLastError();
 }
