@@ -662,16 +662,23 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
             constexpr uint32_t id_intra = idesc_bf16(D, 64, true, false);
             constexpr uint32_t id_state = idesc_bf16(D, D, true, true);
             const uint32_t tS = tmem + Cf::kColS, tHi = tmem + Cf::kColHi, tLo = tmem + Cf::kColLo;
+            // the issue loops of the linear rule at head size 128 run unrolled
+            // (the tensor core there waits on the issuing warp); the others keep
+            // the compact loops, whose smaller code the other roles share
+            constexpr int kUnr = (TF32 && D == 128) ? 16 : 1;
 
             // state update of chunk i: S^T += V^T . Kd (+ V^T . Kd_lo)
             auto issue_state_update = [&](int s) {
                 uint8_t* khi = GATED ? Kd(s) : Kb(s);
                 const uint32_t khi_lbo = GATED ? 8192u : (uint32_t)Cf::kKBlk;  // stride of 64-feature blocks
-#pragma unroll 1
+                const uint64_t dv0 = sdesc_sw128(smem_u32(Vb(s)), 8192, 1024);
+                const uint64_t dk0 = sdesc_sw128(smem_u32(khi), khi_lbo, 1024);
+                const uint64_t dl0 = sdesc_sw128(smem_u32(Klo(s)), 8192, 1024);
+#pragma unroll kUnr
                 for (int ks = 0; ks < kC / 16; ++ks) {
-                    const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                    mma_ss(tS, av, sdesc_sw128(smem_u32(khi + ks * 2048), khi_lbo, 1024), id_state, 1, lead);
-                    if (SPLITK) mma_ss(tS, av, sdesc_sw128(smem_u32(Klo(s) + ks * 2048), 8192, 1024), id_state, 1, lead);
+                    const uint64_t o = (uint64_t)(ks * 2048 >> 4);
+                    mma_ss(tS, dv0 + o, dk0 + o, id_state, 1, lead);
+                    if (SPLITK) mma_ss(tS, dv0 + o, dl0 + o, id_state, 1, lead);
                 }
             };
 
@@ -760,12 +767,13 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         }
                         if (MODE == kCausal) {
                             // scores, and in columns 64..71 phi(q).[Z_hi; Z_lo] from the Z rows
-#pragma unroll 1
+                            const uint64_t dq0 = sdesc_sw128(smem_u32(Qb(sq)), 16, 1024);
+                            const uint64_t dk0 = sdesc_sw128(smem_u32(Kb(s)), 16, 1024);
+#pragma unroll kUnr
                             for (int ks = 0; ks < D / 16; ++ks) {
                                 const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
                                 const uint32_t ko = (ks >> 2) * Cf::kKBlk + (ks & 3) * 32;
-                                mma_ss(tA, sdesc_sw128(smem_u32(Qb(sq) + qo), 16, 1024),
-                                       sdesc_sw128(smem_u32(Kb(s) + ko), 16, 1024), id_scores, ks > 0, lead);
+                                mma_ss(tA, dq0 + (qo >> 4), dk0 + (ko >> 4), id_scores, ks > 0, lead);
                             }
                         } else {
 #pragma unroll 1
@@ -795,11 +803,11 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     // inter: Y^T = S_prev^T . Q^T (tf32 from the fp32 state, or hi + lo)
                     const uint32_t tY = tmem + Cf::kColY + 64 * yb;
                     if (TF32) {
-#pragma unroll 1
+                        const uint64_t df0 = sdesc_sw128(smem_u32(Qf(sq)), 16, 1024);
+#pragma unroll kUnr
                         for (int ks = 0; ks < D / 8; ++ks) {
                             const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
-                            mma_ts_tf32(tY, tS + ks * 8, sdesc_sw128(smem_u32(Qf(sq) + ko), 16, 1024),
-                                        id_inter_tf32, ks > 0, lead);
+                            mma_ts_tf32(tY, tS + ks * 8, df0 + (ko >> 4), id_inter_tf32, ks > 0, lead);
                         }
                     } else {
 #pragma unroll 1
@@ -824,12 +832,14 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         if (!ok) break;
                         tc_fence_after();
                         // intra: Y^T += V^T . A^T (hi [+ lo])
-#pragma unroll 1
+                        const uint64_t dv0 = sdesc_sw128(smem_u32(Vb(s)), 8192, 1024);
+                        const uint64_t dh0 = sdesc_sw128(smem_u32(ATh(tb)), 16, 1024);
+                        const uint64_t dl0 = sdesc_sw128(smem_u32(ATl(tb)), 16, 1024);
+#pragma unroll kUnr
                         for (int ks = 0; ks < kC / 16; ++ks) {
-                            const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                            mma_ss(tY, av, sdesc_sw128(smem_u32(ATh(tb) + ks * 32), 16, 1024), id_intra, 1, lead);
-                            if (ALO)
-                                mma_ss(tY, av, sdesc_sw128(smem_u32(ATl(tb) + ks * 32), 16, 1024), id_intra, 1, lead);
+                            const uint64_t av = dv0 + (uint64_t)(ks * 2048 >> 4);
+                            mma_ss(tY, av, dh0 + (uint64_t)(ks * 32 >> 4), id_intra, 1, lead);
+                            if (ALO) mma_ss(tY, av, dl0 + (uint64_t)(ks * 32 >> 4), id_intra, 1, lead);
                         }
                     }
                     mma_commit(&y_full[yb], lead);
