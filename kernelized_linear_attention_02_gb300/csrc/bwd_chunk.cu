@@ -383,8 +383,8 @@ struct MidSmem {
     static constexpr int kY = kQ + 2 * kTok;      // dy of the head: rows t
     static constexpr int kP = kY + kTok;          // P, then Pd: rows t, j contiguous; hi, mid, lo
     static constexpr int kDs = kP + 3 * kPart;    // ds: rows t, v contiguous; hi, mid
-    static constexpr int kF = kDs + 2 * kTok;     // fp32: z_c [D], den [64], dd [64], phi(q) . z_c [64]
-    static constexpr int kBar = kF + 4 * (D + 192);
+    static constexpr int kF = kDs + 2 * kTok;     // fp32: z_c [D], den, dd, phi(q) . z_c [64 each], half sums [2][64] x 2
+    static constexpr int kBar = kF + 4 * (D + 448);
     static constexpr int kBytes = kBar + 64 + 1024;
 };
 // TMEM columns: token-row products (a)-(d) share kTokAcc (D columns); dR,
@@ -397,7 +397,7 @@ struct MidTmem {
 };
 
 template <int D, bool kSplit>
-__global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __grid_constant__ BArgs a) {
+__global__ void __launch_bounds__(256, D == 64 ? 2 : 1) bwd_mid_kernel(const __grid_constant__ BArgs a) {
     using L = Lay<D>;
     using S = MidSmem<D>;
     using TM = MidTmem<D>;
@@ -415,6 +415,8 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
     float* den_s = zc + D;
     float* dd_s = den_s + 64;
     float* az = dd_s + 64;
+    float* rsp = az + 64;      // [2][64] row sums of P over each column half
+    float* dotp = rsp + 128;   // [2][64] dy . num over each column half
     uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + S::kBar);
     uint64_t* bar_mma = bar_ld + 1;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_ld + 2);
@@ -439,8 +441,8 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
         tmem_relinquish();
     }
     const int64_t krow0 = ((int64_t)b * a.T + t0) * a.Hkv + hk;
-    load_rows<D, kSplit ? 2 : 1>(Kt, a.k, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
-    load_rows<D, 0>(Vt, a.v, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
+    load_rows<D, kSplit ? 2 : 1, 256>(Kt, a.k, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
+    load_rows<D, 0, 256>(Vt, a.v, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
     if (tid < D) {
         zc[tid] = norm ? reinterpret_cast<const float*>(wsc + L::kV)[tid] : 0.f;
     }
@@ -460,7 +462,11 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
     constexpr uint32_t idF = idesc_bf16(D, 64, true, true);     // ds^T P and a^T Pd
     constexpr uint32_t idDS = idesc_bf16(64, D, false, true);   // ds S_c^T and Pd kt: B MN-major
     uint32_t ph = 0;
-    const int trow = 16 * warp + (lane & 15);  // token row of this thread (lanes 0-15)
+    // Epilogues: warps w and w + 4 read the same TMEM lane quarter (w); warp w
+    // takes the first half of the columns, warp w + 4 the second.  Token-row
+    // products (M = 64) live in lanes 0-15 of each quarter.
+    const int quarter = warp & 3, half = warp >> 2;
+    const int trow = 16 * quarter + (lane & 15);  // token row of this thread (lanes 0-15)
     const bool has_row = lane < 16;
     float racc = 0.f;  // dr_c[tid] over the heads
 
@@ -483,8 +489,8 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
     for (int r = 0; r < G && ok; ++r) {
         const int hq = hk * G + r;
         const int64_t qrow0 = ((int64_t)b * a.T + t0) * a.Hq + hq;
-        load_rows<D, kSplit ? 2 : 1>(Qt, a.q, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid, norm ? az : nullptr, zc);
-        load_rows<D, 0>(Yt, a.dy, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid);
+        load_rows<D, kSplit ? 2 : 1, 256>(Qt, a.q, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid, norm ? az : nullptr, zc);
+        load_rows<D, 0, 256>(Yt, a.dy, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid);
 
         // (a) P = a kt^T and a . z_c
         ok = mma_round([&] {
@@ -502,34 +508,33 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
         });
         if (!ok) break;
         {
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tmem_addr(tTok, 32 * warp, 0), r0);
-            tmem_ld32(tmem_addr(tTok, 32 * warp, 32), r1);
+            // P row (this half's 32 columns) in three parts, and its row sum
+            uint32_t r0[32];
+            tmem_ld32(tmem_addr(tTok, 32 * quarter, 32 * half), r0);
             tmem_ld_wait();
             reg_fence(r0);
-            reg_fence(r1);
             if (has_row) {
                 const bool tv = trow < nvalid;
                 float rs = 0.f;
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int cc = 4 * half + c4;
                     float f8[8];
 #pragma unroll
                     for (int x = 0; x < 8; ++x) {
                         const int j = 8 * cc + x;
-                        f8[x] = (tv && j <= trow) ? __uint_as_float(j < 32 ? r0[j] : r1[j - 32]) : 0.f;
+                        f8[x] = (tv && j <= trow) ? __uint_as_float(r0[8 * c4 + x]) : 0.f;
                     }
                     uint4 hi, mid, lo;
                     split8x3(f8, hi, mid, lo);
                     st16(Pt + toff<64>(trow, cc), hi);
                     st16(Pt + kPart + toff<64>(trow, cc), mid);
                     st16(Pt + 2 * kPart + toff<64>(trow, cc), lo);
+                    // the weights exactly as the product P v sees them, so that
+                    // y = num / den is the weighted mean the gradient's sums assume
                     rs += sum_parts(hi, mid) + sum_parts(lo, make_uint4(0, 0, 0, 0));
                 }
-                // the row sum of the weights exactly as the product P v sees them, so
-                // that y = num / den is the weighted mean the gradient's sums assume
-                den_s[trow] = norm ? rs + az[trow] + a.eps : 1.f;
-                az[trow] = 0.f;  // for the next head (its loader runs after three barriers)
+                rsp[64 * half + trow] = rs;
             }
         }
         // (b) num = a S_c + P v
@@ -557,20 +562,23 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
         {
             // ds = scale dy / den in three bf16 parts (hi and mid in Dt, lo over
             // dy's own row of Yt once it is read), dd = -scale (dy . num) / den^2
-            const float den = has_row ? den_s[trow] : 1.f;
+            const float den =
+                has_row ? (norm ? rsp[trow] + rsp[64 + trow] + az[trow] + a.eps : 1.f) : 1.f;
+            if (has_row && half == 0) den_s[trow] = den;
             const float sden = a.scale / den;
             const bool tv = has_row && trow < nvalid;
             float dot = 0.f;
 #pragma unroll 1
-            for (int c32 = 0; c32 < D / 32; ++c32) {
+            for (int c32 = 0; c32 < D / 64; ++c32) {
+                const int col = (D / 2) * half + 32 * c32;
                 uint32_t rn[32];
-                tmem_ld32(tmem_addr(tTok, 32 * warp, 32 * c32), rn);
+                tmem_ld32(tmem_addr(tTok, 32 * quarter, col), rn);
                 tmem_ld_wait();
                 reg_fence(rn);
                 if (has_row) {
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
-                        const int cc = 4 * c32 + q4;
+                        const int cc = col / 8 + q4;
                         float dyv[8], dsv[8];
                         unpack8(*reinterpret_cast<const uint4*>(Yt + toff<64>(trow, cc)), dyv);
 #pragma unroll
@@ -586,7 +594,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
                     }
                 }
             }
-            if (has_row) dd_s[trow] = (tv && norm) ? -a.scale * dot / (den * den) : 0.f;
+            if (has_row) dotp[64 * half + trow] = dot;
         }
         // (c) ds v^T (all three parts of ds: Pd = ds v^T + dd cancels to
         // nearly zero where y_t is close to v_j); (e) dR += a^T ds; (f) d v^T += ds^T P
@@ -613,25 +621,29 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
         });
         if (!ok) break;
         {
-            // Pd = ds v^T + dd (j <= t)
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tmem_addr(tTok, 32 * warp, 0), r0);
-            tmem_ld32(tmem_addr(tTok, 32 * warp, 32), r1);
+            // Pd = ds v^T + dd (j <= t), dd = -scale (dy . num) / den^2
+            uint32_t r0[32];
+            tmem_ld32(tmem_addr(tTok, 32 * quarter, 32 * half), r0);
             tmem_ld_wait();
             reg_fence(r0);
-            reg_fence(r1);
             if (has_row) {
                 const bool tv = trow < nvalid;
-                const float dd = dd_s[trow];
+                const float den = den_s[trow];
+                const float dd = (tv && norm) ? -a.scale * (dotp[trow] + dotp[64 + trow]) / (den * den) : 0.f;
+                if (half == 0) {
+                    dd_s[trow] = dd;
+                    az[trow] = 0.f;  // for the next head (its loader runs after two barriers)
+                }
                 // three parts: Pd kt sums terms that cancel (a query with few active
                 // feature dimensions has d a ~ 0 along them)
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int cc = 4 * half + c4;
                     float f8[8];
 #pragma unroll
                     for (int x = 0; x < 8; ++x) {
                         const int j = 8 * cc + x;
-                        f8[x] = (tv && j <= trow) ? __uint_as_float(j < 32 ? r0[j] : r1[j - 32]) + dd : 0.f;
+                        f8[x] = (tv && j <= trow) ? __uint_as_float(r0[8 * c4 + x]) + dd : 0.f;
                     }
                     uint4 hi, mid, lo;
                     split8x3(f8, hi, mid, lo);
@@ -678,18 +690,19 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
             const float dd = has_row ? dd_s[trow] : 0.f;
             const __nv_bfloat16* qr = a.q + (qrow0 + (int64_t)(tv ? trow : 0) * a.Hq) * D;
 #pragma unroll 1
-            for (int c32 = 0; c32 < D / 32; ++c32) {
+            for (int c32 = 0; c32 < D / 64; ++c32) {
+                const int col = (D / 2) * half + 32 * c32;
                 uint32_t rd[32];
-                tmem_ld32(tmem_addr(tTok, 32 * warp, 32 * c32), rd);
+                tmem_ld32(tmem_addr(tTok, 32 * quarter, col), rd);
                 tmem_ld_wait();
                 reg_fence(rd);
                 if (tv) {
                     uint4 qraw[4];
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) qraw[q4] = *reinterpret_cast<const uint4*>(qr + 32 * c32 + 8 * q4);
+                    for (int q4 = 0; q4 < 4; ++q4) qraw[q4] = *reinterpret_cast<const uint4*>(qr + col + 8 * q4);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
-                        const int k0 = 32 * c32 + 8 * q4;
+                        const int k0 = col + 8 * q4;
                         float qx[8], o[8];
                         unpack8(qraw[q4], qx);
 #pragma unroll
@@ -723,16 +736,17 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
     }
     if (ok) {
         // dR_c -> kDS ([k][v]), dr_c -> kDZ, intra d v -> kPV ([j][v]), intra d kt -> kPK ([j][k])
-        const int row = acc_row<D>(warp, lane);
+        const int row = acc_row<D>(quarter, lane);
         float* dR = reinterpret_cast<float*>(wsc + L::kDS);
 #pragma unroll 1
-        for (int c32 = 0; c32 < D / 32; ++c32) {
+        for (int c32 = 0; c32 < D / 64; ++c32) {
+            const int col = (D / 2) * half + 32 * c32;
             uint32_t rr[32];
-            tmem_ld32(tmem_addr(tmem + TM::kR, 32 * warp, 32 * c32), rr);
+            tmem_ld32(tmem_addr(tmem + TM::kR, 32 * quarter, col), rr);
             tmem_ld_wait();
             reg_fence(rr);
             if (row >= 0) {
-                float4* dst = reinterpret_cast<float4*>(dR + (size_t)row * D + 32 * c32);
+                float4* dst = reinterpret_cast<float4*>(dR + (size_t)row * D + col);
 #pragma unroll
                 for (int x = 0; x < 8; ++x)
                     dst[x] = make_float4(__uint_as_float(rr[4 * x]), __uint_as_float(rr[4 * x + 1]),
@@ -741,11 +755,11 @@ __global__ void __launch_bounds__(128, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
         }
         float* pv = reinterpret_cast<float*>(wsc + L::kPV);
         float* pk = reinterpret_cast<float*>(wsc + L::kPK);
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
+        {
+            const int h = half;
             uint32_t rf[32], rg[32];
-            tmem_ld32(tmem_addr(tmem + TM::kF, 32 * warp, 32 * h), rf);
-            tmem_ld32(tmem_addr(tmem + TM::kG, 32 * warp, 32 * h), rg);
+            tmem_ld32(tmem_addr(tmem + TM::kF, 32 * quarter, 32 * h), rf);
+            tmem_ld32(tmem_addr(tmem + TM::kG, 32 * quarter, 32 * h), rg);
             tmem_ld_wait();
             reg_fence(rf);
             reg_fence(rg);
@@ -901,7 +915,7 @@ cudaError_t run(const BArgs& a, unsigned streams, cudaStream_t st) {
     const unsigned scan_grid = streams * (unsigned)scan_ctas<D>();
     bwd_kv_kernel<D, kSplit><<<chunks, 128, KvSmem<D, kSplit>::kBytes, st>>>(a);
     bwd_scan_kernel<D, false><<<scan_grid, kScanThreads, 0, st>>>(a);
-    bwd_mid_kernel<D, kSplit><<<chunks, 128, MidSmem<D>::kBytes, st>>>(a);
+    bwd_mid_kernel<D, kSplit><<<chunks, 256, MidSmem<D>::kBytes, st>>>(a);
     bwd_scan_kernel<D, true><<<scan_grid, kScanThreads, 0, st>>>(a);
     bwd_kvgrad_kernel<D, kSplit><<<chunks, 256, KgSmem<D>::kBytes, st>>>(a);
     note_launch(5);
