@@ -269,8 +269,12 @@ la_status la_decode_step_delta(const la_params* p, const void* q, const void* k,
  *   dq, dk, dv       outputs in out_dtype, the shapes of q, k, v.
  *   dS0, dZ0         gradients of the initial state (float32), or NULL.
  *   ws               workspace of la_backward_workspace_bytes(p) bytes.
- * Two CUDA-core passes (tokens forward for dq, backward for dk, dv), one CTA
- * per (batch, kv head) stream.  LA_ERR_UNSUPPORTED for the other rules. */
+ * bf16 inputs with key_dim == value_dim in {64, 128} and 16-byte aligned
+ * pointers run the chunk-parallel form on the tensor cores (five launches:
+ * per-chunk key/value products, a forward scan of the chunk start states, a
+ * per-chunk kernel for dq and the chunk's reverse-state increment, a reverse
+ * scan, a per-chunk kernel for dk and dv); other shapes and float32 inputs
+ * run two CUDA-core token scans.  LA_ERR_UNSUPPORTED for the other rules. */
 size_t la_backward_workspace_bytes(const la_params* p);
 la_status la_backward_causal(const la_params* p, const void* q, const void* k, const void* v, const float* S0,
                              const float* Z0, const void* dy, void* dq, void* dk, void* dv, float* dS0, float* dZ0,

@@ -299,38 +299,40 @@ __global__ void __launch_bounds__(128, 1) bwd_kv_kernel(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ scan
-// Thread (v, key group of 4) of a stream carries M[4 g .. 4 g + 3][v] (and,
-// for g = 0, the vector element v) through the chunks: forward, the start
-// states S_c = S0 + sum_{c'<c} dS_c' and z_c; reverse, R_{c+1} = sum_{c'>c} dR_c'
-// and r_{c+1}, then dS0 = R_0 and dZ0 = r_0.  Each chunk's matrix goes to its
-// tile (rows v, k contiguous, hi and lo) and its vector to kV.  Loads run
-// kScanDepth chunks ahead of the additions.
+// The chunk states as prefix sums over the chunks, element by element:
+// forward, S_c = S0 + sum_{c'<c} dS_c' and z_c; reverse, R_{c+1} =
+// sum_{c'>c} dR_c' and r_{c+1}, then dS0 = R_0 and dZ0 = r_0.  Each chunk's
+// matrix goes to its tile (rows v, k contiguous, hi and lo) and its vector to
+// kV.  A CTA owns 32 values v of one key group of 4 (and, for key group 0,
+// the vector elements v) and splits the chunks into kScanSegs segments, one
+// warp each: pass 1 sums each segment's increments (independent loads, all in
+// flight), the segments' offsets follow from those sums in shared memory,
+// and pass 2 walks each segment again writing the running state, so no thread
+// walks more than nc / kScanSegs chunks in sequence.
 constexpr int kScanThreads = 256;
 constexpr int kScanRows = 4;
-constexpr int kScanDepth = 8;
+constexpr int kScanSegs = kScanThreads / 32;
 template <int D>
-constexpr int scan_ctas() { return D * D / kScanRows / kScanThreads; }
+constexpr int scan_ctas() { return D * D / kScanRows / 32; }
 
 template <int D, bool kRev>
 __global__ void __launch_bounds__(kScanThreads) bwd_scan_kernel(const __grid_constant__ BArgs a) {
     using L = Lay<D>;
     constexpr int kCtas = scan_ctas<D>();
     constexpr int R = kScanRows;
+    __shared__ float part[kScanSegs][32][R + 1];
     const int bh = blockIdx.x / kCtas;
-    const int g = (blockIdx.x - bh * kCtas) * kScanThreads + threadIdx.x;
-    const int v = g % D, k0 = R * (g / D);
-    const bool vec = a.norm && g < D;  // also carries vector element v
+    const int e = blockIdx.x - bh * kCtas;           // element block: 32 values v x one key group
+    const int lane = threadIdx.x & 31, seg = threadIdx.x >> 5;
+    const int v = 32 * (e % (D / 32)) + lane, k0 = R * (e / (D / 32));
+    const bool vec = a.norm && k0 == 0;  // also carries vector element v
     const int nc = a.nc;
     uint8_t* ws0 = a.ws + (size_t)bh * nc * L::kChunk;
     // 8-byte half of the 16-byte chunk that holds keys k0 .. k0 + 3 of row v
     const uint32_t soff = (k0 >> 6) * (D * 128) + swc(v, (k0 & 63) >> 3) + ((k0 & 4) ? 8 : 0);
-
-    float m[R], mv = 0.f;
-#pragma unroll
-    for (int i = 0; i < R; ++i) m[i] = (!kRev && a.S0) ? a.S0[(size_t)bh * D * D + (size_t)(k0 + i) * D + v] : 0.f;
-    if (!kRev && vec && a.Z0) mv = a.Z0[(size_t)bh * D + v];
-
-    float nb[kScanDepth][R], nv[kScanDepth];
+    // this warp's segment of the walk order (reverse: chunks nc-1 .. 0)
+    const int per = (nc + kScanSegs - 1) / kScanSegs;
+    const int i0 = min(nc, seg * per), i1 = min(nc, i0 + per);
     auto chunk_of = [&](int i) { return kRev ? nc - 1 - i : i; };
     auto load = [&](int i, float (&n)[R], float& x) {
         const uint8_t* w = ws0 + (size_t)chunk_of(i) * L::kChunk;
@@ -339,16 +341,56 @@ __global__ void __launch_bounds__(kScanThreads) bwd_scan_kernel(const __grid_con
         for (int q = 0; q < R; ++q) n[q] = d[(k0 + q) * D + v];
         x = vec ? reinterpret_cast<const float*>(w + L::kDZ)[v] : 0.f;
     };
-#pragma unroll
-    for (int i = 0; i < kScanDepth; ++i)
-        if (i < nc) load(i, nb[i], nv[i]);
+
+    // pass 1: this segment's sum, eight chunks of loads at a time
+    float tot[R] = {0.f, 0.f, 0.f, 0.f}, totv = 0.f;
 #pragma unroll 1
-    for (int i0 = 0; i0 < nc; i0 += kScanDepth) {
+    for (int i = i0; i < i1; i += 8) {
+        float n8[8][R], x8[8];
 #pragma unroll
-        for (int j = 0; j < kScanDepth; ++j) {
-            const int i = i0 + j;
-            if (i < nc) {
-                uint8_t* w = ws0 + (size_t)chunk_of(i) * L::kChunk;
+        for (int u = 0; u < 8; ++u) {
+            if (i + u < i1) {
+                load(i + u, n8[u], x8[u]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < R; ++q) n8[u][q] = 0.f;
+                x8[u] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+#pragma unroll
+            for (int q = 0; q < R; ++q) tot[q] += n8[u][q];
+            totv += x8[u];
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < R; ++q) part[seg][lane][q] = tot[q];
+    part[seg][lane][R] = totv;
+    __syncthreads();
+
+    // the state entering this segment: the start value plus the earlier segments' sums
+    float m[R], mv = 0.f;
+#pragma unroll
+    for (int q = 0; q < R; ++q) m[q] = (!kRev && a.S0) ? a.S0[(size_t)bh * D * D + (size_t)(k0 + q) * D + v] : 0.f;
+    if (!kRev && vec && a.Z0) mv = a.Z0[(size_t)bh * D + v];
+    for (int sg = 0; sg < seg; ++sg) {
+#pragma unroll
+        for (int q = 0; q < R; ++q) m[q] += part[sg][lane][q];
+        mv += part[sg][lane][R];
+    }
+
+    // pass 2: the running state of every chunk of the segment
+#pragma unroll 1
+    for (int i = i0; i < i1; i += 8) {
+        float n8[8][R], x8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (i + u < i1) load(i + u, n8[u], x8[u]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (i + u < i1) {
+                uint8_t* w = ws0 + (size_t)chunk_of(i + u) * L::kChunk;
                 uint32_t hi[R / 2], lo[R / 2];
 #pragma unroll
                 for (int x = 0; x < R / 2; ++x) split2(m[2 * x], m[2 * x + 1], hi[x], lo[x]);
@@ -356,16 +398,16 @@ __global__ void __launch_bounds__(kScanThreads) bwd_scan_kernel(const __grid_con
                 *reinterpret_cast<uint2*>(w + L::kT + 2 * D * D + soff) = make_uint2(lo[0], lo[1]);
                 if (vec) reinterpret_cast<float*>(w + L::kV)[v] = mv;
 #pragma unroll
-                for (int q = 0; q < R; ++q) m[q] += nb[j][q];
-                mv += nv[j];
-                if (i + kScanDepth < nc) load(i + kScanDepth, nb[j], nv[j]);
+                for (int q = 0; q < R; ++q) m[q] += n8[u][q];
+                mv += x8[u];
             }
         }
     }
-    if (kRev) {
+    // reverse: after the last segment, the total is dS0 (and dZ0)
+    if (kRev && seg == kScanSegs - 1) {
         if (a.dS0) {
 #pragma unroll
-            for (int i = 0; i < R; ++i) a.dS0[(size_t)bh * D * D + (size_t)(k0 + i) * D + v] = m[i];
+            for (int q = 0; q < R; ++q) a.dS0[(size_t)bh * D * D + (size_t)(k0 + q) * D + v] = m[q];
         }
         if (vec && a.dZ0) a.dZ0[(size_t)bh * D + v] = mv;
     }
