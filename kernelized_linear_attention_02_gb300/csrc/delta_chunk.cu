@@ -662,6 +662,14 @@ __global__ void __launch_bounds__(256, 1)
     const float* wg = reinterpret_cast<const float*>(wsc + Ws::kG);
     if (tid < 64) Gs[tid] = wg[tid];
     const uint64_t vword = (uint64_t)__float_as_uint(wg[64]) | ((uint64_t)__float_as_uint(wg[65]) << 32);
+    // U'^T row v (warps 0-3), in flight while the loads and the first products run
+    float upre[kC];
+    if (warp < 4) {
+        const float* up = reinterpret_cast<const float*>(wsc + Ws::kU);
+        const int v = (warp & 3) * 32 + lane;
+#pragma unroll
+        for (int t = 0; t < kC; ++t) upre[t] = up[t * kD + v];
+    }
     bool ok = warp_wait(bar_ld, ld_phase++ & 1, err, kErrLoad);
     ok = __syncthreads_and(ok);
 
@@ -729,14 +737,13 @@ __global__ void __launch_bounds__(256, 1)
         tmem_ld_wait();
         reg_fence(r0);
         reg_fence(r1);
-        const float* up = reinterpret_cast<const float*>(wsc + Ws::kU);
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
             float f[8];
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
                 const int t = 8 * cc + x;
-                f[x] = up[t * kD + v] - __uint_as_float(t < 32 ? r0[t] : r1[t - 32]);
+                f[x] = upre[t] - __uint_as_float(t < 32 ? r0[t] : r1[t - 32]);
             }
             uint4 hi, lo;
             split8(f, hi, lo);
@@ -751,11 +758,10 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll 1
     for (int pr = 0; pr < npairs && ok; ++pr) {
         if (pr > 0) {
-            // next head pair: queries, then scores and P (the previous pair's
-            // products have completed: the output stage waited for them)
+            // next head pair: its queries were requested when the previous
+            // pair's products completed; then scores and P
             tc_fence_before();
             __syncthreads();
-            if (tid == 0) load_pair(pr, 0);
             ok = warp_wait(bar_ld, ld_phase++ & 1, err, kErrLoad);
             ok = __syncthreads_and(ok);
             if (!ok) break;
@@ -799,6 +805,8 @@ __global__ void __launch_bounds__(256, 1)
         ok = __syncthreads_and(ok);
         if (!ok) break;
         tc_fence_after();
+        // the products have read this pair's queries: the next pair's load overlaps the outputs
+        if (tid == 0 && pr + 1 < npairs) load_pair(pr + 1, 0);
         {
             // outputs: warps 0-3 the pair's first head, warps 4-7 its second
             const int r = warp >> 2, v = quad * 32 + lane, hq = 2 * pr + r;

@@ -370,26 +370,41 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     const int npairs = (G + 1) / 2;
 #pragma unroll 1
-    for (int pr = 0; pr < npairs && ok; ++pr) {
-        // Qbar of query heads 2 pr and 2 pr + 1: rows (r, t), q o e^{G_t}
-#pragma unroll 4
-        for (int e = tid; e < 128 * 16; e += 256) {
-            const int row = e >> 4, cc = e & 15, k0 = 8 * cc, r = row >> 6, t = row & 63;
-            const int hq = 2 * pr + r;
-            float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (hq < G && ((vw >> t) & 1)) {
-                const uint4 qq = *reinterpret_cast<const uint4*>(
-                    q + (((size_t)b * a.T + t0 + t) * a.Hq + (size_t)hk * G + hq) * kD + k0);
-                const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(&qq);
+    // Qbar of query heads 2 pr and 2 pr + 1: rows (r, t), q o e^{G_t}, built by
+    // nthr threads (the loads of four rows in flight before their stores)
+    auto build_qbar = [&](int pr, int bt, int nthr) {
+#pragma unroll 1
+        for (int e0 = bt; e0 < 128 * 16; e0 += 4 * nthr) {
+            uint4 qq[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + u * nthr, row = e >> 4, cc = e & 15, r = row >> 6, t = row & 63;
+                const int hq = 2 * pr + r;
+                qq[u] = (e < 128 * 16 && hq < G && ((vw >> t) & 1))
+                            ? *reinterpret_cast<const uint4*>(
+                                  q + (((size_t)b * a.T + t0 + t) * a.Hq + (size_t)hk * G + hq) * kD + 8 * cc)
+                            : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + u * nthr;
+                if (e >= 128 * 16) continue;
+                const int row = e >> 4, cc = e & 15, k0 = 8 * cc, t = row & 63;
+                const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(&qq[u]);
+                float f[8];
 #pragma unroll
                 for (int x = 0; x < 8; ++x) f[x] = __bfloat162float(qp[x]) * __expf(Gs[t * kD + k0 + x]);
+                uint4 hi, lo;
+                split8(f, hi, lo);
+                const uint32_t off = (cc >> 3) * 16384 + swc(row, cc & 7);
+                st16(Qb + off, hi);
+                st16(Qb + 32768 + off, lo);
             }
-            uint4 hi, lo;
-            split8(f, hi, lo);
-            const uint32_t off = (cc >> 3) * 16384 + swc(row, cc & 7);
-            st16(Qb + off, hi);
-            st16(Qb + 32768 + off, lo);
         }
+    };
+    if (npairs > 0) build_qbar(0, tid, 256);
+#pragma unroll 1
+    for (int pr = 0; pr < npairs && ok; ++pr) {
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
@@ -420,6 +435,9 @@ __global__ void __launch_bounds__(256, 1)
         ok = __syncthreads_and(ok);
         if (!ok) break;
         tc_fence_after();
+        // X and the scores have read this pair's Qbar: warps 0-3 build the next
+        // pair's while warps 4-7 build P
+        if (warp < 4 && pr + 1 < npairs) build_qbar(pr + 1, tid, 128);
         if (warp >= 4) {
             // P rows (r, t): masked scores, l <= t
             const int row = quad * 32 + lane, r = row >> 6, t = row & 63, hq = 2 * pr + r;
