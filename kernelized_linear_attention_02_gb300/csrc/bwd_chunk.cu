@@ -124,29 +124,41 @@ __device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
 // 64 token rows (t0 .. t0 + 63, rows at or past nvalid zero) of one head of a
 // (B, T, H, D) bf16 tensor into a 64-row tile; kMode 0: as they are, 1: phi
 // as one bf16 part, 2: phi as hi (tile) and lo (tile + 128 D).
-// kNT threads; every load is issued before the first store.  With az, each
-// row's phi (as the tile holds it) . z is added into az[row] (shared atomics).
-template <int D, int kMode, int kNT = 128>
-__device__ __forceinline__ void load_rows(uint8_t* tile, const __nv_bfloat16* src, int64_t row0, int64_t rstride,
-                                          int nvalid, int fmap, float eps, int tid, float* az = nullptr,
-                                          const float* zc = nullptr) {
-    constexpr int kCpr = D / 8, kIter = kC * kCpr / kNT;
+// The 64 token rows (t0 .. t0 + 63, rows at or past nvalid zero) of one head
+// of a (B, T, H, D) bf16 tensor, by kNT threads: fetch_rows issues the loads,
+// store_rows writes the tile (kMode 0: as they are, 1: phi as one bf16 part,
+// 2: phi as hi (tile) and lo (tile + 128 D)); with az, each row's phi (as the
+// tile holds it) . z is added into az[row] (shared atomics).  Several
+// fetches can be in flight before their stores.
+template <int D, int kNT>
+struct Rows {
+    static constexpr int kCpr = D / 8, kIter = kC * kCpr / kNT;
     uint4 raw[kIter];
+};
+template <int D, int kNT>
+__device__ __forceinline__ void fetch_rows(Rows<D, kNT>& r, const __nv_bfloat16* src, int64_t row0, int64_t rstride,
+                                           int nvalid, int tid) {
+    constexpr int kCpr = Rows<D, kNT>::kCpr;
 #pragma unroll
-    for (int i = 0; i < kIter; ++i) {
+    for (int i = 0; i < Rows<D, kNT>::kIter; ++i) {
         const int e = tid + kNT * i, t = e / kCpr, cc = e - t * kCpr;
-        raw[i] = t < nvalid ? *reinterpret_cast<const uint4*>(src + (row0 + t * rstride) * D + 8 * cc)
-                            : make_uint4(0, 0, 0, 0);
+        r.raw[i] = t < nvalid ? *reinterpret_cast<const uint4*>(src + (row0 + t * rstride) * D + 8 * cc)
+                              : make_uint4(0, 0, 0, 0);
     }
+}
+template <int D, int kMode, int kNT>
+__device__ __forceinline__ void store_rows(uint8_t* tile, const Rows<D, kNT>& r, int nvalid, int fmap, float eps,
+                                           int tid, float* az = nullptr, const float* zc = nullptr) {
+    constexpr int kCpr = Rows<D, kNT>::kCpr;
 #pragma unroll
-    for (int i = 0; i < kIter; ++i) {
+    for (int i = 0; i < Rows<D, kNT>::kIter; ++i) {
         const int e = tid + kNT * i, t = e / kCpr, cc = e - t * kCpr;
         const uint32_t off = toff<64>(t, cc);
         if (kMode == 0) {
-            st16(tile + off, raw[i]);
+            st16(tile + off, r.raw[i]);
         } else {
             float f[8];
-            unpack8(raw[i], f);
+            unpack8(r.raw[i], f);
 #pragma unroll
             for (int x = 0; x < 8; ++x) f[x] = t < nvalid ? phi_f(fmap, f[x], eps) : 0.f;
             uint4 hi, lo;
@@ -164,6 +176,14 @@ __device__ __forceinline__ void load_rows(uint8_t* tile, const __nv_bfloat16* sr
             }
         }
     }
+}
+template <int D, int kMode, int kNT = 128>
+__device__ __forceinline__ void load_rows(uint8_t* tile, const __nv_bfloat16* src, int64_t row0, int64_t rstride,
+                                          int nvalid, int fmap, float eps, int tid, float* az = nullptr,
+                                          const float* zc = nullptr) {
+    Rows<D, kNT> r;
+    fetch_rows<D, kNT>(r, src, row0, rstride, nvalid, tid);
+    store_rows<D, kMode, kNT>(tile, r, nvalid, fmap, eps, tid, az, zc);
 }
 
 // x = hi + mid + lo in three bf16 parts (about 24 significant bits), for 8 values
@@ -241,8 +261,13 @@ __global__ void __launch_bounds__(128, 1) bwd_kv_kernel(const __grid_constant__ 
         tmem_relinquish();
     }
     const int64_t row0 = ((int64_t)b * a.T + t0) * a.Hkv + hk;
-    load_rows<D, kSplit ? 2 : 1>(Kt, a.k, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
-    load_rows<D, 0>(Vt, a.v, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
+    {
+        Rows<D, 128> rk, rv;  // both tiles' loads in flight at once
+        fetch_rows<D, 128>(rk, a.k, row0, a.Hkv, nvalid, tid);
+        fetch_rows<D, 128>(rv, a.v, row0, a.Hkv, nvalid, tid);
+        store_rows<D, kSplit ? 2 : 1, 128>(Kt, rk, nvalid, a.fmap, a.eps, tid);
+        store_rows<D, 0, 128>(Vt, rv, nvalid, a.fmap, a.eps, tid);
+    }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -483,12 +508,22 @@ __global__ void __launch_bounds__(256, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
         tmem_relinquish();
     }
     const int64_t krow0 = ((int64_t)b * a.T + t0) * a.Hkv + hk;
-    load_rows<D, kSplit ? 2 : 1, 256>(Kt, a.k, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
-    load_rows<D, 0, 256>(Vt, a.v, krow0, a.Hkv, nvalid, a.fmap, a.eps, tid);
-    if (tid < D) {
-        zc[tid] = norm ? reinterpret_cast<const float*>(wsc + L::kV)[tid] : 0.f;
+    const int64_t qrow00 = ((int64_t)b * a.T + t0) * a.Hq + (int64_t)hk * G;  // first query head's rows
+    {
+        // keys, values and the first head's queries and dy: every load in flight at once
+        Rows<D, 256> rk, rv, rq, ry;
+        fetch_rows<D, 256>(rk, a.k, krow0, a.Hkv, nvalid, tid);
+        fetch_rows<D, 256>(rv, a.v, krow0, a.Hkv, nvalid, tid);
+        fetch_rows<D, 256>(rq, a.q, qrow00, a.Hq, nvalid, tid);
+        fetch_rows<D, 256>(ry, a.dy, qrow00, a.Hq, nvalid, tid);
+        if (tid < D) zc[tid] = norm ? reinterpret_cast<const float*>(wsc + L::kV)[tid] : 0.f;
+        if (tid < 64) az[tid] = 0.f;
+        __syncthreads();  // z_c and the zeroed row sums before the query tile's dot products
+        store_rows<D, kSplit ? 2 : 1, 256>(Kt, rk, nvalid, a.fmap, a.eps, tid);
+        store_rows<D, 0, 256>(Vt, rv, nvalid, a.fmap, a.eps, tid);
+        store_rows<D, kSplit ? 2 : 1, 256>(Qt, rq, nvalid, a.fmap, a.eps, tid, norm ? az : nullptr, zc);
+        store_rows<D, 0, 256>(Yt, ry, nvalid, a.fmap, a.eps, tid);
     }
-    if (tid < 64) az[tid] = 0.f;
     bool ok = warp_wait(bar_ld, 0, err, kErrLoad);
     tc_fence_before();
     ok = __syncthreads_and(ok);
@@ -531,8 +566,13 @@ __global__ void __launch_bounds__(256, D == 64 ? 2 : 1) bwd_mid_kernel(const __g
     for (int r = 0; r < G && ok; ++r) {
         const int hq = hk * G + r;
         const int64_t qrow0 = ((int64_t)b * a.T + t0) * a.Hq + hq;
-        load_rows<D, kSplit ? 2 : 1, 256>(Qt, a.q, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid, norm ? az : nullptr, zc);
-        load_rows<D, 0, 256>(Yt, a.dy, qrow0, a.Hq, nvalid, a.fmap, a.eps, tid);
+        if (r > 0) {  // (the first head's rows were loaded with the keys)
+            Rows<D, 256> rq, ry;
+            fetch_rows<D, 256>(rq, a.q, qrow0, a.Hq, nvalid, tid);
+            fetch_rows<D, 256>(ry, a.dy, qrow0, a.Hq, nvalid, tid);
+            store_rows<D, kSplit ? 2 : 1, 256>(Qt, rq, nvalid, a.fmap, a.eps, tid, norm ? az : nullptr, zc);
+            store_rows<D, 0, 256>(Yt, ry, nvalid, a.fmap, a.eps, tid);
+        }
 
         // (a) P = a kt^T and a . z_c
         ok = mma_round([&] {
@@ -865,8 +905,13 @@ __global__ void __launch_bounds__(256, 1) bwd_kvgrad_kernel(const __grid_constan
         tmem_relinquish();
     }
     const int64_t row0 = ((int64_t)b * a.T + t0) * a.Hkv + hk;
-    load_rows<D, kSplit ? 2 : 1, 256>(Kt, a.k, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
-    load_rows<D, 0, 256>(Vt, a.v, row0, a.Hkv, nvalid, a.fmap, a.eps, tid);
+    {
+        Rows<D, 256> rk, rv;  // both tiles' loads in flight at once
+        fetch_rows<D, 256>(rk, a.k, row0, a.Hkv, nvalid, tid);
+        fetch_rows<D, 256>(rv, a.v, row0, a.Hkv, nvalid, tid);
+        store_rows<D, kSplit ? 2 : 1, 256>(Kt, rk, nvalid, a.fmap, a.eps, tid);
+        store_rows<D, 0, 256>(Vt, rv, nvalid, a.fmap, a.eps, tid);
+    }
     if (tid < D) rv[tid] = a.norm ? reinterpret_cast<const float*>(wsc + L::kV)[tid] : 0.f;
     bool ok = warp_wait(bar_ld, 0, a.err, kErrLoad);
     fence_proxy_async();
