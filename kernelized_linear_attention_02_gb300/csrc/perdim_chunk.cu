@@ -60,6 +60,12 @@ __device__ __forceinline__ uint64_t valid_word(const Args& a, int b, int t0) {
     return step_word(valid(2 * lane), valid(2 * lane + 1));
 }
 
+// eight consecutive floats of shared memory (32-byte aligned) in two 16-byte loads
+__device__ __forceinline__ void load_g8(const float* p, float (&g)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    g[0] = a.x, g[1] = a.y, g[2] = a.z, g[3] = a.w, g[4] = b.x, g[5] = b.y, g[6] = b.z, g[7] = b.w;
+}
+
 __device__ __forceinline__ float load_g(const Args& a, int b, int hk, int t, int k) {
     return fmaxf(__bfloat162float(a.decay[(((size_t)b * a.T + t) * a.Hkv + hk) * kD + k]), kMinLogDecay);
 }
@@ -352,10 +358,11 @@ __global__ void __launch_bounds__(256, 1)
         }
         *reinterpret_cast<uint4*>(Vt + off) = vv;
         if (fac) {
-            float f[8];
+            float f[8], g8[8];
+            load_g8(Gs + l * kD + k0, g8);
             const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(&kk);
 #pragma unroll
-            for (int x = 0; x < 8; ++x) f[x] = __bfloat162float(kp[x]) * __expf(-Gs[l * kD + k0 + x]);
+            for (int x = 0; x < 8; ++x) f[x] = __bfloat162float(kp[x]) * __expf(-g8[x]);
             uint4 hi, lo;
             split8(f, hi, lo);
             st16(Kb + off, hi);
@@ -391,9 +398,10 @@ __global__ void __launch_bounds__(256, 1)
                 if (e >= 128 * 16) continue;
                 const int row = e >> 4, cc = e & 15, k0 = 8 * cc, t = row & 63;
                 const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(&qq[u]);
-                float f[8];
+                float f[8], g8[8];
+                load_g8(Gs + t * kD + k0, g8);
 #pragma unroll
-                for (int x = 0; x < 8; ++x) f[x] = __bfloat162float(qp[x]) * __expf(Gs[t * kD + k0 + x]);
+                for (int x = 0; x < 8; ++x) f[x] = __bfloat162float(qp[x]) * __expf(g8[x]);
                 uint4 hi, lo;
                 split8(f, hi, lo);
                 const uint32_t off = (cc >> 3) * 16384 + swc(row, cc & 7);
