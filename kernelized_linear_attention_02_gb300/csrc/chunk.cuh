@@ -152,11 +152,12 @@ struct Cfg {
     // phi(Q) (64 x D, D/32 swizzled blocks of 8 KB); the gated rule, whose
     // state is rescaled every chunk anyway, reads a bf16 hi/lo copy of it
     static constexpr bool kTf32 = !GATED;
-    // linear causal with grouped query heads (G > 1, decided at run time):
-    // two MMA issuers -- warp 1 the scores and the intra products, warp 14 the
-    // read-outs of all G heads with the carried state and the state updates --
-    // so that the waits of one overlap the issue of the other.  With one query
-    // head per kv head the single issuer interleaves them better.
+    // linear causal with grouped query heads (G > 1) or at head size 128
+    // (decided at launch): two MMA issuers -- warp 1 the scores and the intra
+    // products, warp 14 the read-outs of all G heads with the carried state
+    // and the state updates -- so that the waits of one overlap the issue of
+    // the other.  At head size 64 with one query head per kv head the single
+    // issuer interleaves them better.
     static constexpr bool kSplitMma = kTf32 && MODE == kCausal;
     static constexpr int kQf = (kHasQ && kTf32) ? 2 * kTile : 0;
     static constexpr int kQStage = kHasQ ? kTile * (GATED ? 2 : 1) + kQf : 0;
@@ -267,8 +268,8 @@ __device__ __forceinline__ __nv_bfloat16& bf_at(uint8_t* base, uint32_t off) {
 }
 
 // SPLIT: two MMA issuers (linear causal rule with G > 1 query heads per kv
-// head, see Cfg::kSplitMma); a separate instantiation, so that the kernels
-// for G = 1 carry no code of the split issue.  MASK: the sequence-validity
+// head or at head size 128, see Cfg::kSplitMma); a separate instantiation,
+// so that the single-issuer kernels carry no code of the split issue.  MASK: the sequence-validity
 // mask is read (Keras request, Masking); without it the mask pointer is a
 // constant null and every mask branch folds away, so unmasked calls run
 // exactly the code they would run without mask support.
@@ -703,12 +704,13 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     }
                     // scores, and in columns 64..71 phi(q).[Z_hi; Z_lo] from the Z rows
                     const uint32_t tA = tmem + Cf::kColA + 80 * ab;
+                    const uint64_t dq0 = sdesc_sw128(smem_u32(Qb(sq)), 16, 1024);
+                    const uint64_t dk0 = sdesc_sw128(smem_u32(Kb(s)), 16, 1024);
 #pragma unroll 1
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
                         const uint32_t ko = (ks >> 2) * Cf::kKBlk + (ks & 3) * 32;
-                        mma_ss(tA, sdesc_sw128(smem_u32(Qb(sq) + qo), 16, 1024),
-                               sdesc_sw128(smem_u32(Kb(s) + ko), 16, 1024), id_scores, ks > 0, lead);
+                        mma_ss(tA, dq0 + (qo >> 4), dk0 + (ko >> 4), id_scores, ks > 0, lead);
                     }
                     mma_commit(&a_full[ab], lead);
                     mma_commit(&empty_q[sq], lead);  // this warp is done with the query slot
@@ -719,11 +721,14 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t tY = tmem + Cf::kColY + 64 * yb;
+                    const uint64_t dv0 = sdesc_sw128(smem_u32(Vb(s)), 8192, 1024);
+                    const uint64_t dh0 = sdesc_sw128(smem_u32(ATh(tb)), 16, 1024);
+                    const uint64_t dl0 = sdesc_sw128(smem_u32(ATl(tb)), 16, 1024);
 #pragma unroll 1
                     for (int ks = 0; ks < kC / 16; ++ks) {
-                        const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                        mma_ss(tY, av, sdesc_sw128(smem_u32(ATh(tb) + ks * 32), 16, 1024), id_intra, 1, lead);
-                        if (ALO) mma_ss(tY, av, sdesc_sw128(smem_u32(ATl(tb) + ks * 32), 16, 1024), id_intra, 1, lead);
+                        const uint64_t av = dv0 + (uint64_t)(ks * 2048 >> 4);
+                        mma_ss(tY, av, dh0 + (uint64_t)(ks * 32 >> 4), id_intra, 1, lead);
+                        if (ALO) mma_ss(tY, av, dl0 + (uint64_t)(ks * 32 >> 4), id_intra, 1, lead);
                     }
                     mma_commit(&y_full[yb], lead);
                     if (r == G - 1) mma_commit(&empty_kv[s], lead);  // this warp is done with the K/V slot
@@ -1196,6 +1201,7 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
             constexpr uint32_t id_inter_tf32 = idesc_tf32(D, 64);
             constexpr uint32_t id_state = idesc_bf16(D, D, true, true);
             const uint32_t tS = tmem + Cf::kColS;
+            constexpr int kUnr2 = 1;
             for (int i = 0; i < nck && ok; ++i) {
                 const int s = i % NKV1;
                 // S before chunk i: the start state (state warps) or this warp's last update
@@ -1213,11 +1219,11 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t tY = tmem + Cf::kColY + 64 * yb;
-#pragma unroll 1
+                    const uint64_t df0 = sdesc_sw128(smem_u32(Qf(sq)), 16, 1024);
+#pragma unroll kUnr2
                     for (int ks = 0; ks < D / 8; ++ks) {
                         const uint32_t ko = (ks >> 2) * 8192 + (ks & 3) * 32;
-                        mma_ts_tf32(tY, tS + ks * 8, sdesc_sw128(smem_u32(Qf(sq) + ko), 16, 1024), id_inter_tf32,
-                                    ks > 0, lead);
+                        mma_ts_tf32(tY, tS + ks * 8, df0 + (ko >> 4), id_inter_tf32, ks > 0, lead);
                     }
                     mma_commit(&empty_q[sq], lead);     // this warp is done with the query slot
                     mma_commit(&inter_cmp[yb], lead);   // the intra product may add to Y^T
@@ -1231,13 +1237,14 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                 if (!ok) break;
                 tc_fence_after();
                 // S^T += V^T . phi(K) (+ V^T . phi(K)_lo)
-#pragma unroll 1
+                const uint64_t dv0 = sdesc_sw128(smem_u32(Vb(s)), 8192, 1024);
+                const uint64_t dk0 = sdesc_sw128(smem_u32(Kb(s)), (uint32_t)Cf::kKBlk, 1024);
+                const uint64_t dl0 = sdesc_sw128(smem_u32(Klo(s)), 8192, 1024);
+#pragma unroll kUnr2
                 for (int ks = 0; ks < kC / 16; ++ks) {
-                    const uint64_t av = sdesc_sw128(smem_u32(Vb(s) + ks * 2048), 8192, 1024);
-                    mma_ss(tS, av, sdesc_sw128(smem_u32(Kb(s) + ks * 2048), (uint32_t)Cf::kKBlk, 1024), id_state, 1,
-                           lead);
-                    if (SPLITK)
-                        mma_ss(tS, av, sdesc_sw128(smem_u32(Klo(s) + ks * 2048), 8192, 1024), id_state, 1, lead);
+                    const uint64_t o = (uint64_t)(ks * 2048 >> 4);
+                    mma_ss(tS, dv0 + o, dk0 + o, id_state, 1, lead);
+                    if (SPLITK) mma_ss(tS, dv0 + o, dl0 + o, id_state, 1, lead);
                 }
                 mma_commit(&empty_kv[s], lead);  // this warp is done with the K/V slot
                 mma_commit(upd_done, lead);

@@ -57,8 +57,10 @@ template <int D, int MODE, int OUT, bool MASK = false>
 struct Dispatch {
     template <bool NORM, int FMAP, bool GATED>
     static cudaError_t one(const Launch& L, cudaStream_t st) {
-        // linear causal rule with grouped query heads: the two-issuer kernel
-        if (MODE == kCausal && !GATED && L.args.G > 1)
+        // linear causal rule with grouped query heads, or at head size 128: the
+        // two-issuer kernel (at head size 64 with one query head per kv head
+        // the single issuer measured faster)
+        if (MODE == kCausal && !GATED && (L.args.G > 1 || D == 128))
             return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, MODE == kCausal && !GATED, MASK>(L, st);
         return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, false, MASK>(L, st);
     }
