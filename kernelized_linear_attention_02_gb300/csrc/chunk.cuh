@@ -117,7 +117,9 @@ template <bool SPLIT>
 constexpr int block_threads() { return SPLIT ? 512 : kThreads; }
 constexpr int kStateWarp0 = 2, kEpiWarp0 = 6, kFeatWarp0 = 10, kMmaSWarp = 14;  // warp 15: see kFeatMovedTo
 
-template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16>
+// AT2: two masked-score buffers where shared memory holds them (the
+// two-issuer kernel for grouped query heads)
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16, bool AT2 = false>
 struct Cfg {
     // the state update takes its key operand as bf16 hi + lo wherever that
     // operand is not exactly a bf16 value: the gated rule's decayed keys, and
@@ -165,10 +167,9 @@ struct Cfg {
     // would put up to 2^-9 of relative error on single output rows (the first
     // token of a sequence is one score times one value row)
     static constexpr bool kALo = true;
-    // one buffer of masked scores: the epilogue writes item n's once the intra
-    // product of item n - 1 (which read the previous ones) has completed
-    static constexpr int kNAT = MODE == kCausal ? 1 : 0;
-    static constexpr int kAT = kNAT * 2 * 8192;  // per buffer: hi, lo (64 x 64 bf16 each)
+    // masked-score buffers (hi, lo: 64 x 64 bf16 each): the epilogue writes
+    // item n's once the intra product of item n - kNAT has completed; two when
+    // shared memory holds them at the ring depths one buffer allows (below)
     static constexpr int kZrApply = (MODE == kApply && NORM) ? kZr : 0;
     // bf16 output: each item's 64 x D output tile is staged in shared memory
     // and leaves with 16-byte stores.  Row pitch D + 8 elements (16 bytes of
@@ -193,8 +194,8 @@ struct Cfg {
     // gated rule, which has none -- then the barriers
     static constexpr int kMiscNorm = GATED ? 0 : 1024 + 2 * kZpart * 4;
     static constexpr int kMisc = kMiscNorm + 512;
-    static constexpr int bytes(int nkv, int nq) {
-        return 1024 + nkv * kKvStage + nq * kQStage + kAT + kZrApply + kYS + kMisc + nkv * kGStage;
+    static constexpr int bytes(int nkv, int nq, int nat = MODE == kCausal ? 1 : 0) {
+        return 1024 + nkv * kKvStage + nq * kQStage + nat * 2 * 8192 + kZrApply + kYS + kMisc + nkv * kGStage;
     }
     static constexpr int kLimit = 227 * 1024;
     // ring depths: the deepest of (4,4), (4,3), (3,3), (3,2), (2,2) that
@@ -207,8 +208,10 @@ struct Cfg {
     static constexpr int kNQ0 = fits(kNKV0, 4) ? 4 : fits(kNKV0, 3) ? 3 : fits(kNKV0, 2) ? 2 : 1;
     static constexpr int kNKV = kHasKV ? kNKV0 : 0;
     static constexpr int kNQ = kHasQ ? kNQ0 : 0;
+    static constexpr int kNAT = MODE != kCausal ? 0 : (AT2 && bytes(kNKV, kNQ, 2) <= kLimit) ? 2 : 1;
+    static constexpr int kAT = kNAT * 2 * 8192;
     static_assert(kNKV <= 4 && kNQ <= 4, "barrier arrays hold four stages");
-    static constexpr int kSmem = bytes(kNKV, kNQ);
+    static constexpr int kSmem = bytes(kNKV, kNQ, kNAT);
     static_assert(kSmem <= kLimit, "shared memory budget");
     // TMEM columns
     // score buffers (64 + 8 columns for phi(q).Z each); the linear rule needs
@@ -267,17 +270,20 @@ __device__ __forceinline__ __nv_bfloat16& bf_at(uint8_t* base, uint32_t off) {
     return *reinterpret_cast<__nv_bfloat16*>(base + off);
 }
 
-// SPLIT: two MMA issuers (linear causal rule with G > 1 query heads per kv
-// head or at head size 128, see Cfg::kSplitMma); a separate instantiation,
-// so that the single-issuer kernels carry no code of the split issue.  MASK: the sequence-validity
+// SPLIT: 0 one MMA issuer; 1 two MMA issuers (linear causal rule at head
+// size 128 with one query head per kv head); 2 two MMA issuers for grouped
+// query heads, with two masked-score buffers where they fit and the scores of
+// the next item issued ahead of the current intra product (see
+// Cfg::kSplitMma).  Separate instantiations, so that each kernel carries only
+// the issue code it runs.  MASK: the sequence-validity
 // mask is read (Keras request, Masking); without it the mask pointer is a
 // constant null and every mask branch folds away, so unmasked calls run
 // exactly the code they would run without mask support.
-template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16, bool SPLIT = false, bool MASK = false>
-__global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>::kSplitMma && SPLIT>(), 1)
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16, int SPLIT = 0, bool MASK = false>
+__global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>::kSplitMma && SPLIT != 0>(), 1)
     chunk_kernel(const __grid_constant__ Args a, const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                  const __grid_constant__ CUtensorMap mapV) {
-    using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>;
+    using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16, SPLIT == 2>;
     constexpr bool SPLITK = Cf::kSplitK;
     constexpr bool TF32 = Cf::kTf32;
     constexpr bool ALO = Cf::kALo;
@@ -329,7 +335,7 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
     // capture by reference, and reading the parameter block through its
     // address inside hot loops would be a long-latency load per use.
     const int T = a.T, Hq = a.Hq, Hkv = a.Hkv, G = a.G, nseg = a.nseg;
-    constexpr bool split = Cf::kSplitMma && SPLIT;  // two MMA issuers
+    constexpr bool split = Cf::kSplitMma && SPLIT != 0;  // two MMA issuers
     constexpr int fmap = FMAP;
     const float eps = a.eps, scale = a.scale;
     const __nv_bfloat16* __restrict__ decay = a.decay;
@@ -684,6 +690,72 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
             };
 
             if constexpr (split) {
+                if constexpr (SPLIT == 2) {
+                // scores and intra products; the read-outs and updates are warp 14's.
+                // Grouped query heads (SPLIT 2): the scores of item n + 1 go out
+                // before the intra product of item n, so the epilogue masks them
+                // while that product waits for its masked scores; crossing into
+                // the next chunk needs a second key/value stage (this warp
+                // releases the current one at its end).  With one query head per
+                // kv head the look-ahead (which then always crosses into the next
+                // chunk) measured slower.
+                const int N = nck * G;
+                auto issue_scores = [&](int n) -> bool {
+                    const int i = n / G, r = n - i * G, s = i % NKV1, sq = n % NQ1, ab = n % NA;
+                    if (r == 0) {
+                        if (!warp_wait(&conv_kv[s], (i / NKV1) & 1, err, kErrConvKV)) return false;
+                        tc_fence_after();
+                    }
+                    if (!warp_wait(&conv_q[sq], (n / NQ1) & 1, err, kErrConvQ)) return false;
+                    tc_fence_after();
+                    if (n >= NA) {
+                        if (!warp_wait(&a_empty[ab], ((n / NA) & 1) ^ 1, err, kErrAEmpty)) return false;
+                        tc_fence_after();
+                    }
+                    // scores, and in columns 64..71 phi(q).[Z_hi; Z_lo] from the Z rows
+                    const uint32_t tA = tmem + Cf::kColA + 80 * ab;
+                    const uint64_t dq0 = sdesc_sw128(smem_u32(Qb(sq)), 16, 1024);
+                    const uint64_t dk0 = sdesc_sw128(smem_u32(Kb(s)), 16, 1024);
+#pragma unroll 1
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t qo = (ks >> 2) * 8192 + (ks & 3) * 32;
+                        const uint32_t ko = (ks >> 2) * Cf::kKBlk + (ks & 3) * 32;
+                        mma_ss(tA, dq0 + (qo >> 4), dk0 + (ko >> 4), id_scores, ks > 0, lead);
+                    }
+                    mma_commit(&a_full[ab], lead);
+                    mma_commit(&empty_q[sq], lead);  // this warp is done with the query slot
+                    return true;
+                };
+                if (N > 0) ok = issue_scores(0);
+                for (int n = 0; n < N && ok; ++n) {
+                    const int i = n / G, r = n - i * G, s = i % NKV1, yb = n % NY;
+                    const int tb = n % NAT;
+                    const bool look = n + 1 < N && (r + 1 < G || NKV1 >= 2);
+                    if (look) {
+                        ok = issue_scores(n + 1);
+                        if (!ok) break;
+                    }
+                    ok = warp_wait(&at_full[tb], (n / NAT) & 1, err, kErrATFull);
+                    if (!ok) break;
+                    // the read-out of item n (warp 14) starts this Y^T buffer: complete first
+                    ok = warp_wait(&inter_cmp[yb], (n / NY) & 1, err, kErrStateDone);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t tY = tmem + Cf::kColY + 64 * yb;
+                    const uint64_t dv0 = sdesc_sw128(smem_u32(Vb(s)), 8192, 1024);
+                    const uint64_t dh0 = sdesc_sw128(smem_u32(ATh(tb)), 16, 1024);
+                    const uint64_t dl0 = sdesc_sw128(smem_u32(ATl(tb)), 16, 1024);
+#pragma unroll 1
+                    for (int ks = 0; ks < kC / 16; ++ks) {
+                        const uint64_t av = dv0 + (uint64_t)(ks * 2048 >> 4);
+                        mma_ss(tY, av, dh0 + (uint64_t)(ks * 32 >> 4), id_intra, 1, lead);
+                        if (ALO) mma_ss(tY, av, dl0 + (uint64_t)(ks * 32 >> 4), id_intra, 1, lead);
+                    }
+                    mma_commit(&y_full[yb], lead);
+                    if (r == G - 1) mma_commit(&empty_kv[s], lead);  // this warp is done with the K/V slot
+                    if (!look && n + 1 < N) ok = issue_scores(n + 1);
+                }
+                } else {
                 // scores and intra products; the read-outs and updates are warp 14's
                 const int N = nck * G;
                 for (int n = 0; n < N && ok; ++n) {
@@ -732,6 +804,7 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                     }
                     mma_commit(&y_full[yb], lead);
                     if (r == G - 1) mma_commit(&empty_kv[s], lead);  // this warp is done with the K/V slot
+                }
                 }
                 mma_commit(final_done, lead);  // every operation of this warp complete
             } else {

@@ -11,9 +11,9 @@
 namespace la {
 namespace chunk {
 
-template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUTBF, bool SPLIT = false, bool MASK = false>
+template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUTBF, int SPLIT = 0, bool MASK = false>
 cudaError_t run_one(const Launch& L, cudaStream_t st) {
-    using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUTBF>;
+    using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUTBF, SPLIT == 2>;
     auto kern = chunk_kernel<D, MODE, NORM, FMAP, GATED, OUTBF, SPLIT, MASK>;
     // per device: the context in which the shared-memory limit of this
     // instantiation was raised (0 = not yet); a new context (a device reset)
@@ -34,7 +34,7 @@ cudaError_t run_one(const Launch& L, cudaStream_t st) {
         // the kernel waits for it (griddepcontrol.wait) before reading its output
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = L.grid;
-        cfg.blockDim = dim3(block_threads<Cf::kSplitMma && SPLIT>());
+        cfg.blockDim = dim3(block_threads<Cf::kSplitMma && SPLIT != 0>());
         cfg.dynamicSmemBytes = Cf::kSmem;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -45,7 +45,7 @@ cudaError_t run_one(const Launch& L, cudaStream_t st) {
         e = cudaLaunchKernelEx(&cfg, kern, L.args, L.mq, L.mk, L.mv);
         if (e != cudaSuccess) return e;
     } else {
-        kern<<<L.grid, block_threads<Cf::kSplitMma && SPLIT>(), Cf::kSmem, st>>>(L.args, L.mq, L.mk, L.mv);
+        kern<<<L.grid, block_threads<Cf::kSplitMma && SPLIT != 0>(), Cf::kSmem, st>>>(L.args, L.mq, L.mk, L.mv);
     }
     note_launch();
     return cudaGetLastError();
@@ -57,12 +57,14 @@ template <int D, int MODE, int OUT, bool MASK = false>
 struct Dispatch {
     template <bool NORM, int FMAP, bool GATED>
     static cudaError_t one(const Launch& L, cudaStream_t st) {
-        // linear causal rule with grouped query heads, or at head size 128: the
-        // two-issuer kernel (at head size 64 with one query head per kv head
-        // the single issuer measured faster)
-        if (MODE == kCausal && !GATED && (L.args.G > 1 || D == 128))
-            return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, MODE == kCausal && !GATED, MASK>(L, st);
-        return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, false, MASK>(L, st);
+        // linear causal rule: the two-issuer kernel for grouped query heads, and
+        // at head size 128 with one query head per kv head (at head size 64 the
+        // single issuer measured faster there)
+        if constexpr (MODE == kCausal && !GATED) {
+            if (L.args.G > 1) return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, 2, MASK>(L, st);
+            if constexpr (D == 128) return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, 1, MASK>(L, st);
+        }
+        return run_one<D, MODE, NORM, FMAP, GATED, OUT == 1, 0, MASK>(L, st);
     }
     template <bool NORM>
     static cudaError_t fmap(const Launch& L, cudaStream_t st) {
