@@ -197,7 +197,13 @@ struct Cfg {
     static constexpr int bytes(int nkv, int nq, int nat = MODE == kCausal ? 1 : 0) {
         return 1024 + nkv * kKvStage + nq * kQStage + nat * 2 * 8192 + kZrApply + kYS + kMisc + nkv * kGStage;
     }
-    static constexpr int kLimit = 227 * 1024;
+    // the linear rule's state pass at head size 64 runs two CTAs per SM (its
+    // ring sized for half the shared memory, its TMEM the state's D
+    // columns): the two-pass sequence split then runs its state pass on twice
+    // as many, half-length sub-segments in one wave.  (The gated state pass
+    // would spill at the register budget of two CTAs.)
+    static constexpr bool kTwoPerSm = MODE == kState && D == 64 && !GATED;
+    static constexpr int kLimit = kTwoPerSm ? 113 * 1024 : 227 * 1024;
     // ring depths: the deepest of (4,4), (4,3), (3,3), (3,2), (2,2) that
     // shared memory holds (key/value and query stages), else fewer
     static constexpr bool fits(int nkv, int nq) {
@@ -223,8 +229,8 @@ struct Cfg {
     static constexpr uint32_t kColLo = D + D / 2;  // S^T lo (gated)
     static constexpr uint32_t kColA = kTf32 ? D : 2 * D;  // score buffers, 80 columns apart
     static constexpr uint32_t kColY = kColA + 80 * kNA;
-    static constexpr uint32_t kTmemCols = 512;
-    static_assert(kColY + 64 * kNY <= kTmemCols, "TMEM budget");
+    static constexpr uint32_t kTmemCols = MODE == kState ? D : 512;  // the state pass holds S^T alone
+    static_assert(MODE == kState || kColY + 64 * kNY <= kTmemCols, "TMEM budget");
 };
 
 // Rounds a shared-memory pointer up to 1024 bytes by pointer arithmetic (not
@@ -280,7 +286,8 @@ __device__ __forceinline__ __nv_bfloat16& bf_at(uint8_t* base, uint32_t off) {
 // constant null and every mask branch folds away, so unmasked calls run
 // exactly the code they would run without mask support.
 template <int D, int MODE, bool NORM, int FMAP, bool GATED, bool OUT_BF16, int SPLIT = 0, bool MASK = false>
-__global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>::kSplitMma && SPLIT != 0>(), 1)
+__global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>::kSplitMma && SPLIT != 0>(),
+                                  Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16>::kTwoPerSm ? 2 : 1)
     chunk_kernel(const __grid_constant__ Args a, const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                  const __grid_constant__ CUtensorMap mapV) {
     using Cf = Cfg<D, MODE, NORM, FMAP, GATED, OUT_BF16, SPLIT == 2>;
@@ -951,9 +958,10 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
         bool ok = true;
 
         // ---- start state -> S^T (fp32) in TMEM.  Causal segment s > 0 folds
-        // the increments of segments 0..s-1 (from the state pass) onto the
-        // initial state, decay-weighted for gated.
+        // the increments of segments 0..s-1 (from the state pass, fold_r per
+        // segment) onto the initial state, decay-weighted for gated.
         const bool fold = MODE == kCausal && a.S_seg && seg > 0;
+        const int nfold = seg * a.fold_r, fstride = nseg * a.fold_r;  // increments to fold; per (b, kv head)
         const float* S_start = MODE == kState ? nullptr : a.S_init;
         if (MODE == kCausal) griddep_wait();  // the segment state pass has completed
         // Loads are batched 32 columns x 2 segments at a time (independent
@@ -965,9 +973,9 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
             for (int x = 0; x < 32; ++x)
                 run[x] = (S_start && vrow_ok) ? S_start[(size_t)bh * D * D + (size_t)(c0 + x) * D + vrow] : 0.f;
             if (fold && vrow_ok) {
-                for (int p = 0; p < seg; p += 2) {
-                    const bool two = p + 1 < seg;
-                    const float* s0 = a.S_seg + ((size_t)bh * nseg + p) * D * D + (size_t)c0 * D + vrow;
+                for (int p = 0; p < nfold; p += 2) {
+                    const bool two = p + 1 < nfold;
+                    const float* s0 = a.S_seg + ((size_t)bh * fstride + p) * D * D + (size_t)c0 * D + vrow;
                     const float* s1 = s0 + (size_t)D * D;
                     float d0[32], d1[32];
 #pragma unroll
@@ -975,8 +983,8 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
                         d0[x] = s0[(size_t)x * D];
                         d1[x] = two ? s1[(size_t)x * D] : 0.f;
                     }
-                    const float w0 = GATED ? __expf(a.G_seg[(size_t)bh * nseg + p]) : 1.f;
-                    const float w1 = (GATED && two) ? __expf(a.G_seg[(size_t)bh * nseg + p + 1]) : 1.f;
+                    const float w0 = GATED ? __expf(a.G_seg[(size_t)bh * fstride + p]) : 1.f;
+                    const float w1 = (GATED && two) ? __expf(a.G_seg[(size_t)bh * fstride + p + 1]) : 1.f;
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
                         run[x] = GATED ? fmaf(w0, run[x], d0[x]) : run[x] + d0[x];
@@ -1366,11 +1374,12 @@ __global__ void __launch_bounds__(block_threads<Cfg<D, MODE, NORM, FMAP, GATED, 
             zreg = a.Z_init ? a.Z_init[(size_t)bh * D + ct] : 0.f;
             if (fold && a.Z_seg) {
                 // independent loads, four in flight; summed in segment order
-                for (int p = 0; p < seg; p += 4) {
+                const int nfold = seg * a.fold_r, fstride = nseg * a.fold_r;
+                for (int p = 0; p < nfold; p += 4) {
                     float z4[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        z4[u] = p + u < seg ? a.Z_seg[((size_t)bh * nseg + p + u) * D + ct] : 0.f;
+                        z4[u] = p + u < nfold ? a.Z_seg[((size_t)bh * fstride + p + u) * D + ct] : 0.f;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) zreg += z4[u];
                 }

@@ -22,6 +22,7 @@ struct Args {
     int B, T, Hq, Hkv, G;
     int cps;   // chunks per segment
     int nseg;  // segments per (b, kv head)
+    int fold_r;  // causal: state-pass increments per segment (the state pass may run on sub-segments)
     int fmap;
     float eps, scale;
     const float* S_init;  // (B*Hkv, Dk, Dv) initial state (causal) or the global state (apply); may be null

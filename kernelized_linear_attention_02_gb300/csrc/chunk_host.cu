@@ -59,6 +59,7 @@ bool dev_info(DevInfo* out) {
 
 struct Plan {
     int nseg, cps;
+    int sub = 1;  // causal: state-pass sub-segments per segment
 };
 
 // Enough (batch, kv head, segment) tiles for one CTA per SM, never more
@@ -70,6 +71,18 @@ Plan plan_segments(int64_t BH, int nchunks, int sms) {
     return {(nchunks + cps - 1) / cps, cps};
 }
 
+// Causal plan.  At head size 64 the linear rule's state pass runs two CTAs
+// per SM (chunk.cuh, Cfg::kTwoPerSm), so it takes each full segment as two
+// half-length sub-segments whenever their CTAs still fit in one wave: its
+// chain of chunks per CTA halves, and each causal segment folds twice as many
+// increments.
+Plan plan_causal(int64_t BH, int nchunks, int sms, int D, bool gated) {
+    Plan pl = plan_segments(BH, nchunks, sms);
+    if (D == 64 && !gated && pl.nseg > 1 && pl.cps % 2 == 0 && pl.cps >= 4 && (int64_t)(pl.nseg - 1) * 2 * BH <= 2LL * sms)
+        pl.sub = 2;
+    return pl;
+}
+
 struct WsLayout {
     size_t S_seg = 0, Z_seg = 0, G_seg = 0, S_tot = 0, Z_tot = 0, total = 0;
 };
@@ -77,18 +90,20 @@ struct WsLayout {
 // state when the caller streams in place (S_out == S0), because the last
 // segment writes the final state while other segments may still read S0.
 
-WsLayout ws_layout(const Problem& P, bool causal, int nseg) {
+WsLayout ws_layout(const Problem& P, bool causal, int nseg, int sub = 1) {
     WsLayout w;
     const size_t BH = static_cast<size_t>(P.B) * P.Hkv;
     const size_t D = P.Dk;
     size_t off = 0;
     if (causal && nseg <= 1) return w;
+    // one increment per state-pass (sub-)segment
+    const size_t ninc = static_cast<size_t>(nseg) * sub;
     w.S_seg = off;
-    off += round_up(BH * nseg * D * D * sizeof(float));
+    off += round_up(BH * ninc * D * D * sizeof(float));
     w.Z_seg = off;
-    off += round_up(BH * nseg * D * sizeof(float));
+    off += round_up(BH * ninc * D * sizeof(float));
     w.G_seg = off;
-    off += round_up(BH * nseg * sizeof(float));
+    off += round_up(BH * ninc * sizeof(float));
     {
         w.S_tot = off;
         off += round_up(BH * D * D * sizeof(float));
@@ -164,6 +179,7 @@ chunk::Launch base_launch(const Problem& P, int mode, const DevInfo& di) {
     a.scale = P.scale;
     a.mask = P.mask;
     a.err = di.err;
+    a.fold_r = 1;
     return L;
 }
 
@@ -209,8 +225,12 @@ size_t chunk_workspace_bytes(const Problem& P, bool causal) {
     DevInfo di;
     if (!dev_info(&di)) return 0;
     const int nchunks = (int)((P.T + 63) / 64);
+    if (causal) {
+        const Plan pl = plan_causal((int64_t)P.B * P.Hkv, nchunks, di.sms, (int)P.Dk, P.gated != 0);
+        return ws_layout(P, true, pl.nseg, pl.sub).total;
+    }
     const Plan pl = plan_segments((int64_t)P.B * P.Hkv, nchunks, di.sms);
-    return ws_layout(P, causal, pl.nseg).total;
+    return ws_layout(P, false, pl.nseg).total;
 }
 
 cudaError_t chunk_causal(const Problem& P, const void* q, const void* k, const void* v, const void* decay,
@@ -221,8 +241,8 @@ cudaError_t chunk_causal(const Problem& P, const void* q, const void* k, const v
     const int D = P.Dk;
     const int64_t BH = (int64_t)P.B * P.Hkv;
     const int nchunks = (int)((P.T + 63) / 64);
-    const Plan pl = plan_segments(BH, nchunks, di.sms);
-    const WsLayout wl = ws_layout(P, true, pl.nseg);
+    const Plan pl = plan_causal(BH, nchunks, di.sms, D, P.gated != 0);
+    const WsLayout wl = ws_layout(P, true, pl.nseg, pl.sub);
     char* w = static_cast<char*>(ws);
 
     chunk::Launch L = base_launch(P, chunk::kCausal, di);
@@ -253,9 +273,12 @@ cudaError_t chunk_causal(const Problem& P, const void* q, const void* k, const v
             if (e != cudaSuccess) return e;
             L.args.Z_init = Z_copy;
         }
+        // the state pass over segments 0..nseg-2, each as pl.sub sub-segments
         chunk::Launch Ls = L;
         Ls.mode = chunk::kState;
-        Ls.grid = dim3((unsigned)BH, (unsigned)(pl.nseg - 1));
+        Ls.args.cps = pl.cps / pl.sub;
+        Ls.args.nseg = pl.nseg * pl.sub;
+        Ls.grid = dim3((unsigned)BH, (unsigned)((pl.nseg - 1) * pl.sub));
         Ls.args.S_dst = S_seg;
         Ls.args.Z_dst = P.norm ? Z_seg : nullptr;
         Ls.args.G_dst = G_seg;
@@ -264,6 +287,7 @@ cudaError_t chunk_causal(const Problem& P, const void* q, const void* k, const v
         L.args.S_seg = S_seg;
         L.args.Z_seg = P.norm ? Z_seg : nullptr;
         L.args.G_seg = G_seg;
+        L.args.fold_r = pl.sub;
         L.pdl = true;  // overlaps the state pass's tail; waits for it before the fold
     }
     L.grid = dim3((unsigned)BH, (unsigned)pl.nseg);

@@ -118,6 +118,14 @@ def test_masked_sequence_segments(shape, rule):
         masked_case(*shape, torch.bfloat16, kind, fmap, norm, rule=rule, seed=17)
 
 
+
+@pytest.mark.parametrize("kind", ["right", "left", "gaps", "random"])
+def test_masked_state_pass_sub_segments(kind):
+    """The masked state pass on half-length sub-segments (head size 64, 16
+    streams of 64 chunks): invalid runs cross sub-segment boundaries."""
+    masked_case(2, 64 * 63 + 37, 16, 8, 64, 64, torch.bfloat16, kind, "elu_plus_one", True, seed=23)
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=ids)
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("kind", inputs.MASK_KINDS)

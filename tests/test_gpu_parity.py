@@ -246,6 +246,21 @@ def test_gated_infinite_decay(shape, dtype):
     assert_close(to64(S), Sr, tol, "S")
 
 
+
+@pytest.mark.parametrize("mode", [("elu_plus_one", True), ("relu", True), ("none", False)],
+                         ids=lambda m: f"{m[0]}-{'norm' if m[1] else 'raw'}")
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32out", "bf16out"])
+def test_causal_state_pass_sub_segments(mode, out_dtype):
+    """Head size 64 with 16 (batch, kv head) streams of 64 chunks: 8 sequence
+    segments of 8 chunks, whose state pass (two CTAs per SM) runs as 14
+    half-length sub-segments, so that every segment folds two increments per
+    earlier segment.  Ragged last chunk, grouped heads, carried initial state
+    and the final state, against the oracle."""
+    fmap, norm = mode
+    run_case(2, 64 * 63 + 37, 16, 8, 64, 64, torch.bfloat16, out_dtype, fmap, norm, S0=True, seed=71,
+             std=0.5 if fmap == "elu_plus_one" else 1.0)
+
+
 @pytest.mark.parametrize("shape", SHAPES[1:], ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("mode", MODES[:3], ids=lambda m: f"{m[0]}-{'norm' if m[1] else 'raw'}")
