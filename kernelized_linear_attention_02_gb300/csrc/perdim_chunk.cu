@@ -120,23 +120,23 @@ __global__ void __launch_bounds__(128, 1)
         float* Gs = reinterpret_cast<float*>(sm + PrepSmem::kG);  // column k is this thread's
         float G = 0.f;
 #pragma unroll 1
-        for (int t16 = 0; t16 < kC; t16 += 16) {
-            float g[16];  // sixteen steps' decays in flight, then their running sum
+        for (int t16 = 0; t16 < kC; t16 += 32) {
+            float g[32];  // thirty-two steps' decays in flight, then their running sum
 #pragma unroll
-            for (int u = 0; u < 16; ++u) g[u] = ((vw >> (t16 + u)) & 1) ? load_g(a, b, hk, t0 + t16 + u, k) : 0.f;
+            for (int u = 0; u < 32; ++u) g[u] = ((vw >> (t16 + u)) & 1) ? load_g(a, b, hk, t0 + t16 + u, k) : 0.f;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < 32; ++u) {
                 G += g[u];
                 Gs[(t16 + u) * kD + k] = G;
             }
         }
         const int kb = k >> 6, kc = k & 63;
 #pragma unroll 1
-        for (int t8 = 0; t8 < kC; t8 += 8) {
-            // eight steps' key and value elements in flight, then their tiles
-            __nv_bfloat16 kk[8], vv[8];
+        for (int t8 = 0; t8 < kC; t8 += 16) {
+            // sixteen steps' key and value elements in flight, then their tiles
+            __nv_bfloat16 kk[16], vv[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < 16; ++u) {
                 const int t = t8 + u;
                 const size_t row = ((size_t)b * a.T + t0 + t) * a.Hkv + hk;
                 const bool ok = (vw >> t) & 1;
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(128, 1)
                 vv[u] = ok ? vin[row * kD + k] : __float2bfloat16_rn(0.f);  // value v = tid, exact
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < 16; ++u) {
                 const int t = t8 + u;
                 const float x = __bfloat162float(kk[u]) * __expf(G - Gs[t * kD + k]);
                 const __nv_bfloat16 h = __float2bfloat16_rn(x);
@@ -308,19 +308,25 @@ __global__ void __launch_bounds__(256, 1)
         const int v = quad * 32 + lane;
         const uint8_t* st = wsc + Ws::kS;
 #pragma unroll 1
-        for (int p = 0; p < 4; ++p) {
-            uint32_t h[16], l[16];
+        for (int p0 = 0; p0 < 4; p0 += 2) {
+            // two 32-key blocks (hi and lo) in flight, then their four TMEM stores
+            uint32_t h[2][16], l[2][16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int k0 = 32 * p + 8 * q4;
-                const uint32_t off = (k0 >> 6) * 16384 + swc(v, (k0 & 63) >> 3);
-                const uint4 hh = *reinterpret_cast<const uint4*>(st + off);
-                const uint4 ll = *reinterpret_cast<const uint4*>(st + 32768 + off);
-                h[4 * q4] = hh.x, h[4 * q4 + 1] = hh.y, h[4 * q4 + 2] = hh.z, h[4 * q4 + 3] = hh.w;
-                l[4 * q4] = ll.x, l[4 * q4 + 1] = ll.y, l[4 * q4 + 2] = ll.z, l[4 * q4 + 3] = ll.w;
+            for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int k0 = 32 * (p0 + pp) + 8 * q4;
+                    const uint32_t off = (k0 >> 6) * 16384 + swc(v, (k0 & 63) >> 3);
+                    const uint4 hh = *reinterpret_cast<const uint4*>(st + off);
+                    const uint4 ll = *reinterpret_cast<const uint4*>(st + 32768 + off);
+                    h[pp][4 * q4] = hh.x, h[pp][4 * q4 + 1] = hh.y, h[pp][4 * q4 + 2] = hh.z, h[pp][4 * q4 + 3] = hh.w;
+                    l[pp][4 * q4] = ll.x, l[pp][4 * q4 + 1] = ll.y, l[pp][4 * q4 + 2] = ll.z, l[pp][4 * q4 + 3] = ll.w;
+                }
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+                tmem_st16(tmem_addr(tmem + kOutSHi, quad * 32, 16 * (p0 + pp)), h[pp]);
+                tmem_st16(tmem_addr(tmem + kOutSLo, quad * 32, 16 * (p0 + pp)), l[pp]);
             }
-            tmem_st16(tmem_addr(tmem + kOutSHi, quad * 32, 16 * p), h);
-            tmem_st16(tmem_addr(tmem + kOutSLo, quad * 32, 16 * p), l);
         }
         tmem_st_wait();
     } else {
@@ -328,12 +334,12 @@ __global__ void __launch_bounds__(256, 1)
         const int k = tid - 128;
         float G_ = 0.f, mn = 0.f, mx = 0.f;
 #pragma unroll 1
-        for (int t8 = 0; t8 < kC; t8 += 16) {
-            float g[16];  // sixteen steps' decays in flight, then their running sum
+        for (int t8 = 0; t8 < kC; t8 += 32) {
+            float g[32];  // thirty-two steps' decays in flight, then their running sum
 #pragma unroll
-            for (int u = 0; u < 16; ++u) g[u] = ((vw >> (t8 + u)) & 1) ? load_g(a, b, hk, t0 + t8 + u, k) : 0.f;
+            for (int u = 0; u < 32; ++u) g[u] = ((vw >> (t8 + u)) & 1) ? load_g(a, b, hk, t0 + t8 + u, k) : 0.f;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < 32; ++u) {
                 G_ += g[u];
                 Gs[(t8 + u) * kD + k] = G_;
                 mn = fminf(mn, G_);
@@ -376,15 +382,14 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t mma_phase = 0;
     bool ok = true;
     const int npairs = (G + 1) / 2;
-#pragma unroll 1
     // Qbar of query heads 2 pr and 2 pr + 1: rows (r, t), q o e^{G_t}, built by
-    // nthr threads (the loads of four rows in flight before their stores)
+    // nthr threads (the loads of eight rows in flight before their stores)
     auto build_qbar = [&](int pr, int bt, int nthr) {
 #pragma unroll 1
-        for (int e0 = bt; e0 < 128 * 16; e0 += 4 * nthr) {
-            uint4 qq[4];
+        for (int e0 = bt; e0 < 128 * 16; e0 += 8 * nthr) {
+            uint4 qq[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const int e = e0 + u * nthr, row = e >> 4, cc = e & 15, r = row >> 6, t = row & 63;
                 const int hq = 2 * pr + r;
                 qq[u] = (e < 128 * 16 && hq < G && ((vw >> t) & 1))
@@ -393,7 +398,7 @@ __global__ void __launch_bounds__(256, 1)
                             : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const int e = e0 + u * nthr;
                 if (e >= 128 * 16) continue;
                 const int row = e >> 4, cc = e & 15, k0 = 8 * cc, t = row & 63;
