@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(128, 1)
 // S <- gamma o S + N.  Loads run kScanDepth chunks ahead of the recurrence.
 constexpr int kScanThreads = 256;  // 32 values x 8 key groups
 constexpr int kScanCtas = 8;       // per stream: 4 value blocks x 2 key-group halves
-constexpr int kScanDepth = 4;
+constexpr int kScanDepth = 8;
 
 __global__ void __launch_bounds__(kScanThreads) perdim_scan_kernel(const __grid_constant__ Args a) {
     const int bh = blockIdx.x / kScanCtas, j = blockIdx.x - bh * kScanCtas;
