@@ -283,15 +283,17 @@ __global__ void __launch_bounds__(128, 1) bwd_kv_kernel(const __grid_constant__ 
         }
         mma_commit(bar);
     }
-    // dz[k] = sum_t phi(k[t][k]) in fp32 while the product runs, of phi as the
-    // products see it (hi + lo, or one part), so that z and S describe the same keys
+    // dz[k] = sum_t phi(k[t][k]) in fp32 while the product runs, from the key
+    // tile itself: phi as the products see it (hi + lo, or one part), so that z
+    // and S describe the same keys; rows past the sequence hold zeros
     if (a.norm && tid < D) {
         float z = 0.f;
 #pragma unroll 8
-        for (int t = 0; t < nvalid; ++t) {
-            const float f = phi_f(a.fmap, __bfloat162float(a.k[(row0 + (int64_t)t * a.Hkv) * D + tid]), a.eps);
-            const __nv_bfloat16 h = __float2bfloat16_rn(f);
-            z += __bfloat162float(h) + (kSplit ? __bfloat162float(__float2bfloat16_rn(f - __bfloat162float(h))) : 0.f);
+        for (int t = 0; t < kC; ++t) {
+            const uint32_t off = toff_e<64>(t, tid);
+            float f = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Kt + off));
+            if (kSplit) f += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Kt + kC * D * 2 + off));
+            z += f;
         }
         reinterpret_cast<float*>(wsc + L::kDZ)[tid] = z;
     }
