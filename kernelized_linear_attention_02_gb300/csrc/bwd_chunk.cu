@@ -121,9 +121,6 @@ __device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
     for (int x = 0; x < 8; ++x) f[x] = __bfloat162float(p[x]);
 }
 
-// 64 token rows (t0 .. t0 + 63, rows at or past nvalid zero) of one head of a
-// (B, T, H, D) bf16 tensor into a 64-row tile; kMode 0: as they are, 1: phi
-// as one bf16 part, 2: phi as hi (tile) and lo (tile + 128 D).
 // The 64 token rows (t0 .. t0 + 63, rows at or past nvalid zero) of one head
 // of a (B, T, H, D) bf16 tensor, by kNT threads: fetch_rows issues the loads,
 // store_rows writes the tile (kMode 0: as they are, 1: phi as one bf16 part,
@@ -176,14 +173,6 @@ __device__ __forceinline__ void store_rows(uint8_t* tile, const Rows<D, kNT>& r,
             }
         }
     }
-}
-template <int D, int kMode, int kNT = 128>
-__device__ __forceinline__ void load_rows(uint8_t* tile, const __nv_bfloat16* src, int64_t row0, int64_t rstride,
-                                          int nvalid, int fmap, float eps, int tid, float* az = nullptr,
-                                          const float* zc = nullptr) {
-    Rows<D, kNT> r;
-    fetch_rows<D, kNT>(r, src, row0, rstride, nvalid, tid);
-    store_rows<D, kMode, kNT>(tile, r, nvalid, fmap, eps, tid, az, zc);
 }
 
 // x = hi + mid + lo in three bf16 parts (about 24 significant bits), for 8 values
