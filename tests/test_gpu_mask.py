@@ -126,6 +126,12 @@ def test_masked_state_pass_sub_segments(kind):
     masked_case(2, 64 * 63 + 37, 16, 8, 64, 64, torch.bfloat16, kind, "elu_plus_one", True, seed=23)
 
 
+def test_masked_one_stream_longest_fold():
+    """The masked state pass with one stream of 601 chunks (300 sub-segments
+    folded by the last segment), interior gaps crossing their boundaries."""
+    masked_case(1, 64 * 600 + 17, 2, 1, 64, 64, torch.bfloat16, "gaps", "elu_plus_one", True, seed=29)
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=ids)
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("kind", inputs.MASK_KINDS)

@@ -261,6 +261,15 @@ def test_causal_state_pass_sub_segments(mode, out_dtype):
              std=0.5 if fmap == "elu_plus_one" else 1.0)
 
 
+def test_causal_one_stream_longest_fold():
+    """One (batch, kv head) stream of 601 chunks at head size 64: 151 segments
+    of 4 chunks (the last holds one ragged chunk), a state pass of 300
+    sub-segments, and a last segment that folds all 300 increments onto the
+    carried initial state."""
+    run_case(1, 64 * 600 + 17, 2, 1, 64, 64, torch.bfloat16, torch.float32, "elu_plus_one", True, S0=True,
+             seed=73, std=0.5)
+
+
 @pytest.mark.parametrize("shape", SHAPES[1:], ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("mode", MODES[:3], ids=lambda m: f"{m[0]}-{'norm' if m[1] else 'raw'}")
