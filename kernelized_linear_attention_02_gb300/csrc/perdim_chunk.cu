@@ -114,8 +114,19 @@ __global__ void __launch_bounds__(128, 1)
     const uint64_t vw = *s_word;
 
     {
-        // key dimension k = tid: cumulative decay down the chunk, then
-        // Khat[l][k] = k_l[k] e^{G_C[k] - G_l[k]} into the (rows l) tile
+        // the chunk's keys and values as 16-byte chunks (row l, eight key or
+        // value dimensions), all in flight while the decays load and sum
+        constexpr int kIt = kC * (kD / 8) / 128;
+        uint4 kq[kIt], vq[kIt];
+#pragma unroll
+        for (int i = 0; i < kIt; ++i) {
+            const int e = tid + 128 * i, l = e >> 4, cc = e & 15;
+            const size_t row = ((size_t)b * a.T + t0 + l) * a.Hkv + hk;
+            const bool ok = (vw >> l) & 1;
+            kq[i] = ok ? *reinterpret_cast<const uint4*>(kin + row * kD + 8 * cc) : make_uint4(0, 0, 0, 0);
+            vq[i] = ok ? *reinterpret_cast<const uint4*>(vin + row * kD + 8 * cc) : make_uint4(0, 0, 0, 0);
+        }
+        // key dimension k = tid: cumulative decay down the chunk
         const int k = tid;
         float* Gs = reinterpret_cast<float*>(sm + PrepSmem::kG);  // column k is this thread's
         float G = 0.f;
@@ -130,32 +141,28 @@ __global__ void __launch_bounds__(128, 1)
                 Gs[(t16 + u) * kD + k] = G;
             }
         }
-        const int kb = k >> 6, kc = k & 63;
-#pragma unroll 1
-        for (int t8 = 0; t8 < kC; t8 += 16) {
-            // sixteen steps' key and value elements in flight, then their tiles
-            __nv_bfloat16 kk[16], vv[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int t = t8 + u;
-                const size_t row = ((size_t)b * a.T + t0 + t) * a.Hkv + hk;
-                const bool ok = (vw >> t) & 1;
-                kk[u] = ok ? kin[row * kD + k] : __float2bfloat16_rn(0.f);
-                vv[u] = ok ? vin[row * kD + k] : __float2bfloat16_rn(0.f);  // value v = tid, exact
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int t = t8 + u;
-                const float x = __bfloat162float(kk[u]) * __expf(G - Gs[t * kD + k]);
-                const __nv_bfloat16 h = __float2bfloat16_rn(x);
-                const uint32_t off = kb * 8192 + swe(t, kc);
-                *reinterpret_cast<__nv_bfloat16*>(Kh + off) = h;
-                *reinterpret_cast<__nv_bfloat16*>(Kh + 16384 + off) = __float2bfloat16_rn(x - __bfloat162float(h));
-                *reinterpret_cast<__nv_bfloat16*>(Vt + off) = vv[u];
-            }
-        }
         // the chunk's transition is diagonal: gamma[k] = e^{G_C[k]}, fp32
         reinterpret_cast<float*>(wsc + Ws::kG)[k] = __expf(G);
+        __syncthreads();  // every column of G (G_C in its last row)
+        // Khat[l][k] = k_l[k] e^{G_C[k] - G_l[k]} (hi, lo) and V into the (rows l) tiles
+#pragma unroll
+        for (int i = 0; i < kIt; ++i) {
+            const int e = tid + 128 * i, l = e >> 4, cc = e & 15, k0 = 8 * cc;
+            float f[8], gl[8], gc[8];
+            const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(&kq[i]);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) f[x] = __bfloat162float(kp[x]);
+            load_g8(Gs + l * kD + k0, gl);
+            load_g8(Gs + (kC - 1) * kD + k0, gc);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) f[x] *= __expf(gc[x] - gl[x]);
+            uint4 hi, lo;
+            split8(f, hi, lo);
+            const uint32_t off = (cc >> 3) * 8192 + swc(l, cc & 7);
+            st16(Kh + off, hi);
+            st16(Kh + 16384 + off, lo);
+            st16(Vt + off, vq[i]);  // values exact
+        }
     }
     fence_proxy_async();
     tc_fence_before();
