@@ -66,8 +66,21 @@ __device__ __forceinline__ void load_g8(const float* p, float (&g)[8]) {
     g[0] = a.x, g[1] = a.y, g[2] = a.z, g[3] = a.w, g[4] = b.x, g[5] = b.y, g[6] = b.z, g[7] = b.w;
 }
 
-__device__ __forceinline__ float load_g(const Args& a, int b, int hk, int t, int k) {
-    return fmaxf(__bfloat162float(a.decay[(((size_t)b * a.T + t) * a.Hkv + hk) * kD + k]), kMinLogDecay);
+// The log decays of a chunk's steps, loaded as 16-byte chunks (chunk i of
+// thread `th`: step e / 16, key dimensions 8 (e % 16) .. + 7, e = th + nthr i;
+// zero for masked-out steps and steps past T), floored at kMinLogDecay into G[t][k].
+template <int kN>
+__device__ __forceinline__ void store_decays(float* Gs, const uint4 (&dq)[kN], int th, int nthr) {
+#pragma unroll
+    for (int i = 0; i < kN; ++i) {
+        const int e = th + nthr * i, l = e >> 4, k0 = 8 * (e & 15);
+        const __nv_bfloat16* p = reinterpret_cast<const __nv_bfloat16*>(&dq[i]);
+        float g[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) g[x] = fmaxf(__bfloat162float(p[x]), kMinLogDecay);
+        *reinterpret_cast<float4*>(Gs + l * kD + k0) = make_float4(g[0], g[1], g[2], g[3]);
+        *reinterpret_cast<float4*>(Gs + l * kD + k0 + 4) = make_float4(g[4], g[5], g[6], g[7]);
+    }
 }
 
 // ------------------------------------------------------------------ prep
@@ -117,7 +130,7 @@ __global__ void __launch_bounds__(128, 1)
         // the chunk's keys and values as 16-byte chunks (row l, eight key or
         // value dimensions), all in flight while the decays load and sum
         constexpr int kIt = kC * (kD / 8) / 128;
-        uint4 kq[kIt], vq[kIt];
+        uint4 kq[kIt], vq[kIt], dq[kIt];
 #pragma unroll
         for (int i = 0; i < kIt; ++i) {
             const int e = tid + 128 * i, l = e >> 4, cc = e & 15;
@@ -125,21 +138,18 @@ __global__ void __launch_bounds__(128, 1)
             const bool ok = (vw >> l) & 1;
             kq[i] = ok ? *reinterpret_cast<const uint4*>(kin + row * kD + 8 * cc) : make_uint4(0, 0, 0, 0);
             vq[i] = ok ? *reinterpret_cast<const uint4*>(vin + row * kD + 8 * cc) : make_uint4(0, 0, 0, 0);
+            dq[i] = ok ? *reinterpret_cast<const uint4*>(a.decay + row * kD + 8 * cc) : make_uint4(0, 0, 0, 0);
         }
-        // key dimension k = tid: cumulative decay down the chunk
+        float* Gs = reinterpret_cast<float*>(sm + PrepSmem::kG);
+        store_decays(Gs, dq, tid, 128);
+        __syncthreads();
+        // key dimension k = tid: cumulative decay down the chunk, in place
         const int k = tid;
-        float* Gs = reinterpret_cast<float*>(sm + PrepSmem::kG);  // column k is this thread's
         float G = 0.f;
-#pragma unroll 1
-        for (int t16 = 0; t16 < kC; t16 += 32) {
-            float g[32];  // thirty-two steps' decays in flight, then their running sum
-#pragma unroll
-            for (int u = 0; u < 32; ++u) g[u] = ((vw >> (t16 + u)) & 1) ? load_g(a, b, hk, t0 + t16 + u, k) : 0.f;
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                G += g[u];
-                Gs[(t16 + u) * kD + k] = G;
-            }
+#pragma unroll 8
+        for (int t = 0; t < kC; ++t) {
+            G += Gs[t * kD + k];
+            Gs[t * kD + k] = G;
         }
         // the chunk's transition is diagonal: gamma[k] = e^{G_C[k]}, fp32
         reinterpret_cast<float*>(wsc + Ws::kG)[k] = __expf(G);
@@ -337,21 +347,26 @@ __global__ void __launch_bounds__(256, 1)
         }
         tmem_st_wait();
     } else {
-        // key dimension k: cumulative decay down the chunk into G[t][k]
+        // the chunk's log decays into G (warps 4-7), then the cumulative decay
+        // of key dimension k down the chunk, in place
         const int k = tid - 128;
+        uint4 dq[kC * (kD / 8) / 128];
+#pragma unroll
+        for (int i = 0; i < kC * (kD / 8) / 128; ++i) {
+            const int e = k + 128 * i, l = e >> 4, cc = e & 15;
+            const size_t row = ((size_t)b * a.T + t0 + l) * a.Hkv + hk;
+            dq[i] = ((vw >> l) & 1) ? *reinterpret_cast<const uint4*>(a.decay + row * kD + 8 * cc)
+                                    : make_uint4(0, 0, 0, 0);
+        }
+        store_decays(Gs, dq, k, 128);
+        named_bar_sync(1, 128);  // warps 4-7
         float G_ = 0.f, mn = 0.f, mx = 0.f;
-#pragma unroll 1
-        for (int t8 = 0; t8 < kC; t8 += 32) {
-            float g[32];  // thirty-two steps' decays in flight, then their running sum
-#pragma unroll
-            for (int u = 0; u < 32; ++u) g[u] = ((vw >> (t8 + u)) & 1) ? load_g(a, b, hk, t0 + t8 + u, k) : 0.f;
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                G_ += g[u];
-                Gs[(t8 + u) * kD + k] = G_;
-                mn = fminf(mn, G_);
-                mx = fmaxf(mx, G_);
-            }
+#pragma unroll 8
+        for (int t = 0; t < kC; ++t) {
+            G_ += Gs[t * kD + k];
+            Gs[t * kD + k] = G_;
+            mn = fminf(mn, G_);
+            mx = fmaxf(mx, G_);
         }
         fac = mn > -kFactorRange && mx < kFactorRange;
     }
